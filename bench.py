@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized self-speculative hot path on GB300.
+
+A step is one speculative round over the LLaMA-2-7B-shaped linears
+(32 layers x {q, k, v, o 4096x4096; gate, up 4096->11008; down 11008->4096}
++ lm_head 4096->32000), nested 4+4-bit weights, group 128, batch 1, k = 4:
+  4 draft passes   : every linear, base plane only, M = 1 (one persistent launch each)
+  1 verify pass    : every linear, both planes (8-bit target), M = k+1 = 5
+  acceptance       : greedy and sampled (T = 1) on the lm_head outputs, V = 32000
+Value = algorithmic HBM bytes of the round / device time (GB/s), whole job.
+Synthetic, seeded inputs; the packed weights (6.8 GB) exceed L2, so every
+pass streams from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "nested-quant draft GEMV / verify GEMM HBM GB/s (% of peak); accept rounds/s"
+WORKLOAD = "llama2-7b-linears-32L-g128-b1-k4"
+K_DRAFT = 4
+GROUP = 128
+V_LM = 32000
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (read-only queries)."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ model
+def linear_list():
+    from quantized_self_speculative_gb300 import synth
+    layer, lm, n_layers = synth.llama2_7b_linears()
+    shapes = []
+    for li in range(n_layers):
+        for name, n, k in layer:
+            shapes.append((f"L{li}.{name}", n, k))
+    shapes.append((lm[0], lm[1], lm[2]))
+    return shapes
+
+
+def draft_bytes(n, k, M, g=GROUP):
+    return n * k // 2 + 2 * n * k // g + M * k * 2 + M * n * 4
+
+
+def verify_bytes(n, k, M, g=GROUP):
+    return n * k + 2 * n * k // g + M * k * 2 + M * n * 4
+
+
+def accept_bytes(B, k, V, sampled):
+    return B * ((2 * k + 1) if sampled else (k + 1)) * V * 4 + B * k * 4 + B * (k + 2) * 4
+
+
+class Round:
+    """Device state of one speculative round (weights resident in HBM)."""
+
+    def __init__(self, device, seed=0):
+        import torch
+        from quantized_self_speculative_gb300 import nq
+        self.torch, self.nq = torch, nq
+        self.dev = device
+        self.shapes = linear_list()
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed)
+        self.layers = []
+        for _, n, k in self.shapes:
+            w = torch.randn((n, k), generator=gen, device=device, dtype=torch.float32).mul_(0.02)
+            self.layers.append(nq.pack_weights(w, nq.FMT_NESTED44, GROUP))
+            del w
+        torch.cuda.synchronize()
+        # activations: one slab per round (q/k/v share an input, gate/up share one)
+        M_v = K_DRAFT + 1
+        specs = []   # (pass, layer index, M, k)
+        for p in range(K_DRAFT):
+            specs += [(p, i, 1, k) for i, (_, n, k) in enumerate(self.shapes)]
+        specs += [(K_DRAFT, i, M_v, k) for i, (_, n, k) in enumerate(self.shapes)]
+        offsets, total, cache = {}, 0, {}
+        for p, i, M, k in specs:
+            name = self.shapes[i][0]
+            key = (p, name.split(".")[0], "qkv" if name.endswith((".q", ".k", ".v")) else
+                   "gu" if name.endswith((".gate", ".up")) else name)
+            if key not in cache:
+                cache[key] = total
+                total += M * k
+            offsets[(p, i)] = cache[key]
+        self.x_host = torch.empty(total, dtype=torch.bfloat16).pin_memory()
+        self.x_host.copy_(torch.randn(total, generator=torch.Generator().manual_seed(seed + 1)).to(torch.bfloat16))
+        self.x_dev = self.x_host.to(device)
+        self.h2d_bytes = total * 2
+        self.dl = torch.empty((1, K_DRAFT, V_LM), dtype=torch.float32, device=device)
+        self.tl = torch.empty((1, K_DRAFT + 1, V_LM), dtype=torch.float32, device=device)
+        self.batches = []
+        for p in range(K_DRAFT + 1):
+            M = 1 if p < K_DRAFT else M_v
+            xs, ys = [], []
+            for i, (name, n, k) in enumerate(self.shapes):
+                o = offsets[(p, i)]
+                xs.append(self.x_dev[o:o + M * k].view(M, k))
+                if name == "lm_head":
+                    ys.append(self.dl[0, p:p + 1] if p < K_DRAFT else self.tl[0])
+                else:
+                    ys.append(torch.empty((M, n), dtype=torch.float32, device=device))
+            self.batches.append(nq.LinearBatch(p == K_DRAFT, self.layers, xs, ys))
+        g = np.random.default_rng(seed + 2)
+        self.draft = torch.from_numpy(g.integers(0, V_LM, size=(1, K_DRAFT), dtype=np.int32)).to(device)
+        self.seeds = torch.from_numpy(np.array([seed + 3], dtype=np.int64)).to(device)
+        self.ws_g = nq.accept_workspace(1, K_DRAFT, V_LM, device)
+        self.ws_s = nq.accept_workspace(1, K_DRAFT, V_LM, device)
+        self.out_g = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=device)
+        self.cnt_g = torch.empty(1, dtype=torch.int32, device=device)
+        self.out_s = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=device)
+        self.cnt_s = torch.empty(1, dtype=torch.int32, device=device)
+        self.res_host = torch.empty(2 * (K_DRAFT + 2), dtype=torch.int32).pin_memory()
+        self.round_idx = 0
+        self.bytes_draft_pass = sum(draft_bytes(n, k, 1) for _, n, k in self.shapes)
+        self.bytes_verify = sum(verify_bytes(n, k, M_v) for _, n, k in self.shapes)
+        self.bytes_accept = accept_bytes(1, K_DRAFT, V_LM, False) + accept_bytes(1, K_DRAFT, V_LM, True)
+        self.bytes_round = K_DRAFT * self.bytes_draft_pass + self.bytes_verify + self.bytes_accept
+        self.launches_per_round = K_DRAFT + 1 + 2
+
+    def run(self, events=None):
+        nq = self.nq
+        for p in range(K_DRAFT + 1):
+            if events is not None:
+                events[p].record()
+            self.batches[p]()
+        if events is not None:
+            events[K_DRAFT + 1].record()
+        nq.accept_greedy(self.draft, self.tl, ws=self.ws_g, out_tok=self.out_g, out_cnt=self.cnt_g)
+        nq.accept_sample(self.draft, self.dl, self.tl, 1.0, self.seeds, self.round_idx, ws=self.ws_s,
+                         out_tok=self.out_s, out_cnt=self.cnt_s)
+        if events is not None:
+            events[K_DRAFT + 2].record()
+        self.round_idx += 1
+
+    def run_e2e(self):
+        """The same round through the public API with host buffers: the round's
+        activations come from pinned host memory; the emitted tokens return."""
+        torch = self.torch
+        self.x_dev.copy_(self.x_host, non_blocking=True)
+        self.run()
+        self.res_host[0:K_DRAFT + 1].copy_(self.out_g[0], non_blocking=True)
+        self.res_host[K_DRAFT + 1:K_DRAFT + 2].copy_(self.cnt_g, non_blocking=True)
+        self.res_host[K_DRAFT + 2:2 * K_DRAFT + 3].copy_(self.out_s[0], non_blocking=True)
+        self.res_host[2 * K_DRAFT + 3:2 * K_DRAFT + 4].copy_(self.cnt_s, non_blocking=True)
+        return self.res_host
+
+    @property
+    def d2h_bytes(self):
+        return 2 * (K_DRAFT + 2) * 4
+
+
+# ------------------------------------------------------------------ acceptance at the sweep shape
+def accept_sweep(device, iters=20):
+    """Acceptance kernels alone at B = 64, V = 152064 (fp32 logits ~ N(0, 3))."""
+    import torch
+    from quantized_self_speculative_gb300 import nq
+    out = {}
+    B, V = 64, 152064
+    gen = torch.Generator(device=device)
+    gen.manual_seed(5)
+    for k in (4, 8):
+        tl = torch.randn((B, k + 1, V), generator=gen, device=device).mul_(3.0)
+        dl = (tl[:, :k] + 0.3 * torch.randn((B, k, V), generator=gen, device=device)).contiguous()
+        d = dl.argmax(-1).to(torch.int32)
+        seeds = torch.arange(B, dtype=torch.int64, device=device)
+        ws = nq.accept_workspace(B, k, V, device)
+        res = {}
+        for kind in ("greedy", "sample"):
+            def call(r):
+                if kind == "greedy":
+                    nq.accept_greedy(d, tl, ws=ws)
+                else:
+                    nq.accept_sample(d, dl, tl, 1.0, seeds, r, ws=ws)
+            for r in range(3):
+                call(r)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for r in range(iters):
+                call(r)
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / iters
+            byts = accept_bytes(B, k, V, kind == "sample")
+            res[kind] = {"us": round(us, 2), "rounds_per_s": round(B / (us * 1e-6), 1),
+                         "gbs": round(byts / (us * 1e-6) / 1e9, 1)}
+        out[f"k{k}"] = res
+        del tl, dl
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample_step(state):
+    """A bounded sample of the round on the CPU oracle: draft (M=1) and verify
+    (M=5) of the q, gate and down linears, plus greedy and sampled acceptance
+    at V = 32000.  Returns algorithmic bytes processed."""
+    import oracle as O
+    from quantized_self_speculative_gb300 import synth
+    if "packed" not in state:
+        packed = []
+        for i, (n, k) in enumerate([(4096, 4096), (11008, 4096), (4096, 11008)]):
+            w = synth.weights(9000 + i, n, k)
+            packed.append((n, k) + O.pack_nested(w, GROUP))
+        state["packed"] = packed
+        state["x1"] = {k: synth.activations_bf16(9100 + k, 1, k) for k in (4096, 11008)}
+        state["x5"] = {k: synth.activations_bf16(9200 + k, 5, k) for k in (4096, 11008)}
+        tl = synth.target_logits(9300, 1, K_DRAFT, V_LM, 2.0)
+        dl = synth.draft_logits_from(tl, 9301, 0.5)
+        state["acc"] = (tl, dl, synth.draft_tokens_greedy(dl), synth.draft_tokens_sampled(dl, 9302))
+    byts = 0
+    for n, k, base, resid, scales in state["packed"]:
+        O.linear(O.FMT_NESTED44, n, k, GROUP, base, resid, scales, state["x1"][k], False)
+        O.linear(O.FMT_NESTED44, n, k, GROUP, base, resid, scales, state["x5"][k], True)
+        byts += draft_bytes(n, k, 1) + verify_bytes(n, k, 5)
+    tl, dl, dg, ds = state["acc"]
+    O.accept_greedy(dg, tl)
+    O.accept_sample(ds, dl, tl, 1.0, synth.seeds_for(0, 1), 0)
+    byts += accept_bytes(1, K_DRAFT, V_LM, False) + accept_bytes(1, K_DRAFT, V_LM, True)
+    return byts
+
+
+def cpu_baseline(min_seconds=10.0):
+    state = {}
+    oracle_sample_step(state)          # packs (untimed) and warms up
+    t0 = time.perf_counter()
+    byts, steps = 0, 0
+    while time.perf_counter() - t0 < min_seconds:
+        byts += oracle_sample_step(state)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} x (draft M=1 + verify M=5 of the 4096x4096, 11008x4096, 4096x11008 linears, "
+                      f"greedy + sampled acceptance B=1 k=4 V=32000), single-threaded C, fp64 accumulation",
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+# ------------------------------------------------------------------ arms
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    state = {}
+    oracle_sample_step(state)
+    for _ in range(args.warmup):
+        oracle_sample_step(state)
+    t0 = time.perf_counter()
+    byts = sum(oracle_sample_step(state) for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = byts / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "oracle sample of the round"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step: draft M=1 + verify M=5 of three LLaMA-2-7B linear shapes "
+                                       "+ greedy and sampled acceptance (B=1, k=4, V=32000)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from quantized_self_speculative_gb300 import build
+    build.build()
+    R = Round(device, seed=17 + rank)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        R.run()
+    barrier()
+    # ---- timed region: K rounds, per-launch events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(K_DRAFT + 3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = cvd.split(",")[local].strip() if cvd else str(local)
+    with ClockSampler(smi_index) as clk:
+        barrier()
+        start.record()
+        for s in range(args.steps):
+            R.run(ev[s])
+        stop.record()
+        barrier()
+    ms = start.elapsed_time(stop)
+    draft_ms = [ev[s][p].elapsed_time(ev[s][p + 1]) for s in range(args.steps) for p in range(K_DRAFT)]
+    verify_ms = [ev[s][K_DRAFT].elapsed_time(ev[s][K_DRAFT + 1]) for s in range(args.steps)]
+    accept_ms = [ev[s][K_DRAFT + 1].elapsed_time(ev[s][K_DRAFT + 2]) for s in range(args.steps)]
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+    # ---- end to end: host activations in, emitted tokens out
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        R.run_e2e()
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    value = R.bytes_round * args.steps * world / (t_max * 1e-3) / 1e9
+    d_avg = statistics.mean(draft_ms)
+    v_avg = statistics.mean(verify_ms)
+    draft_gbs = R.bytes_draft_pass / (d_avg * 1e-3) / 1e9
+    verify_gbs = R.bytes_verify / (v_avg * 1e-3) / 1e9
+    extras = {}
+    if not args.no_extras:
+        extras["accept_sweep_B64_V152064"] = accept_sweep(device)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
+        "config": {"workload": WORKLOAD, "layers": 32, "group": GROUP, "batch": 1, "k": K_DRAFT,
+                   "draft_M": 1, "verify_M": K_DRAFT + 1, "vocab": V_LM,
+                   "l2": "inputs larger than L2 (6.8 GB packed weights streamed per round)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": round(100 * value / world / hbm, 1),
+        "rounds_per_s": round(args.steps * world / (t_max * 1e-3), 2),
+        "draft_pass": {"us": round(d_avg * 1e3, 1), "gbs": round(draft_gbs, 1), "bytes": R.bytes_draft_pass},
+        "verify_pass": {"us": round(v_avg * 1e3, 1), "gbs": round(verify_gbs, 1), "bytes": R.bytes_verify},
+        "accept_round_us": round(statistics.mean(accept_ms) * 1e3, 2),
+        "roofline": {"bound": "hbm", "kernel": "draft GEMV (one persistent launch per model pass, M=1)",
+                     "achieved": round(draft_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(draft_gbs / hbm, 4), "peak_kind": peak_kind, "traffic": None,
+                     "verify_achieved": round(verify_gbs, 1), "verify_frac": round(verify_gbs / hbm, 4)},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(R.bytes_round * args.steps * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": R.h2d_bytes, "d2h_bytes_per_step": R.d2h_bytes},
+        "gpu_launches": R.launches_per_round * args.steps,
+    }
+    line.update(extras)
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * nq.h -- C ABI of libnq.so: the weight-streaming linears and the acceptance
+ * step of quantized self-speculative decoding, as hand-written CUDA for
+ * sm_103a (GB300).
+ *
+ * Method sources (page title; section / figure / table / equation):
+ *   "BitNest: Bit-Nested Speculative Decoding for Memory-Efficient LLM
+ *    Inference Acceleration" -- Fig. 2 (a b-bit base plus an r-bit
+ *    refinement of the remaining error; drafting reads only the base,
+ *    verification reads both planes to recover the (b+r)-bit target) and
+ *    Fig. 3 (dual-plane storage: two independent 4-bit streams of N/2 bytes
+ *    for N weights; the target recovers the full 8-bit representation).
+ *   "SpecQuant -- Speculative Decoding with Multi-Parent Quantization for
+ *    Adaptive LLM Inference" -- Sec. III.A (Q4 = f(W16,4) INT4, Q8 =
+ *    f(W16,8) FP8, Q16 = W16, all from one FP16 base) and Sec. III.D.3-4
+ *    (parent verification; token acceptance or correction).
+ *   "How Speculative Decoding Speeds Up Inference" -- "Drafting and checking
+ *    tokens" (draft k tokens, check all k positions in one target pass, keep
+ *    the matching prefix, the target's token replaces the first mismatch,
+ *    1..k+1 tokens per pass), Table 1 (k = 4 worked round), "The same output
+ *    as the large model alone" (greedy equivalence; speculative sampling of
+ *    Leviathan et al. / Chen et al.), Eq. (1).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is caller-owned DEVICE memory unless stated
+ *     otherwise; the library allocates nothing and keeps no per-call state.
+ *   - Every call is asynchronous on `stream`; outputs are valid once the
+ *     stream reaches the call.  Arguments are validated on the host before
+ *     any launch; a rejected call launches nothing and returns a status.
+ *   - Device pointers must be 16-byte aligned (NQ_ERR_ALIGN otherwise).
+ *   - Data-dependent faults that only the device can see (non-finite logits,
+ *     out-of-range draft ids) set bits in a sticky per-device status word,
+ *     read (and cleared) with nq_get_device_status().
+ *   - Activations are bfloat16, passed as their uint16_t bit patterns.
+ *   - Results are deterministic: the same inputs give the same bits, and a
+ *     linear's output row for one activation row does not depend on M or on
+ *     the other rows of the batch (batch invariance).
+ */
+#ifndef NQ_H
+#define NQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(NQ_BUILDING) && defined(__GNUC__)
+#define NQ_API __attribute__((visibility("default")))
+#else
+#define NQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NQ_OK = 0,
+    NQ_ERR_ARG = 1,        /* null pointer, unknown format, bad k / M / temperature */
+    NQ_ERR_SHAPE = 2,      /* k_in % group, k_in % 64, group not in {64,128}, sizes too large */
+    NQ_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned */
+    NQ_ERR_CUDA = 4,       /* a CUDA runtime call failed (launch error, bad device) */
+    NQ_ERR_NONFINITE = 5,  /* reported by nq_get_device_status(): non-finite logits */
+    NQ_ERR_TIMEOUT = 6,    /* reserved: a bounded device wait gave up */
+    NQ_ERR_WORKSPACE = 7,  /* workspace smaller than spec_accept_workspace_bytes() */
+    NQ_ERR_TOKEN = 8       /* reported by nq_get_device_status(): draft id outside [0, V) */
+} nq_status;
+
+/* Bits of the sticky device status word. */
+#define NQ_DEV_NONFINITE 0x1u
+#define NQ_DEV_BAD_TOKEN 0x2u
+#define NQ_DEV_TIMEOUT   0x4u
+
+/*
+ * Weight formats (SpecQuant Sec. III.A tiers; BitNest Fig. 3 planes).
+ *   NESTED44    base = 4-bit codes [n_out][k_in/2], resid = 4-bit refinement
+ *               codes [n_out][k_in/2], scales = fp16 [n_out][k_in/group].
+ *               Two's-complement nibbles, element 2j in the low nibble of
+ *               byte j.  Draft value s*q4; target value (s/16)*(16*q4 + r).
+ *   INT4        base + scales exactly as NESTED44, no refinement plane.
+ *   FP8E4M3_ROW base = E4M3FN codes [n_out][k_in], scales = fp32 [n_out]
+ *               (value = scale[n] * e4m3), resid unused, group ignored.
+ *   FP16        base = fp16 weights [n_out][k_in], resid/scales unused.
+ * Valid pairs: draft (nq_draft_gemv*) takes NESTED44 (base plane only) and
+ * INT4; verify (nq_verify_gemm*) takes NESTED44 (both planes), FP8E4M3_ROW
+ * and FP16.  Any other pair returns NQ_ERR_ARG.
+ */
+typedef enum {
+    NQ_FMT_NESTED44 = 0,
+    NQ_FMT_INT4 = 1,
+    NQ_FMT_FP8E4M3_ROW = 2,
+    NQ_FMT_FP16 = 3
+} nq_format;
+
+/* One packed linear layer, W [n_out][k_in] (y = x W^T).  The struct itself is
+ * host memory; the three buffers are device memory owned by the caller. */
+typedef struct {
+    int32_t n_out;
+    int32_t k_in;     /* multiple of 64; for NESTED44/INT4 also of group */
+    int32_t group;    /* 64 or 128 (NESTED44 / INT4); ignored otherwise */
+    int32_t format;   /* nq_format */
+    void *base;
+    void *resid;
+    void *scales;
+} nq_weights;
+
+/* Byte sizes of the three buffers of a packed layer (host-only; no CUDA).
+ * Any output pointer may be NULL.  NQ_ERR_SHAPE / NQ_ERR_ARG on bad shapes. */
+NQ_API nq_status nq_packed_bytes(int n_out, int k_in, int group, int format,
+                          size_t *base_bytes, size_t *resid_bytes, size_t *scale_bytes);
+
+/*
+ * Quantise and pack fp32 weights w [n_out][k_in] (device, row-major) into the
+ * caller-allocated buffers of `out` (sizes from nq_packed_bytes()).
+ * NESTED44 / INT4 (BitNest Fig. 2): per (row, group of `group` inputs)
+ * s = fp16(absmax/7); q4 = clamp(rint(w/s), -8, 7); r = clamp(rint(16 (w/s -
+ * q4)), -8, 7); a group with s == 0 packs to zeros.  FP8E4M3_ROW: s_n =
+ * absmax_row/448, code = E4M3FN(w/s_n), round to nearest even, saturating.
+ * FP16: round to nearest even.  Weights must be finite (non-finite input
+ * gives unspecified codes).  Offline step, not part of a decoding round.
+ */
+NQ_API nq_status nq_pack_weights(const float *w, const nq_weights *out, cudaStream_t stream);
+
+/*
+ * Draft pass linear (BitNest Fig. 2: drafting reads only the base plane):
+ *   y[m][n] = sum_g s[n][g] * sum_{k in g} q4[n][k] * x[m][k]
+ * x: bf16 bits [M][k_in]; y: fp32 [M][n_out]; 1 <= M <= 4096 (the kernel
+ * streams the weights once per 16 activation rows).  Formats: NESTED44, INT4.
+ */
+NQ_API nq_status nq_draft_gemv(const nq_weights *w, const uint16_t *x, int M, float *y, cudaStream_t stream);
+
+/*
+ * Verify pass linear over the k+1 candidate positions (BitNest Fig. 2 and
+ * Fig. 3: both planes rebuild the 8-bit target; SpecQuant Sec. III.D.3):
+ *   NESTED44:    y[m][n] = sum_g (s[n][g]/16) sum_{k in g} (16 q4 + r)[n][k] x[m][k]
+ *   FP8E4M3_ROW: y[m][n] = s[n] sum_k e4m3[n][k] x[m][k]
+ *   FP16:        y[m][n] = sum_k w16[n][k] x[m][k]
+ * Same layouts and limits as nq_draft_gemv.  The FP8 and FP16 tiers multiply
+ * in fp16: activations are rounded bf16 -> fp16 (exact for 2^-14 <= |x| <=
+ * 65504), products accumulate in fp32.
+ */
+NQ_API nq_status nq_verify_gemm(const nq_weights *w, const uint16_t *x, int M, float *y, cudaStream_t stream);
+
+/*
+ * Many independent linears in one persistent launch (e.g. every linear of a
+ * model pass), all at the same M.  w, x and y are HOST arrays of `count`
+ * entries (x[i], y[i] device pointers, layouts as for the single calls).
+ * Equivalent to `count` single calls in order; bit-identical results.
+ * All layers must share the format class of the call (draft or verify).
+ */
+NQ_API nq_status nq_draft_gemv_batch(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                              float *const *y, cudaStream_t stream);
+NQ_API nq_status nq_verify_gemm_batch(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                               float *const *y, cudaStream_t stream);
+
+/*
+ * Device workspace for the acceptance calls, in bytes (host-only).  The
+ * workspace must be zero-filled once before its first use; every call leaves
+ * it ready for the next one.  Calls that share a workspace must not overlap
+ * on the GPU (use one stream, or one workspace per stream).
+ * Limits: 1 <= B <= 65535, 1 <= k <= 16, 1 <= V <= 524288.  Returns 0 on bad sizes.
+ */
+NQ_API size_t spec_accept_workspace_bytes(int B, int k, int V);
+
+/*
+ * Greedy acceptance ("Drafting and checking tokens"; Table 1; "The same
+ * output as the large model alone"):
+ *   t_j = argmax_x tgt_logits[b][j][x] (lowest index on ties), j = 0..k;
+ *   n   = first j < k with draft[b][j] != t_j, else k;
+ *   out_tok[b] = draft[b][0..n-1], t_n, then -1 pads;  out_cnt[b] = n + 1.
+ * draft: int32 [B][k]; tgt_logits: fp32 [B][k+1][V]; out_tok: int32 [B][k+1];
+ * out_cnt: int32 [B].  Non-finite logits set NQ_DEV_NONFINITE and out-of-range
+ * draft ids NQ_DEV_BAD_TOKEN (that row's output is then unspecified).
+ */
+NQ_API nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
+                             int32_t *out_tok, int32_t *out_cnt, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/*
+ * Speculative sampling (Leviathan et al.; Chen et al.; "The same output as
+ * the large model alone"), p = softmax(tgt/T), q = softmax(draft_logits/T):
+ *   for j = 0..k-1: accept draft[b][j] iff u_j < p_j(d_j) / q_j(d_j);
+ *   at the first rejection j draw from normalise(max(0, p_j - q_j)) (from p_j
+ *   if that is all zero) and stop; if all k are accepted draw a bonus token
+ *   from p_k.  Emits 1..k+1 tokens: out_tok / out_cnt as for greedy.
+ * draft_logits: fp32 [B][k][V]; tgt_logits: fp32 [B][k+1][V]; temperature > 0;
+ * seeds: uint64 [B] (device); round: caller's round counter.  Uniforms come
+ * from Philox4x32-10 with key = seeds[b], counter = (j, purpose, round) --
+ * purpose 0 accept test, 1 resample, 2 bonus -- so a (seed, round) pair
+ * replays exactly.  The fp32 arithmetic follows a fixed recipe (own base-2
+ * exponential, power-of-two max/sum trees over 16-entry leaves, sum-tree
+ * sampling) so that every decision is reproducible bit for bit.
+ */
+NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
+                             int B, int k, int V, float temperature, const uint64_t *seeds,
+                             uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+NQ_API const char *nq_status_string(int status);
+
+/* Read, then clear, the sticky device status word of the current device
+ * (NQ_DEV_* bits), ordered after all work already queued on `stream`
+ * (blocks the host until then). */
+NQ_API nq_status nq_get_device_status(cudaStream_t stream, uint32_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NQ_H */

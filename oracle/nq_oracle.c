@@ -386,6 +386,8 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  *   leaf s = serial fp32 sum, in index order, of e2(t(x))
  *   merge  (m1,s1),(m2,s2): the larger m survives; s = fma(s_small,
  *            e2(m_small - m_large), s_large); a (-inf, 0) pad is the identity
+ *   valid  = every logit finite and every leaf's mz finite (a logit whose
+ *            scaled value underflows gets probability 0)
  *   tree   = leaves padded to a power of two with (-inf, 0), merged pairwise,
  *            left operand first, level by level -> (M, S)
  *   p(x)   = RN(e2(t(x)) * F_leaf), F_leaf = RN(e2(mz_leaf - M) * RN(1/S))
@@ -480,9 +482,10 @@ static ms_t ms_tree(const ms_t *leaf, int L)
 int orc_softmax_canonical(const float *l, int V, float T, float *p)
 {
     float c = orc_temper_coef(T);
-    for (int x = 0; x < V; x++) if (!isfinite(l[x]) || !isfinite(l[x] * c)) return -1;
+    for (int x = 0; x < V; x++) if (!isfinite(l[x])) return -1;
     ms_t *leaf = malloc(sizeof(ms_t) * n_leaves(V));
     int L = leaf_stats(l, V, c, leaf);
+    for (int i = 0; i < L; i++) if (!isfinite(leaf[i].m)) { free(leaf); return -1; }
     ms_t root = ms_tree(leaf, L);
     float inv_s = 1.0f / root.s;
     for (int i = 0; i < L; i++) {

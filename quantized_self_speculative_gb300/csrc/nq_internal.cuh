@@ -1,0 +1,149 @@
+// nq_internal.cuh -- device helpers and host plumbing shared by the libnq
+// translation units.  Product code only (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/nq.h"
+
+namespace nq {
+
+// ---------------------------------------------------------------- host side
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of the sticky status word of the current device (set up once
+// per device with cudaGetSymbolAddress); nullptr if that failed.
+unsigned int *device_status_ptr();
+
+// Multiprocessor count of the current device (cached).
+int sm_count();
+
+inline nq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA; }
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ void set_status(unsigned int *status, unsigned int bits)
+{
+    if (status) atomicOr(status, bits);
+}
+
+// Streamed 16/8/4-byte global loads that bypass L1 allocation (read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// D += A(16x16) * B(16x8), bf16 inputs, fp32 accumulators (legacy warp MMA).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two 4-bit two's-complement codes -> bf16x2 holding (136 + code) each.
+// Nibble i of w goes to the low half, nibble i+4 to the high half.  The
+// constant 0x4300 is bf16 128.0 (unit spacing); XOR 8 maps the signed nibble
+// to offset binary, so the value is 128 + (nib ^ 8) = 136 + code, exactly.
+template <int I>
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w)
+{
+    return ((w >> (4 * I)) & 0x000F000Fu) ^ 0x43084308u;
+}
+
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2 (bytes 0,1 and 2,3), exact.
+// Byte 2i goes to the low half of the result, byte 2i+1 to the high half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+// ---------------------------------------------------------------- canonical
+// fp32 recipe of the sampled acceptance (see spec_accept_sample in nq.h):
+// base-2 exponential of t <= 0.5: 0 below -125, else P(f) 2^n with n =
+// rint(t), f = t - n (exact) and P the degree-6 Taylor polynomial of 2^f,
+// coefficients ln2^i / i! rounded to fp32, Horner with fused multiply-add.
+__device__ __forceinline__ float exp2_canon(float t)
+{
+    const float c0 = 1.0f, c1 = 0.693147180559945309417f, c2 = 0.240226506959100712333f,
+                c3 = 0.0555041086648215799531f, c4 = 0.00961812910762847716197f,
+                c5 = 0.00133335581464284434234f, c6 = 0.000154035303933816099545f;
+    float tc = fmaxf(t, -125.0f);
+    float n = rintf(tc);
+    float f = __fsub_rn(tc, n);
+    float p = __fmaf_rn(c6, f, c5);
+    p = __fmaf_rn(p, f, c4);
+    p = __fmaf_rn(p, f, c3);
+    p = __fmaf_rn(p, f, c2);
+    p = __fmaf_rn(p, f, c1);
+    p = __fmaf_rn(p, f, c0);
+    float r = __int_as_float(__float_as_int(p) + (static_cast<int>(n) << 23));
+    return t < -125.0f ? 0.0f : r;
+}
+
+struct MaxSum { float m, s; };
+
+// Merge two (max, sum) nodes; the larger max survives, the other sum is
+// rescaled by 2^(m_small - m_large); a (-inf, 0) pad is the identity.
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b)
+{
+    if (b.m == -INFINITY) return a;
+    if (a.m == -INFINITY) return b;
+    MaxSum r;
+    if (a.m >= b.m) { r.m = a.m; r.s = __fmaf_rn(b.s, exp2_canon(__fsub_rn(b.m, a.m)), a.s); }
+    else            { r.m = b.m; r.s = __fmaf_rn(a.s, exp2_canon(__fsub_rn(a.m, b.m)), b.s); }
+    return r;
+}
+
+// Philox4x32-10 (Salmon et al., SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Uniform in [0,1) for (row seed, position, purpose, round): word 0's top 24 bits.
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
+{
+    uint4 o = philox4x32_10(make_uint4(j, purpose, static_cast<uint32_t>(round), static_cast<uint32_t>(round >> 32)),
+                            make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
+    return __fmul_rn(__uint2float_rn(o.x >> 8), 5.9604644775390625e-08f);
+}
+
+}  // namespace nq

@@ -1,0 +1,245 @@
+"""Thin ctypes binding of libnq.so (include/nq.h).  Argument marshalling only:
+every step of the hot path runs in the library's CUDA kernels.  PyTorch
+provides device memory and the current stream.
+
+The library must have been built (``quantized_self_speculative_gb300.build``);
+there is no fallback: a missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnq.so")
+
+NQ_OK, NQ_ERR_ARG, NQ_ERR_SHAPE, NQ_ERR_ALIGN, NQ_ERR_CUDA = 0, 1, 2, 3, 4
+NQ_ERR_NONFINITE, NQ_ERR_TIMEOUT, NQ_ERR_WORKSPACE, NQ_ERR_TOKEN = 5, 6, 7, 8
+NQ_DEV_NONFINITE, NQ_DEV_BAD_TOKEN, NQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
+FMT_NESTED44, FMT_INT4, FMT_FP8E4M3_ROW, FMT_FP16 = 0, 1, 2, 3
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class nq_weights(C.Structure):
+    _fields_ = [("n_out", C.c_int32), ("k_in", C.c_int32), ("group", C.c_int32), ("format", C.c_int32),
+                ("base", C.c_void_p), ("resid", C.c_void_p), ("scales", C.c_void_p)]
+
+
+def lib():
+    """Load libnq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libnq.so is missing at {LIB_PATH}; build it with "
+                                   "`python -m quantized_self_speculative_gb300.build` (needs nvcc)")
+            L = C.CDLL(LIB_PATH)
+            vp, i32, sz, u64, f32 = C.c_void_p, C.c_int, C.c_size_t, C.c_uint64, C.c_float
+            W = C.POINTER(nq_weights)
+            L.nq_packed_bytes.argtypes = [i32, i32, i32, i32, C.POINTER(sz), C.POINTER(sz), C.POINTER(sz)]
+            L.nq_pack_weights.argtypes = [vp, W, vp]
+            for name in ("nq_draft_gemv", "nq_verify_gemm"):
+                getattr(L, name).argtypes = [W, vp, i32, vp, vp]
+            for name in ("nq_draft_gemv_batch", "nq_verify_gemm_batch"):
+                getattr(L, name).argtypes = [i32, W, C.POINTER(vp), i32, C.POINTER(vp), vp]
+            L.spec_accept_workspace_bytes.argtypes = [i32, i32, i32]
+            L.spec_accept_workspace_bytes.restype = sz
+            L.spec_accept_greedy.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+            L.spec_accept_sample.argtypes = [vp, vp, vp, i32, i32, i32, f32, vp, u64, vp, vp, vp, sz, vp]
+            L.nq_status_string.argtypes = [i32]
+            L.nq_status_string.restype = C.c_char_p
+            L.nq_get_device_status.argtypes = [vp, C.POINTER(C.c_uint32)]
+            for name in ("nq_packed_bytes", "nq_pack_weights", "nq_draft_gemv", "nq_verify_gemm",
+                         "nq_draft_gemv_batch", "nq_verify_gemm_batch", "spec_accept_greedy",
+                         "spec_accept_sample", "nq_get_device_status"):
+                getattr(L, name).restype = i32
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nq_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != NQ_OK:
+        raise NQError(status, what)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, what: str) -> int:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor of {dtype}")
+    return t.data_ptr()
+
+
+# ---------------------------------------------------------------- weights
+def packed_bytes(n_out: int, k_in: int, group: int, fmt: int):
+    b, r, s = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    _check(lib().nq_packed_bytes(n_out, k_in, group, fmt, C.byref(b), C.byref(r), C.byref(s)), "nq_packed_bytes")
+    return b.value, r.value, s.value
+
+
+@dataclass
+class PackedLinear:
+    """A packed linear layer W [n_out][k_in]; buffers are uint8 device tensors."""
+    n_out: int
+    k_in: int
+    group: int
+    fmt: int
+    base: torch.Tensor
+    resid: Optional[torch.Tensor]
+    scales: Optional[torch.Tensor]
+
+    def struct(self) -> nq_weights:
+        return nq_weights(self.n_out, self.k_in, self.group, self.fmt, self.base.data_ptr(),
+                          None if self.resid is None else self.resid.data_ptr(),
+                          None if self.scales is None else self.scales.data_ptr())
+
+    def as_int4(self) -> "PackedLinear":
+        """The INT4 view of a NESTED44 layer (same base plane and scales)."""
+        return PackedLinear(self.n_out, self.k_in, self.group, FMT_INT4, self.base, None, self.scales)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.base, self.resid, self.scales) if t is not None)
+
+
+def alloc_packed(n_out: int, k_in: int, group: int, fmt: int, device=None) -> PackedLinear:
+    device = device or torch.device("cuda")
+    b, r, s = packed_bytes(n_out, k_in, group, fmt)
+    mk = lambda n: torch.empty(n, dtype=torch.uint8, device=device) if n else None
+    return PackedLinear(n_out, k_in, group, fmt, mk(b), mk(r), mk(s))
+
+
+def pack_weights(w: torch.Tensor, fmt: int = FMT_NESTED44, group: int = 128, stream=None) -> PackedLinear:
+    n, k = w.shape
+    out = alloc_packed(n, k, group, fmt, w.device)
+    st = out.struct()
+    _check(lib().nq_pack_weights(_dev(w, torch.float32, "w"), C.byref(st), _stream(stream)), "nq_pack_weights")
+    return out
+
+
+def pack_from_host(base, resid, scales, n_out, k_in, group, fmt, device=None) -> PackedLinear:
+    """Upload already-packed planes (numpy arrays) to the device."""
+    device = device or torch.device("cuda")
+    t = lambda a: None if a is None else torch.from_numpy(a.reshape(-1).view("uint8").copy()).to(device)
+    return PackedLinear(n_out, k_in, group, fmt, t(base), t(resid), t(scales))
+
+
+# ---------------------------------------------------------------- linears
+def _linear(fn: str, w: PackedLinear, x: torch.Tensor, y: Optional[torch.Tensor], stream) -> torch.Tensor:
+    M = x.shape[0]
+    if x.shape[-1] != w.k_in:
+        raise ValueError("x must be [M][k_in]")
+    if y is None:
+        y = torch.empty((M, w.n_out), dtype=torch.float32, device=x.device)
+    st = w.struct()
+    xp = _dev(x, torch.bfloat16, "x") if x.dtype == torch.bfloat16 else _dev(x, torch.int16, "x")
+    _check(getattr(lib(), fn)(C.byref(st), xp, M, _dev(y, torch.float32, "y"), _stream(stream)), fn)
+    return y
+
+
+def draft_gemv(w: PackedLinear, x: torch.Tensor, y=None, stream=None) -> torch.Tensor:
+    """Draft pass: base plane only.  x: bf16 [M][k_in] -> y fp32 [M][n_out]."""
+    return _linear("nq_draft_gemv", w, x, y, stream)
+
+
+def verify_gemm(w: PackedLinear, x: torch.Tensor, y=None, stream=None) -> torch.Tensor:
+    """Verify pass: both planes (8-bit target), or the FP8 / FP16 tiers."""
+    return _linear("nq_verify_gemm", w, x, y, stream)
+
+
+class LinearBatch:
+    """Prebuilt argument arrays for nq_{draft_gemv,verify_gemm}_batch: one
+    persistent launch over many independent linears at the same M."""
+
+    def __init__(self, verify: bool, layers: Sequence[PackedLinear], xs: Sequence[torch.Tensor],
+                 ys: Sequence[torch.Tensor]):
+        n = len(layers)
+        assert n == len(xs) == len(ys) and n > 0
+        self.fn = "nq_verify_gemm_batch" if verify else "nq_draft_gemv_batch"
+        self.M = xs[0].shape[0]
+        for L, x, y in zip(layers, xs, ys):
+            assert x.shape == (self.M, L.k_in) and y.shape == (self.M, L.n_out)
+            _dev(x, torch.bfloat16, "x")
+            _dev(y, torch.float32, "y")
+        self.count = n
+        self.w = (nq_weights * n)(*[L.struct() for L in layers])
+        self.x = (C.c_void_p * n)(*[x.data_ptr() for x in xs])
+        self.y = (C.c_void_p * n)(*[y.data_ptr() for y in ys])
+        self._keep = (list(layers), list(xs), list(ys))
+
+    def __call__(self, stream=None):
+        _check(getattr(lib(), self.fn)(self.count, self.w, self.x, self.M, self.y, _stream(stream)), self.fn)
+
+
+# ---------------------------------------------------------------- acceptance
+def workspace_bytes(B: int, k: int, V: int) -> int:
+    return lib().spec_accept_workspace_bytes(B, k, V)
+
+
+def accept_workspace(B: int, k: int, V: int, device=None) -> torch.Tensor:
+    """Zero-filled workspace (the calls leave it ready for reuse)."""
+    n = workspace_bytes(B, k, V)
+    if n == 0:
+        raise NQError(NQ_ERR_ARG, "spec_accept_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def accept_greedy(draft: torch.Tensor, tgt_logits: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                  out_tok=None, out_cnt=None, stream=None):
+    B, k = draft.shape
+    V = tgt_logits.shape[-1]
+    if tgt_logits.shape != (B, k + 1, V):
+        raise ValueError("tgt_logits must be [B][k+1][V]")
+    ws = ws if ws is not None else accept_workspace(B, k, V, draft.device)
+    out_tok = out_tok if out_tok is not None else torch.empty((B, k + 1), dtype=torch.int32, device=draft.device)
+    out_cnt = out_cnt if out_cnt is not None else torch.empty(B, dtype=torch.int32, device=draft.device)
+    _check(lib().spec_accept_greedy(_dev(draft, torch.int32, "draft"), _dev(tgt_logits, torch.float32, "tgt_logits"),
+                                    B, k, V, _dev(out_tok, torch.int32, "out_tok"), _dev(out_cnt, torch.int32, "out_cnt"),
+                                    _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "spec_accept_greedy")
+    return out_tok, out_cnt
+
+
+def accept_sample(draft: torch.Tensor, draft_logits: torch.Tensor, tgt_logits: torch.Tensor, temperature: float,
+                  seeds: torch.Tensor, round_: int, ws: Optional[torch.Tensor] = None, out_tok=None, out_cnt=None,
+                  stream=None):
+    B, k = draft.shape
+    V = tgt_logits.shape[-1]
+    if tgt_logits.shape != (B, k + 1, V) or draft_logits.shape != (B, k, V):
+        raise ValueError("draft_logits must be [B][k][V] and tgt_logits [B][k+1][V]")
+    ws = ws if ws is not None else accept_workspace(B, k, V, draft.device)
+    out_tok = out_tok if out_tok is not None else torch.empty((B, k + 1), dtype=torch.int32, device=draft.device)
+    out_cnt = out_cnt if out_cnt is not None else torch.empty(B, dtype=torch.int32, device=draft.device)
+    seeds_p = _dev(seeds, torch.int64, "seeds") if seeds.dtype == torch.int64 else _dev(seeds, torch.uint64, "seeds")
+    _check(lib().spec_accept_sample(_dev(draft, torch.int32, "draft"), _dev(draft_logits, torch.float32, "draft_logits"),
+                                    _dev(tgt_logits, torch.float32, "tgt_logits"), B, k, V, float(temperature),
+                                    seeds_p, int(round_) & (2**64 - 1), _dev(out_tok, torch.int32, "out_tok"),
+                                    _dev(out_cnt, torch.int32, "out_cnt"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+                                    _stream(stream)), "spec_accept_sample")
+    return out_tok, out_cnt
+
+
+def device_status(stream=None) -> int:
+    """Read and clear the sticky device status word (NQ_DEV_* bits)."""
+    v = C.c_uint32()
+    _check(lib().nq_get_device_status(_stream(stream), C.byref(v)), "nq_get_device_status")
+    return v.value

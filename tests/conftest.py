@@ -14,3 +14,15 @@ def pytest_configure(config):
 
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="session")
+def nq():
+    """The CUDA binding, with libnq.so built for sm_103a (fails loudly if it cannot be)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test selected but no CUDA device is visible")
+    from quantized_self_speculative_gb300 import build, nq as binding
+    build.build()
+    binding.lib()
+    return binding

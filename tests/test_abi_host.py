@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads and exports every symbol that include/nq.h
+declares; host-side sizes and argument validation work without a GPU (every
+call here is rejected before any CUDA call, and no pointer is dereferenced)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_self_speculative_gb300 import build, nq
+    build.build()
+    return nq.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"NQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    assert {"nq_pack_weights", "nq_draft_gemv", "nq_verify_gemm", "spec_accept_greedy",
+            "spec_accept_sample"} <= names
+    assert len(names) >= 11
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_packed_bytes(L):
+    from quantized_self_speculative_gb300 import nq
+    assert nq.packed_bytes(4096, 4096, 128, nq.FMT_NESTED44) == (4096 * 2048, 4096 * 2048, 4096 * 32 * 2)
+    assert nq.packed_bytes(1024, 1024, 64, nq.FMT_INT4) == (1024 * 512, 0, 1024 * 16 * 2)
+    assert nq.packed_bytes(512, 3584, 0, nq.FMT_FP8E4M3_ROW) == (512 * 3584, 0, 512 * 4)
+    assert nq.packed_bytes(512, 3584, 0, nq.FMT_FP16) == (512 * 3584 * 2, 0, 0)
+    for args, st in [((64, 96, 64, nq.FMT_NESTED44), nq.NQ_ERR_SHAPE),     # k % 64
+                     ((64, 192, 128, nq.FMT_NESTED44), nq.NQ_ERR_SHAPE),   # k % group
+                     ((64, 256, 96, nq.FMT_INT4), nq.NQ_ERR_SHAPE),        # group not 64/128
+                     ((0, 256, 64, nq.FMT_INT4), nq.NQ_ERR_SHAPE),
+                     ((64, 256, 64, 7), nq.NQ_ERR_ARG)]:
+        with pytest.raises(nq.NQError) as e:
+            nq.packed_bytes(*args)
+        assert e.value.status == st
+
+
+def test_workspace_bytes(L):
+    from quantized_self_speculative_gb300 import nq
+    # counters rounded to 256 B, then (2k+1) partials per 4096-entry chunk per row
+    assert nq.workspace_bytes(64, 8, 152064) == 256 + 64 * 17 * 38 * 8
+    assert nq.workspace_bytes(1, 4, 4096) == 256 + 9 * 8
+    for bad in [(0, 4, 10), (1, 0, 10), (1, 17, 10), (1, 4, 0), (1, 4, 524289), (65536, 1, 1)]:
+        assert nq.workspace_bytes(*bad) == 0
+
+
+def test_status_strings(L):
+    from quantized_self_speculative_gb300 import nq
+    assert nq.status_string(0) == "NQ_OK"
+    assert "WORKSPACE" in nq.status_string(nq.NQ_ERR_WORKSPACE)
+    assert nq.status_string(99) == "unknown nq_status"
+
+
+def test_host_validation_rejects_before_launch(L):
+    from quantized_self_speculative_gb300 import nq
+    A = 0x10000            # fake, 16-byte aligned device addresses: never dereferenced
+    W = nq.nq_weights(256, 512, 128, nq.FMT_NESTED44, A, A + 0x100000, A + 0x200000)
+    assert L.nq_draft_gemv(None, A, 1, A, None) == nq.NQ_ERR_ARG
+    assert L.nq_draft_gemv(C.byref(W), A, 0, A, None) == nq.NQ_ERR_ARG           # M = 0
+    assert L.nq_draft_gemv(C.byref(W), A + 2, 1, A, None) == nq.NQ_ERR_ALIGN      # x misaligned
+    bad = nq.nq_weights(256, 512, 128, nq.FMT_NESTED44, A + 8, A, A)
+    assert L.nq_verify_gemm(C.byref(bad), A, 1, A, None) == nq.NQ_ERR_ALIGN
+    i4 = nq.nq_weights(256, 512, 128, nq.FMT_INT4, A, None, A)
+    assert L.nq_verify_gemm(C.byref(i4), A, 1, A, None) == nq.NQ_ERR_ARG        # INT4 is draft-only
+    f16 = nq.nq_weights(256, 512, 0, nq.FMT_FP16, A, None, None)
+    assert L.nq_draft_gemv(C.byref(f16), A, 1, A, None) == nq.NQ_ERR_ARG        # FP16 is verify-only
+    g96 = nq.nq_weights(256, 576, 96, nq.FMT_NESTED44, A, A, A)
+    assert L.nq_draft_gemv(C.byref(g96), A, 1, A, None) == nq.NQ_ERR_SHAPE
+    nores = nq.nq_weights(256, 512, 128, nq.FMT_NESTED44, A, None, A)
+    assert L.nq_verify_gemm(C.byref(nores), A, 1, A, None) == nq.NQ_ERR_ARG
+    # batch: layers of different kernel families in one call are rejected
+    ws = (nq.nq_weights * 2)(W, nq.nq_weights(256, 512, 64, nq.FMT_NESTED44, A, A, A))
+    ptrs = (C.c_void_p * 2)(A, A)
+    assert L.nq_draft_gemv_batch(2, ws, ptrs, 1, ptrs, None) == nq.NQ_ERR_ARG
+    assert L.nq_draft_gemv_batch(0, ws, ptrs, 1, ptrs, None) == nq.NQ_ERR_ARG
+    # acceptance
+    need = nq.workspace_bytes(4, 4, 5000)
+    assert L.spec_accept_greedy(A, A, 4, 0, 5000, A, A, A, need, None) == nq.NQ_ERR_ARG        # k = 0
+    assert L.spec_accept_greedy(A, A, 4, 4, 5000, A, A, A + 4, need, None) == nq.NQ_ERR_ALIGN  # ws
+    assert L.spec_accept_greedy(A, A, 4, 4, 5000, A, A, A, need - 1, None) == nq.NQ_ERR_WORKSPACE
+    assert L.spec_accept_greedy(A, A, 4, 4, 5000, A, A, None, need, None) == nq.NQ_ERR_ARG
+    assert L.spec_accept_sample(A, A, A, 4, 4, 5000, 0.0, A, 0, A, A, A, need, None) == nq.NQ_ERR_ARG
+    assert L.spec_accept_sample(A, A, A, 4, 4, 5000, float("nan"), A, 0, A, A, A, need, None) == nq.NQ_ERR_ARG
+    assert L.spec_accept_sample(A, A + 4, A, 4, 4, 5000, 1.0, A, 0, A, A, A, need, None) == nq.NQ_ERR_ALIGN
+    assert L.nq_pack_weights(None, C.byref(W), None) == nq.NQ_ERR_ARG
+    assert L.nq_pack_weights(A + 4, C.byref(W), None) == nq.NQ_ERR_ALIGN
+    assert L.nq_get_device_status(None, None) == nq.NQ_ERR_ARG
+
+
+def test_product_and_oracle_share_nothing():
+    """The CUDA path never imports / links the oracle, and vice versa."""
+    pkg = os.path.join(ROOT, "quantized_self_speculative_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b|nq_oracle|libnq_oracle", src, re.M), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+quantized_self_speculative_gb300|nq_internal|libnq\.so|nq\.h",
+                                 src, re.M), f

@@ -1,0 +1,110 @@
+"""GPU draft GEMV / verify GEMM (K2-K5) vs the fp64-accumulated oracle.
+
+Tolerance: normwise max relative error <= 2e-3 with bf16 activations.
+Planes are packed by the oracle on the CPU and uploaded, so these tests do
+not depend on the GPU packer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_helpers import TOL, bf16_dev, normwise_err, oracle_fmt, oracle_packed
+from quantized_self_speculative_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # (n, k, group): several 64-row units, ragged tails, K segments
+    (1024, 1024, 128),      # the tiny single-layer workload
+    (200, 640, 64),         # ragged last unit
+    (77, 1152, 128),
+    (130, 4096, 64),
+    (40, 11008, 128),       # long K: activation staging in several segments at M > 1
+]
+
+
+def run_and_compare(nq, fmt, verify, n, k, g, M, seed):
+    w = synth.weights(seed, n, k)
+    pl, (base, resid, scales) = oracle_packed(nq, w, fmt, g)
+    x = synth.activations_bf16(seed + 1, M, k)
+    fn = nq.verify_gemm if verify else nq.draft_gemv
+    y = fn(pl, bf16_dev(x))
+    torch.cuda.synchronize()
+    ref = O.linear(oracle_fmt(nq, fmt), n, k, g, base, resid, scales, x, verify)
+    err = normwise_err(y.cpu().numpy(), ref)
+    assert err <= TOL, (fmt, verify, n, k, g, M, err)
+    return err
+
+
+@pytest.mark.parametrize("n,k,g", CASES)
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_nested_draft_and_verify(nq, n, k, g, M):
+    run_and_compare(nq, nq.FMT_NESTED44, False, n, k, g, M, 1000 + n + M)
+    run_and_compare(nq, nq.FMT_NESTED44, True, n, k, g, M, 2000 + n + M)
+
+
+@pytest.mark.parametrize("M", [2, 3, 7, 8, 9, 13, 17, 33])
+def test_nested_other_batch_sizes(nq, M):
+    run_and_compare(nq, nq.FMT_NESTED44, False, 150, 768, 128, M, 3000 + M)
+    run_and_compare(nq, nq.FMT_NESTED44, True, 150, 768, 64, M, 3100 + M)
+
+
+@pytest.mark.parametrize("n,k", [(300, 512), (64, 3584), (129, 1024)])
+@pytest.mark.parametrize("M", [1, 3, 5, 7, 9, 16])
+def test_int4_fp8_fp16_tiers(nq, n, k, M):
+    run_and_compare(nq, nq.FMT_INT4, False, n, k, 128, M, 4000 + n + M)
+    run_and_compare(nq, nq.FMT_FP8E4M3_ROW, True, n, k, 0, M, 4100 + n + M)
+    run_and_compare(nq, nq.FMT_FP16, True, n, k, 0, M, 4200 + n + M)
+
+
+def test_one_hot_columns_are_exact(nq):
+    n, k, g = 96, 512, 128
+    w = synth.weights(4300, n, k)
+    pl, (base, resid, scales) = oracle_packed(nq, w, nq.FMT_NESTED44, g)
+    cols = [0, 1, 127, 128, 300, 511]
+    x = np.zeros((len(cols), k), np.uint16)
+    one = synth.f32_to_bf16_bits(np.float32([1.0]))[0]
+    for i, c in enumerate(cols):
+        x[i, c] = one
+    for verify in (False, True):
+        y = (nq.verify_gemm if verify else nq.draft_gemv)(pl, bf16_dev(x))
+        ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, x, verify)
+        assert np.array_equal(y.cpu().numpy().astype(np.float64), ref)
+
+
+def test_batch_invariance_and_batched_call(nq):
+    """Each output row is bit-identical whatever M is and whether the layer
+    runs alone or inside a batched launch."""
+    shapes = [(256, 1024), (96, 2048), (1000, 512)]
+    layers, xs = [], []
+    for i, (n, k) in enumerate(shapes):
+        pl, _ = oracle_packed(nq, synth.weights(4400 + i, n, k), nq.FMT_NESTED44, 128)
+        layers.append(pl)
+        xs.append(bf16_dev(synth.activations_bf16(4410 + i, 9, k)))
+    for verify in (False, True):
+        fn = nq.verify_gemm if verify else nq.draft_gemv
+        for pl, x in zip(layers, xs):
+            full = fn(pl, x).cpu()
+            for m in range(9):
+                one = fn(pl, x[m:m + 1].contiguous()).cpu()
+                assert torch.equal(one[0], full[m])
+            assert torch.equal(fn(pl, x[:5].contiguous()).cpu(), full[:5])
+        ys = [torch.empty((9, pl.n_out), dtype=torch.float32, device="cuda") for pl in layers]
+        nq.LinearBatch(verify, layers, xs, ys)()
+        for pl, x, y in zip(layers, xs, ys):
+            assert torch.equal(y.cpu(), fn(pl, x).cpu())
+
+
+def test_rejected_arguments(nq):
+    pl, _ = oracle_packed(nq, synth.weights(4500, 64, 256), nq.FMT_NESTED44, 128)
+    x = bf16_dev(synth.activations_bf16(4501, 2, 256))
+    with pytest.raises(nq.NQError) as e:
+        nq.verify_gemm(pl.as_int4(), x)             # INT4 has no refinement plane
+    assert e.value.status == nq.NQ_ERR_ARG
+    fp16, _ = oracle_packed(nq, synth.weights(4502, 64, 256), nq.FMT_FP16, 0)
+    with pytest.raises(nq.NQError):
+        nq.draft_gemv(fp16, x)                      # FP16 is a verify tier only
+    y = torch.empty(2 * 64 + 1, dtype=torch.float32, device="cuda")[1:].view(2, 64)
+    with pytest.raises(nq.NQError) as e:
+        nq.draft_gemv(pl, x, y)
+    assert e.value.status == nq.NQ_ERR_ALIGN
