@@ -69,6 +69,7 @@ typedef enum {
 #define NQ_DEV_NONFINITE 0x1u
 #define NQ_DEV_BAD_TOKEN 0x2u
 #define NQ_DEV_TIMEOUT   0x4u
+#define NQ_DEV_ACT_RANGE 0x8u   /* an activation exceeded the fp16 range (|x| > 65504) */
 
 /*
  * Weight formats (SpecQuant Sec. III.A tiers; BitNest Fig. 3 planes).
@@ -125,6 +126,10 @@ NQ_API nq_status nq_pack_weights(const float *w, const nq_weights *out, cudaStre
  *   y[m][n] = sum_g s[n][g] * sum_{k in g} q4[n][k] * x[m][k]
  * x: bf16 bits [M][k_in]; y: fp32 [M][n_out]; 1 <= M <= 4096 (the kernel
  * streams the weights once per 16 activation rows).  Formats: NESTED44, INT4.
+ * Arithmetic: the 4-bit codes are exact in fp16; activations are rounded
+ * bf16 -> fp16 (exact for 2^-14 <= |x| <= 65504; |x| > 65504 sets
+ * NQ_DEV_ACT_RANGE), products accumulate in fp32, the group scale is applied
+ * once per group in fp32.
  */
 NQ_API nq_status nq_draft_gemv(const nq_weights *w, const uint16_t *x, int M, float *y, cudaStream_t stream);
 
@@ -134,9 +139,8 @@ NQ_API nq_status nq_draft_gemv(const nq_weights *w, const uint16_t *x, int M, fl
  *   NESTED44:    y[m][n] = sum_g (s[n][g]/16) sum_{k in g} (16 q4 + r)[n][k] x[m][k]
  *   FP8E4M3_ROW: y[m][n] = s[n] sum_k e4m3[n][k] x[m][k]
  *   FP16:        y[m][n] = sum_k w16[n][k] x[m][k]
- * Same layouts and limits as nq_draft_gemv.  The FP8 and FP16 tiers multiply
- * in fp16: activations are rounded bf16 -> fp16 (exact for 2^-14 <= |x| <=
- * 65504), products accumulate in fp32.
+ * Same layouts, limits and fp16/fp32 arithmetic as nq_draft_gemv (E4M3 and
+ * fp16 weights are exact in fp16).
  */
 NQ_API nq_status nq_verify_gemm(const nq_weights *w, const uint16_t *x, int M, float *y, cudaStream_t stream);
 

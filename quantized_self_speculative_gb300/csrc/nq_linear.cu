@@ -8,34 +8,38 @@
 // parents of the same base.
 //
 // Design (GB300, HBM-bound at M <= 16):
-//  * Persistent CTAs walk a flat list of 64-row units over all linears of a
-//    batch (one launch streams a whole model pass: no inter-kernel gaps).
+//  * Persistent CTAs walk a flat list of row units over all linears of a
+//    batch, so one launch streams a whole model pass with no inter-kernel gaps.
 //  * Each warp owns 16 output rows and streams them with 128-bit
-//    non-allocating loads, prefetched D quantisation groups ahead in registers.
-//  * Nibbles become bf16 with one LOP3 per pair (magic-number 128 + (nib^8)),
-//    the contraction runs on the warp MMA (m16n8k16, fp32 accumulate) with the
-//    weight rows as the 16-row A operand and the M <= 16 activation rows as
-//    one or two 8-column B tiles.  The +136 bias of the codes is removed by
-//    starting each group's accumulator at -136 * sum(x over the group).
-//  * Per-group scales are applied once per group in fp32.  The K order of
-//    every group is fixed, so each output element is computed by the same
-//    operations whatever M is (batch invariance).
-//  * Activations are staged once per unit in shared memory, permuted to the
-//    operand order and interleaved so that B-fragment loads are conflict-free.
+//    non-allocating loads, several quantisation groups ahead in a register
+//    ring (each slot is refilled right after it is consumed: no copies).
+//  * Dequantisation costs 5 integer ops per 8 weights: a nibble pair masked to
+//    bits 0-3 (or 4-7) of each half and XOR-ed with 8 is, read as an fp16x2,
+//    exactly (code + 8) * 2^-24 (or 16x that) -- fp16 subnormals.  The x16
+//    pairs meet activations staged as x/16, the +8 offset is removed by
+//    starting the group's accumulator at -8 * 2^-24 * sum(x), and the factor
+//    2^24 is folded into the group scale.
+//  * The contraction runs on the warp MMA (m16n8k16, fp16 in, fp32
+//    accumulate) with the 16 weight rows as the A operand and the M <= 16
+//    activation rows as one or two 8-column B tiles.  Each group uses two
+//    short accumulator chains per plane; the scale is applied once per group.
+//  * The K order inside every group is fixed, so an output element is
+//    computed by the same operations whatever M is (batch invariance).
+//  * Activations are staged once per unit in shared memory, converted to
+//    fp16, permuted into operand order and interleaved so that B-fragment
+//    loads are conflict-free.
 #include <algorithm>
-#include <mutex>
+#include <atomic>
+#include <cstdlib>
 
 #include "nq_internal.cuh"
 
 namespace nq {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerUnit = 16 * kWarps;
-constexpr int kXsBytes = 40 * 1024;   // dynamic shared memory: staged activations + bias terms
-constexpr int kRowPad = 64;           // x row stride = 64 (mod 128) bytes -> conflict-free B loads
+constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
 constexpr int kMaxM = 16;             // activation rows per launch (two 8-column MMA tiles)
+constexpr int kXsMax = 48 * 1024;     // dynamic shared memory cap per CTA
 
 enum Kind { kNib = 0, kFp8 = 1, kFp16 = 2 };
 
@@ -50,65 +54,82 @@ struct Prob {
 
 template <int MAXP>
 struct Batch {
-    int count, total_units, M, pad;
+    int count, total_units, M, xs_bytes;
     Prob p[MAXP];
 };
 
 constexpr int kSmallBatch = 4;
 constexpr int kLargeBatch = 256;
 
-template <int KIND, int G>
-struct Geom {
-    static constexpr int CH = G;                              // inputs per chunk (= quantisation group for nibbles)
-    static constexpr int VB = KIND == kNib ? G / 8 : 16;      // bytes per lane per row per plane per chunk
-    static constexpr int WORDS = VB / 4;
-    static constexpr int CHB = CH * 2;                        // staged activation bytes per chunk per row
-    static constexpr int ROWB_NUM = KIND == kNib ? 1 : (KIND == kFp8 ? 2 : 4);  // row bytes = k * ROWB_NUM / 2
-};
-
-template <int KIND, int PLANES, int G>
-struct Slot {
-    uint32_t w[PLANES][2][Geom<KIND, G>::WORDS];
-    unsigned short s[2];
-};
-
-template <int KIND, int PLANES, int G>
-__device__ __forceinline__ void load_slot(Slot<KIND, PLANES, G> &S, const uint8_t *const (&plane_g)[2],
-                                          const uint8_t *const (&plane_g8)[2], int c,
-                                          const unsigned short *sc_g, const unsigned short *sc_g8)
-{
-    using Gm = Geom<KIND, G>;
-    const size_t off = static_cast<size_t>(c) * (4 * Gm::VB);
-#pragma unroll
-    for (int p = 0; p < PLANES; ++p) {
-        if constexpr (Gm::VB == 16) {
-            uint4 a = ld_stream_v4(plane_g[p] + off), b = ld_stream_v4(plane_g8[p] + off);
-            S.w[p][0][0] = a.x; S.w[p][0][1] = a.y; S.w[p][0][2] = a.z; S.w[p][0][3] = a.w;
-            S.w[p][1][0] = b.x; S.w[p][1][1] = b.y; S.w[p][1][2] = b.z; S.w[p][1][3] = b.w;
-        } else {
-            uint2 a = ld_stream_v2(plane_g[p] + off), b = ld_stream_v2(plane_g8[p] + off);
-            S.w[p][0][0] = a.x; S.w[p][0][1] = a.y;
-            S.w[p][1][0] = b.x; S.w[p][1][1] = b.y;
-        }
-    }
-    if constexpr (KIND == kNib) {
-        S.s[0] = ld_nc_u16(sc_g + c);
-        S.s[1] = ld_nc_u16(sc_g8 + c);
-    }
-}
-
 __device__ __forceinline__ uint4 lds128(const unsigned char *p) { return *reinterpret_cast<const uint4 *>(p); }
 
-template <int KIND, int PLANES, int G, int NT, int MAXP>
-__global__ void __launch_bounds__(kThreads)
-linear_kernel(const __grid_constant__ Batch<MAXP> B)
+template <int MAXP>
+__device__ __forceinline__ int find_problem(const Batch<MAXP> &B, int u)
 {
-    using Gm = Geom<KIND, G>;
-    constexpr int CH = Gm::CH, VB = Gm::VB, WORDS = Gm::WORDS, CHB = Gm::CHB;
+    int lo = 0, hi = B.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (B.p[mid].unit_begin <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// D = C + A * B with fp16 inputs and fp32 accumulators.
+__device__ __forceinline__ void mma_f16_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+// fp16x2 operand pairs of one 32-bit word of nibbles (elements k0..k7 of 8):
+// lo1 = (k0, k4) and hi1 = (k2, k6) as (code + 8) * 2^-24;
+// lo16 = (k1, k5) and hi16 = (k3, k7) as 16 (code + 8) * 2^-24.
+struct NibPairs { uint32_t lo1, hi1, lo16, hi16; };
+
+__device__ __forceinline__ NibPairs nib_pairs(uint32_t w)
+{
+    const uint32_t w8 = w >> 8;
+    NibPairs r;
+    r.lo1 = (w & 0x000F000Fu) ^ 0x00080008u;
+    r.lo16 = (w & 0x00F000F0u) ^ 0x00800080u;
+    r.hi1 = (w8 & 0x000F000Fu) ^ 0x00080008u;
+    r.hi16 = (w8 & 0x00F000F0u) ^ 0x00800080u;
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+           (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
+
+__device__ __forceinline__ float h_lo(uint32_t v) { return __half2float(__ushort_as_half(static_cast<unsigned short>(v))); }
+__device__ __forceinline__ float h_hi(uint32_t v) { return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16))); }
+
+// ------------------------------------------------------------------ nibble kernel
+
+template <int PLANES, int G>
+struct NibSlot {
+    uint32_t w[PLANES][2][G / 32];   // [plane][row g / g+8][word]
+    unsigned short s[2];             // fp16 scales of rows g, g+8
+};
+
+template <int PLANES, int G, int NT, int WARPS, int MAXP>
+__global__ void __launch_bounds__(WARPS * 32)
+nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
+{
+    constexpr int THREADS = WARPS * 32;
+    constexpr int VB = G / 8;                  // bytes per lane per row per plane per group
+    constexpr int WORDS = VB / 4;
+    constexpr int CHB = 2 * G;                 // staged fp16 activation bytes per group per row
     constexpr int MT = 8 * NT;
-    constexpr int LANE_BYTES = 2 * PLANES * VB;                   // per chunk
-    constexpr int D = LANE_BYTES >= 128 ? 1 : 128 / LANE_BYTES;   // prefetch depth (chunks)
-    constexpr int CORR = KIND == kNib ? MT * 4 : 0;               // bias-term bytes per chunk
+    constexpr int LANE_BYTES = 2 * PLANES * VB;
+    constexpr int R = LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8);   // ring slots (R-1 groups in flight)
+    constexpr int ROWS = 16 * WARPS;
+    constexpr float kNeg8Ulp = -4.76837158203125e-07f;   // -8 * 2^-24
 
     extern __shared__ __align__(16) unsigned char smem[];
     const int M = B.M;
@@ -116,227 +137,334 @@ linear_kernel(const __grid_constant__ Batch<MAXP> B)
     const int g = lane >> 2, t = lane & 3;
 
     for (int u = blockIdx.x; u < B.total_units; u += gridDim.x) {
-        int lo = 0, hi = B.count - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (B.p[mid].unit_begin <= u) lo = mid; else hi = mid - 1;
-        }
-        const Prob &P = B.p[lo];
-        const int N = P.n, K = P.k, NCH = K / CH;
-        const int rg = (u - P.unit_begin) * kRowsPerUnit + warp * 16 + g, rg8 = rg + 8;
+        const Prob &P = B.p[find_problem(B, u)];
+        const int N = P.n, K = P.k, NG = K / G;
+        const int rg = (u - P.unit_begin) * ROWS + warp * 16 + g, rg8 = rg + 8;
         const bool vg = rg < N, vg8 = rg8 < N;
-        const size_t rowb = static_cast<size_t>(K) * Gm::ROWB_NUM / 2;
-        const uint8_t *pg[2], *pg8[2];
-        pg[0] = P.base + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t;
-        pg8[0] = P.base + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t;
-        pg[1] = PLANES == 2 ? P.resid + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t : pg[0];
-        pg8[1] = PLANES == 2 ? P.resid + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t : pg8[0];
-        const unsigned short *scg = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg ? rg : 0) * NCH;
-        const unsigned short *scg8 = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg8 ? rg8 : 0) * NCH;
+        const size_t rowb = static_cast<size_t>(K) / 2;
+        const uint8_t *pw[PLANES][2];
+        pw[0][0] = P.base + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t;
+        pw[0][1] = P.base + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t;
+        if constexpr (PLANES == 2) {
+            pw[1][0] = P.resid + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t;
+            pw[1][1] = P.resid + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t;
+        }
+        const unsigned short *ps0 = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg ? rg : 0) * NG;
+        const unsigned short *ps1 = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg8 ? rg8 : 0) * NG;
 
-        // chunks per staged segment of activations
-        int cps = (kXsBytes - M * kRowPad) / (M * CHB + CORR);
-        if (cps > NCH) cps = NCH;
+        auto load = [&](NibSlot<PLANES, G> &S, int c) {
+#pragma unroll
+            for (int p = 0; p < PLANES; ++p)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if constexpr (VB == 16) {
+                        const uint4 v = ld_stream_v4(pw[p][r] + static_cast<size_t>(c) * (G / 2));
+                        S.w[p][r][0] = v.x; S.w[p][r][1] = v.y; S.w[p][r][2] = v.z; S.w[p][r][3] = v.w;
+                    } else {
+                        const uint2 v = ld_stream_v2(pw[p][r] + static_cast<size_t>(c) * (G / 2));
+                        S.w[p][r][0] = v.x; S.w[p][r][1] = v.y;
+                    }
+                }
+            S.s[0] = ld_nc_u16(ps0 + c);
+            S.s[1] = ld_nc_u16(ps1 + c);
+        };
+
+        // groups per staged activation segment (a multiple of R unless all of K fits)
+        int cps = (B.xs_bytes - M * kRowPad) / (M * CHB + MT * 4);
+        if (cps >= NG) cps = NG;
+        else cps = max(R, cps / R * R);
         const int RS = cps * CHB + kRowPad;
         unsigned char *xs = smem;
         float *corr = reinterpret_cast<float *>(smem + M * RS);
 
-        Slot<KIND, PLANES, G> ring[D];
+        NibSlot<PLANES, G> ring[R];
 #pragma unroll
-        for (int i = 0; i < D; ++i)
-            if (i < NCH) load_slot(ring[i], pg, pg8, i, scg, scg8);
+        for (int i = 0; i < R - 1; ++i)
+            if (i < NG) load(ring[i], i);
 
-        // stage activations of chunks [c_begin, c_begin + cps) into shared memory
+        // Stage activations of groups [c_begin, c_begin + cps): fp16, operand
+        // order (x0,x4)(x2,x6)(x1/16,x5/16)(x3/16,x7/16) per 8 inputs, plus
+        // the offset correction -8 * 2^-24 * sum(x) per (group, row).
         auto stage = [&](int c_begin) {
-            const int nch = min(cps, NCH - c_begin);
-            const int items_row = nch * (CH / 8);
+            const int nch = min(cps, NG - c_begin);
+            const int items_row = nch * (G / 8);
             const int total = M * items_row;
-            const int total_pad = (total + kThreads - 1) / kThreads * kThreads;
-            for (int i = threadIdx.x; i < total_pad; i += kThreads) {
+            const int total_pad = (total + THREADS - 1) / THREADS * THREADS;
+            bool range = false;
+            for (int i = threadIdx.x; i < total_pad; i += THREADS) {
                 const bool valid = i < total;
                 const int m = valid ? i / items_row : 0, it = valid ? i % items_row : 0;
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid)
                     v = *reinterpret_cast<const uint4 *>(P.x + static_cast<size_t>(m) * K +
-                                                         static_cast<size_t>(c_begin) * CH + it * 8);
-                const int cl = it / (CH / 8), kk = (it % (CH / 8)) * 8;
-                if constexpr (KIND == kNib) {
-                    // operand order within 8 inputs: 0,4,1,5,2,6,3,7 (matches nib_pair_bf16)
-                    uint4 o;
-                    o.x = __byte_perm(v.x, v.z, 0x5410);
-                    o.y = __byte_perm(v.x, v.z, 0x7632);
-                    o.z = __byte_perm(v.y, v.w, 0x5410);
-                    o.w = __byte_perm(v.y, v.w, 0x7632);
-                    const int tl = kk / (2 * VB), wd = (kk % (2 * VB)) / 8;
-                    if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
-                    const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-                    const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-                    const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
-                    const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
-                    float s = __fadd_rn(__fadd_rn(__fadd_rn(x0, x1), __fadd_rn(x2, x3)),
-                                        __fadd_rn(__fadd_rn(x4, x5), __fadd_rn(x6, x7)));
+                                                         static_cast<size_t>(c_begin) * G + it * 8);
+                const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
+                const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
+                uint4 o;
+                o.x = pack_h2(x0, x4);
+                o.y = pack_h2(x2, x6);
+                o.z = pack_h2(__fmul_rn(x1, 0.0625f), __fmul_rn(x5, 0.0625f));
+                o.w = pack_h2(__fmul_rn(x3, 0.0625f), __fmul_rn(x7, 0.0625f));
+                const float amax = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
+                                         fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
+                range |= amax > 65504.0f;
+                const int cl = it / (G / 8), kk = (it % (G / 8)) * 8;
+                const int tl = kk / (2 * VB), wd = (kk % (2 * VB)) / 8;
+                if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
+                // sum of the staged values as the MMA sees them: x~ at even k, 16 * (x/16)~ at odd k
+                const float se = __fadd_rn(__fadd_rn(h_lo(o.x), h_hi(o.x)), __fadd_rn(h_lo(o.y), h_hi(o.y)));
+                const float so = __fadd_rn(__fadd_rn(h_lo(o.z), h_hi(o.z)), __fadd_rn(h_lo(o.w), h_hi(o.w)));
+                float s = __fmaf_rn(16.0f, so, se);
 #pragma unroll
-                    for (int o2 = 1; o2 < CH / 8; o2 <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o2));
-                    if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(-136.0f, s);
-                } else {
-                    // bf16 -> fp16 (round to nearest), natural order
-                    uint32_t h[4];
-                    const uint32_t src[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __half lo16 = __float2half_rn(__uint_as_float(src[q] << 16));
-                        const __half hi16 = __float2half_rn(__uint_as_float(src[q] & 0xFFFF0000u));
-                        h[q] = static_cast<uint32_t>(__half_as_ushort(lo16)) |
-                               (static_cast<uint32_t>(__half_as_ushort(hi16)) << 16);
-                    }
-                    int pos;
-                    if constexpr (KIND == kFp8) pos = 4 * ((kk % 16) / 8) + kk / 16;   // lane kk/16, piece (kk%16)/8
-                    else pos = kk / 8;
-                    if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + pos * 16) = make_uint4(h[0], h[1], h[2], h[3]);
-                }
+                for (int o2 = 1; o2 < G / 8; o2 <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o2));
+                if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(kNeg8Ulp, s);
             }
-            if constexpr (KIND == kNib)
-                for (int i = threadIdx.x; i < nch * (MT - M); i += kThreads)
-                    corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
+            for (int i = threadIdx.x; i < nch * (MT - M); i += THREADS)
+                corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
+            if (range) set_status(status, NQ_DEV_ACT_RANGE);
         };
 
         __syncthreads();   // the previous unit is done with shared memory
         stage(0);
         __syncthreads();
 
-        int mrow[NT];
-        bool mvalid[NT];
+        // per-lane activation rows: rows >= M read a zero-stride dummy (their
+        // columns are never stored)
+        const unsigned char *xrow[NT];
+        int xstep[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            mrow[nt] = nt * 8 + g;
-            mvalid[nt] = mrow[nt] < M;
+            const int m = nt * 8 + g;
+            xrow[nt] = xs + (m < M ? m : 0) * RS + t * 16;
+            xstep[nt] = m < M ? CHB : 0;
         }
 
-        float yacc[NT][4];
+        float y[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) yacc[nt][i] = 0.0f;
+            for (int i = 0; i < 4; ++i) y[nt][i] = 0.0f;
 
-        int seg_begin = 0;
-        for (int c0 = 0; c0 < NCH; c0 += D) {
+        for (int c0 = 0; c0 < NG; c0 += R) {
+            if (c0 > 0 && c0 % cps == 0) {
+                __syncthreads();
+                stage(c0);
+                __syncthreads();
+            }
+            const int cbase = c0 % cps;
 #pragma unroll
-            for (int i = 0; i < D; ++i) {
+            for (int i = 0; i < R; ++i) {
                 const int c = c0 + i;
-                if (c < NCH) {
-                    if (c - seg_begin >= cps) {
-                        seg_begin = c;
-                        __syncthreads();
-                        stage(seg_begin);
-                        __syncthreads();
-                    }
-                    const Slot<KIND, PLANES, G> cur = ring[i];
-                    if (c + D < NCH) load_slot(ring[i], pg, pg8, c + D, scg, scg8);
-                    const int cl = c - seg_begin;
-                    const unsigned char *xc[NT];
+                if (c < NG) {
+                    if (c + R - 1 < NG) load(ring[(i + R - 1) % R], c + R - 1);
+                    const NibSlot<PLANES, G> &S = ring[i];
+                    const int cl = cbase + i;
+                    float accA[NT][PLANES][4], accB[NT][PLANES][4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xc[nt] = xs + (mvalid[nt] ? mrow[nt] : 0) * RS + cl * CHB;
-
-                    if constexpr (KIND == kNib) {
-                        float acc[NT][PLANES][4];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const float2 cc = *reinterpret_cast<const float2 *>(corr + cl * MT + nt * 8 + 2 * t);
-#pragma unroll
-                            for (int p = 0; p < PLANES; ++p) {
-                                acc[nt][p][0] = cc.x; acc[nt][p][1] = cc.y;
-                                acc[nt][p][2] = cc.x; acc[nt][p][3] = cc.y;
-                            }
-                        }
-#pragma unroll
-                        for (int wd = 0; wd < WORDS; ++wd) {
-                            uint4 bq[NT];
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                bq[nt] = mvalid[nt] ? lds128(xc[nt] + (4 * wd + t) * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                            for (int p = 0; p < PLANES; ++p) {
-                                const uint32_t Wg = cur.w[p][0][wd], W8 = cur.w[p][1][wd];
-                                {
-                                    const uint32_t a0 = nib_pair_bf16<0>(Wg), a2 = nib_pair_bf16<1>(Wg);
-                                    const uint32_t a1 = nib_pair_bf16<0>(W8), a3 = nib_pair_bf16<1>(W8);
-#pragma unroll
-                                    for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][p], a0, a1, a2, a3, bq[nt].x, bq[nt].y);
-                                }
-                                {
-                                    const uint32_t a0 = nib_pair_bf16<2>(Wg), a2 = nib_pair_bf16<3>(Wg);
-                                    const uint32_t a1 = nib_pair_bf16<2>(W8), a3 = nib_pair_bf16<3>(W8);
-#pragma unroll
-                                    for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][p], a0, a1, a2, a3, bq[nt].z, bq[nt].w);
-                                }
-                            }
-                        }
-                        const float sg = __half2float(__ushort_as_half(cur.s[0]));
-                        const float sg8 = __half2float(__ushort_as_half(cur.s[1]));
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            yacc[nt][0] = __fmaf_rn(sg, acc[nt][0][0], yacc[nt][0]);
-                            yacc[nt][1] = __fmaf_rn(sg, acc[nt][0][1], yacc[nt][1]);
-                            yacc[nt][2] = __fmaf_rn(sg8, acc[nt][0][2], yacc[nt][2]);
-                            yacc[nt][3] = __fmaf_rn(sg8, acc[nt][0][3], yacc[nt][3]);
-                            if constexpr (PLANES == 2) {
-                                const float rg16 = __fmul_rn(sg, 0.0625f), rg816 = __fmul_rn(sg8, 0.0625f);
-                                yacc[nt][0] = __fmaf_rn(rg16, acc[nt][1][0], yacc[nt][0]);
-                                yacc[nt][1] = __fmaf_rn(rg16, acc[nt][1][1], yacc[nt][1]);
-                                yacc[nt][2] = __fmaf_rn(rg816, acc[nt][1][2], yacc[nt][2]);
-                                yacc[nt][3] = __fmaf_rn(rg816, acc[nt][1][3], yacc[nt][3]);
-                            }
-                        }
-                    } else if constexpr (KIND == kFp8) {
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            uint4 bq[NT];
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                bq[nt] = mvalid[nt] ? lds128(xc[nt] + (4 * q + t) * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int s = 2 * q + h;
-                                uint32_t a0, a2, a1, a3;
-                                e4m3x4_to_f16x2x2(cur.w[0][0][s], a0, a2);
-                                e4m3x4_to_f16x2x2(cur.w[0][1][s], a1, a3);
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    mma_f16(yacc[nt], a0, a1, a2, a3, h ? bq[nt].z : bq[nt].x, h ? bq[nt].w : bq[nt].y);
-                            }
-                        }
-                    } else {
+                    for (int wd = 0; wd < WORDS; ++wd) {
                         uint4 bq[NT];
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            bq[nt] = mvalid[nt] ? lds128(xc[nt] + t * 16) : make_uint4(0, 0, 0, 0);
+                        for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt] + wd * 64);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            mma_f16(yacc[nt], cur.w[0][0][0], cur.w[0][1][0], cur.w[0][0][1], cur.w[0][1][1], bq[nt].x, bq[nt].y);
-                            mma_f16(yacc[nt], cur.w[0][0][2], cur.w[0][1][2], cur.w[0][0][3], cur.w[0][1][3], bq[nt].z, bq[nt].w);
+                        for (int p = 0; p < PLANES; ++p) {
+                            const NibPairs a = nib_pairs(S.w[p][0][wd]), b = nib_pairs(S.w[p][1][wd]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                if (wd == 0) {
+                                    const float2 cc = *reinterpret_cast<const float2 *>(corr + cl * MT + nt * 8 + 2 * t);
+                                    mma_f16_c(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y, cc.x, cc.y, cc.x, cc.y);
+                                    mma_f16_c(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w, 0.f, 0.f, 0.f, 0.f);
+                                } else {
+                                    mma_f16(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y);
+                                    mma_f16(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w);
+                                }
+                            }
+                        }
+                    }
+                    // group scale x 2^24 (undoes the subnormal encoding); refinement plane at s/16
+                    const float s0 = __fmul_rn(__half2float(__ushort_as_half(S.s[0])), 16777216.0f);
+                    const float s1 = __fmul_rn(__half2float(__ushort_as_half(S.s[1])), 16777216.0f);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sc = e < 2 ? s0 : s1;
+                            y[nt][e] = __fmaf_rn(sc, __fadd_rn(accA[nt][0][e], accB[nt][0][e]), y[nt][e]);
+                            if constexpr (PLANES == 2)
+                                y[nt][e] = __fmaf_rn(__fmul_rn(sc, 0.0625f), __fadd_rn(accA[nt][1][e], accB[nt][1][e]), y[nt][e]);
                         }
                     }
                 }
             }
         }
 
-        float rs_g = 1.0f, rs_g8 = 1.0f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = nt * 8 + 2 * t + (e & 1);
+                const bool top = e < 2;
+                if (m < M && (top ? vg : vg8)) P.y[static_cast<size_t>(m) * N + (top ? rg : rg8)] = y[nt][e];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ FP8 / FP16 tier kernel
+
+template <int KIND>
+struct FpGeom {
+    static constexpr int CH = KIND == kFp8 ? 64 : 32;   // inputs per chunk
+    static constexpr int ROWB_NUM = KIND == kFp8 ? 1 : 2;   // row bytes = k * ROWB_NUM
+};
+
+constexpr int kFpWarps = 4;
+
+template <int KIND, int NT, int MAXP>
+__global__ void __launch_bounds__(kFpWarps * 32)
+fp_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
+{
+    constexpr int THREADS = kFpWarps * 32;
+    constexpr int CH = FpGeom<KIND>::CH, CHB = CH * 2;
+    constexpr int R = 5;          // ring slots: 4 chunks (2 rows x 16 B) in flight
+    constexpr int ROWS = 16 * kFpWarps;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int M = B.M;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+
+    for (int u = blockIdx.x; u < B.total_units; u += gridDim.x) {
+        const Prob &P = B.p[find_problem(B, u)];
+        const int N = P.n, K = P.k, NCH = K / CH;
+        const int rg = (u - P.unit_begin) * ROWS + warp * 16 + g, rg8 = rg + 8;
+        const bool vg = rg < N, vg8 = rg8 < N;
+        const size_t rowb = static_cast<size_t>(K) * FpGeom<KIND>::ROWB_NUM;
+        const uint8_t *p0 = P.base + static_cast<size_t>(vg ? rg : 0) * rowb + 16 * t;
+        const uint8_t *p1 = P.base + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + 16 * t;
+
+        int cps = (B.xs_bytes - M * kRowPad) / (M * CHB);
+        if (cps >= NCH) cps = NCH;
+        else cps = max(R, cps / R * R);
+        const int RS = cps * CHB + kRowPad;
+        unsigned char *xs = smem;
+
+        uint4 ring[R][2];
+#pragma unroll
+        for (int i = 0; i < R - 1; ++i)
+            if (i < NCH) {
+                ring[i][0] = ld_stream_v4(p0 + static_cast<size_t>(i) * 64);
+                ring[i][1] = ld_stream_v4(p1 + static_cast<size_t>(i) * 64);
+            }
+
+        auto stage = [&](int c_begin) {
+            const int nch = min(cps, NCH - c_begin);
+            const int items_row = nch * (CH / 8);
+            const int total = M * items_row;
+            bool range = false;
+            for (int i = threadIdx.x; i < total; i += THREADS) {
+                const int m = i / items_row, it = i % items_row;
+                const uint4 v = *reinterpret_cast<const uint4 *>(P.x + static_cast<size_t>(m) * K +
+                                                                 static_cast<size_t>(c_begin) * CH + it * 8);
+                const uint32_t src[4] = {v.x, v.y, v.z, v.w};
+                uint32_t h[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float lo = __uint_as_float(src[q] << 16), hi = __uint_as_float(src[q] & 0xFFFF0000u);
+                    range |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.0f;
+                    h[q] = pack_h2(lo, hi);
+                }
+                const int cl = it / (CH / 8), kk = (it % (CH / 8)) * 8;
+                const int pos = KIND == kFp8 ? 4 * ((kk % 16) / 8) + kk / 16 : kk / 8;
+                *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + pos * 16) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+            if (range) set_status(status, NQ_DEV_ACT_RANGE);
+        };
+
+        __syncthreads();
+        stage(0);
+        __syncthreads();
+
+        const unsigned char *xrow[NT];
+        int xstep[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int m = nt * 8 + g;
+            xrow[nt] = xs + (m < M ? m : 0) * RS + t * 16;
+            xstep[nt] = m < M ? CHB : 0;
+        }
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+
+        for (int c0 = 0; c0 < NCH; c0 += R) {
+            if (c0 > 0 && c0 % cps == 0) {
+                __syncthreads();
+                stage(c0);
+                __syncthreads();
+            }
+            const int cbase = c0 % cps;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int c = c0 + i;
+                if (c < NCH) {
+                    if (c + R - 1 < NCH) {
+                        ring[(i + R - 1) % R][0] = ld_stream_v4(p0 + static_cast<size_t>(c + R - 1) * 64);
+                        ring[(i + R - 1) % R][1] = ld_stream_v4(p1 + static_cast<size_t>(c + R - 1) * 64);
+                    }
+                    const uint4 wa = ring[i][0], wb = ring[i][1];
+                    const int cl = cbase + i;
+                    if constexpr (KIND == kFp8) {
+                        const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, Bw[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            uint4 bq[NT];
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt] + q * 64);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t a0, a2, a1, a3;
+                                e4m3x4_to_f16x2x2(A[2 * q + h], a0, a2);
+                                e4m3x4_to_f16x2x2(Bw[2 * q + h], a1, a3);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma_f16(acc[nt], a0, a1, a2, a3, h ? bq[nt].z : bq[nt].x, h ? bq[nt].w : bq[nt].y);
+                            }
+                        }
+                    } else {
+                        uint4 bq[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt]);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_f16(acc[nt], wa.x, wb.x, wa.y, wb.y, bq[nt].x, bq[nt].y);
+                            mma_f16(acc[nt], wa.z, wb.z, wa.w, wb.w, bq[nt].z, bq[nt].w);
+                        }
+                    }
+                }
+            }
+        }
+
+        float rs0 = 1.0f, rs1 = 1.0f;
         if constexpr (KIND == kFp8) {
             const float *rsc = static_cast<const float *>(P.scales);
-            rs_g = vg ? rsc[rg] : 0.0f;
-            rs_g8 = vg8 ? rsc[rg8] : 0.0f;
+            rs0 = vg ? rsc[rg] : 0.0f;
+            rs1 = vg8 ? rsc[rg8] : 0.0f;
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m = nt * 8 + 2 * t + (i & 1);
-                const bool top = i < 2;
-                const int row = top ? rg : rg8;
+            for (int e = 0; e < 4; ++e) {
+                const int m = nt * 8 + 2 * t + (e & 1);
+                const bool top = e < 2;
                 if (m < M && (top ? vg : vg8)) {
-                    float v = yacc[nt][i];
-                    if constexpr (KIND == kFp8) v = __fmul_rn(top ? rs_g : rs_g8, v);
-                    P.y[static_cast<size_t>(m) * N + row] = v;
+                    float v = acc[nt][e];
+                    if constexpr (KIND == kFp8) v = __fmul_rn(top ? rs0 : rs1, v);
+                    P.y[static_cast<size_t>(m) * N + (top ? rg : rg8)] = v;
                 }
             }
         }
@@ -345,41 +473,73 @@ linear_kernel(const __grid_constant__ Batch<MAXP> B)
 
 // ------------------------------------------------------------------ host side
 
-template <int KIND, int PLANES, int G, int NT, int MAXP>
-int occupancy()
+template <typename F>
+int occupancy_of(F kernel, int threads, int smem)
 {
-    static std::once_flag once;
-    static int occ = 1;
-    std::call_once(once, [] {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, linear_kernel<KIND, PLANES, G, NT, MAXP>, kThreads, kXsBytes) ==
-                cudaSuccess && o > 0)
-            occ = o;
-    });
-    return occ;
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, threads, smem) != cudaSuccess || o < 1) o = 1;
+    return o;
 }
 
-template <int KIND, int PLANES, int G, int NT, int MAXP>
-cudaError_t launch_t(const Batch<MAXP> &b, cudaStream_t stream)
+// Units, shared memory and launch for one kernel instantiation.
+// Resident CTAs per SM for a kernel at a given dynamic shared memory size,
+// cached per 1 KiB bucket (the launch configuration is a pure function of it).
+template <typename F>
+int cached_occupancy(F kernel, int threads, int smem, std::atomic<int> (&cache)[kXsMax / 1024 + 1])
 {
-    const int grid = std::min(b.total_units, sm_count() * occupancy<KIND, PLANES, G, NT, MAXP>());
-    linear_kernel<KIND, PLANES, G, NT, MAXP><<<grid, kThreads, kXsBytes, stream>>>(b);
+    const int bucket = (smem + 1023) / 1024;
+    int o = cache[bucket].load(std::memory_order_relaxed);
+    if (o == 0) {
+        o = occupancy_of(kernel, threads, bucket * 1024);
+        cache[bucket].store(o, std::memory_order_relaxed);
+    }
+    return o;
+}
+
+template <int PLANES, int G, int NT, int WARPS, int MAXP>
+cudaError_t launch_nib(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
+{
+    auto k = nib_kernel<PLANES, G, NT, WARPS, MAXP>;
+    static std::atomic<int> occ[kXsMax / 1024 + 1];
+    const int grid = std::max(1, std::min(b.total_units, sm_count() * cached_occupancy(k, WARPS * 32, b.xs_bytes, occ)));
+    k<<<grid, WARPS * 32, b.xs_bytes, s>>>(b, status);
     return cudaGetLastError();
 }
 
+template <int KIND, int NT, int MAXP>
+cudaError_t launch_fp(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
+{
+    auto k = fp_kernel<KIND, NT, MAXP>;
+    static std::atomic<int> occ[kXsMax / 1024 + 1];
+    const int grid = std::max(1, std::min(b.total_units, sm_count() * cached_occupancy(k, kFpWarps * 32, b.xs_bytes, occ)));
+    k<<<grid, kFpWarps * 32, b.xs_bytes, s>>>(b, status);
+    return cudaGetLastError();
+}
+
+template <int PLANES, int G, int NT, int MAXP>
+cudaError_t dispatch_nib_w(Batch<MAXP> &b, int warps, cudaStream_t s, unsigned int *st)
+{
+    if constexpr (MAXP == kSmallBatch) {
+        return launch_nib<PLANES, G, NT, 4, MAXP>(b, s, st);
+    } else {
+        return warps == 8 ? launch_nib<PLANES, G, NT, 8, MAXP>(b, s, st) : launch_nib<PLANES, G, NT, 4, MAXP>(b, s, st);
+    }
+}
+
 template <int MAXP>
-cudaError_t launch_kind(int kind, int planes, int group, int nt, const Batch<MAXP> &b, cudaStream_t s)
+cudaError_t launch_kind(int kind, int planes, int group, int nt, int warps, Batch<MAXP> &b, cudaStream_t s,
+                        unsigned int *st)
 {
     if (kind == kNib) {
         if (planes == 1) {
-            if (group == 128) return nt == 1 ? launch_t<kNib, 1, 128, 1>(b, s) : launch_t<kNib, 1, 128, 2>(b, s);
-            return nt == 1 ? launch_t<kNib, 1, 64, 1>(b, s) : launch_t<kNib, 1, 64, 2>(b, s);
+            if (group == 128) return nt == 1 ? dispatch_nib_w<1, 128, 1>(b, warps, s, st) : dispatch_nib_w<1, 128, 2>(b, warps, s, st);
+            return nt == 1 ? dispatch_nib_w<1, 64, 1>(b, warps, s, st) : dispatch_nib_w<1, 64, 2>(b, warps, s, st);
         }
-        if (group == 128) return nt == 1 ? launch_t<kNib, 2, 128, 1>(b, s) : launch_t<kNib, 2, 128, 2>(b, s);
-        return nt == 1 ? launch_t<kNib, 2, 64, 1>(b, s) : launch_t<kNib, 2, 64, 2>(b, s);
+        if (group == 128) return nt == 1 ? dispatch_nib_w<2, 128, 1>(b, warps, s, st) : dispatch_nib_w<2, 128, 2>(b, warps, s, st);
+        return nt == 1 ? dispatch_nib_w<2, 64, 1>(b, warps, s, st) : dispatch_nib_w<2, 64, 2>(b, warps, s, st);
     }
-    if (kind == kFp8) return nt == 1 ? launch_t<kFp8, 1, 64, 1>(b, s) : launch_t<kFp8, 1, 64, 2>(b, s);
-    return nt == 1 ? launch_t<kFp16, 1, 32, 1>(b, s) : launch_t<kFp16, 1, 32, 2>(b, s);
+    if (kind == kFp8) return nt == 1 ? launch_fp<kFp8, 1>(b, s, st) : launch_fp<kFp8, 2>(b, s, st);
+    return nt == 1 ? launch_fp<kFp16, 1>(b, s, st) : launch_fp<kFp16, 2>(b, s, st);
 }
 
 // Validate one layer for the given pass; returns the kernel family.
@@ -398,20 +558,54 @@ nq_status check_layer(const nq_weights &w, bool verify, int &kind, int &planes)
     if (!w.base || (planes == 2 && !w.resid) || ((kind == kNib || kind == kFp8) && !w.scales)) return NQ_ERR_ARG;
     if (!aligned16(w.base) || (planes == 2 && !aligned16(w.resid)) || ((kind == kNib || kind == kFp8) && !aligned16(w.scales)))
         return NQ_ERR_ALIGN;
-    const long long units = (static_cast<long long>(w.n_out) + kRowsPerUnit - 1) / kRowsPerUnit;
-    if (units > (1LL << 30)) return NQ_ERR_SHAPE;
+    if (w.n_out > (1 << 28)) return NQ_ERR_SHAPE;
     return NQ_OK;
+}
+
+// Tuning override of the CTA width of batched nibble launches (NQ_LINEAR_WARPS = 4 or 8).
+int linear_warps_override()
+{
+    static const int v = [] {
+        const char *e = std::getenv("NQ_LINEAR_WARPS");
+        const int w = e ? std::atoi(e) : 0;
+        return (w == 4 || w == 8) ? w : 0;
+    }();
+    return v;
+}
+
+// Dynamic shared memory for a launch: all activation rows of the widest layer
+// (in fp16, padded rows, plus offset corrections), capped at kXsMax.
+int xs_bytes_for(int kind, int M, int kmax, int group)
+{
+    const int ch = kind == kNib ? group : (kind == kFp8 ? 64 : 32);
+    const int chunks = kmax / ch;
+    const int mt = M > 8 ? 16 : 8;
+    const long long need = static_cast<long long>(M) * (chunks * 2 * ch + kRowPad) +
+                           (kind == kNib ? static_cast<long long>(chunks) * mt * 4 : 0);
+    return static_cast<int>(std::min<long long>(need, kXsMax));
 }
 
 template <int MAXP>
 nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, int M, float *const *y,
                     int kind, int planes, int group, cudaStream_t stream)
 {
+    unsigned int *status = device_status_ptr();
+    if (!status) return NQ_ERR_CUDA;
     Batch<MAXP> b{};
     for (int m0 = 0; m0 < M; m0 += kMaxM) {
         const int Mc = std::min(kMaxM, M - m0);
         for (int i0 = 0; i0 < count; i0 += MAXP) {
             const int cnt = std::min(MAXP, count - i0);
+            int kmax = 0;
+            long long rows16 = 0;
+            for (int i = 0; i < cnt; ++i) {
+                kmax = std::max(kmax, w[i0 + i].k_in);
+                rows16 += (w[i0 + i].n_out + 15) / 16;
+            }
+            // 8-warp units when there are enough of them to fill the GPU twice
+            int warps = (kind == kNib && MAXP == kLargeBatch && rows16 / 8 >= 2LL * sm_count()) ? 8 : 4;
+            if (kind == kNib && MAXP == kLargeBatch && linear_warps_override() != 0) warps = linear_warps_override();
+            const int rows_per_unit = kind == kNib ? 16 * warps : 16 * kFpWarps;
             long long units = 0;
             for (int i = 0; i < cnt; ++i) {
                 const nq_weights &L = w[i0 + i];
@@ -425,13 +619,14 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
                 p.k = L.k_in;
                 p.unit_begin = static_cast<int>(units);
                 p.pad = 0;
-                units += (L.n_out + kRowsPerUnit - 1) / kRowsPerUnit;
+                units += (L.n_out + rows_per_unit - 1) / rows_per_unit;
             }
             if (units > 0x7fffffffLL) return NQ_ERR_SHAPE;
             b.count = cnt;
             b.total_units = static_cast<int>(units);
             b.M = Mc;
-            const cudaError_t e = launch_kind<MAXP>(kind, planes, group, Mc > 8 ? 2 : 1, b, stream);
+            b.xs_bytes = xs_bytes_for(kind, Mc, kmax, group);
+            const cudaError_t e = launch_kind<MAXP>(kind, planes, group, Mc > 8 ? 2 : 1, warps, b, stream, status);
             if (e != cudaSuccess) return NQ_ERR_CUDA;
         }
     }

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libnq.so")
 
 NQ_OK, NQ_ERR_ARG, NQ_ERR_SHAPE, NQ_ERR_ALIGN, NQ_ERR_CUDA = 0, 1, 2, 3, 4
 NQ_ERR_NONFINITE, NQ_ERR_TIMEOUT, NQ_ERR_WORKSPACE, NQ_ERR_TOKEN = 5, 6, 7, 8
-NQ_DEV_NONFINITE, NQ_DEV_BAD_TOKEN, NQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
+NQ_DEV_NONFINITE, NQ_DEV_BAD_TOKEN, NQ_DEV_TIMEOUT, NQ_DEV_ACT_RANGE = 0x1, 0x2, 0x4, 0x8
 FMT_NESTED44, FMT_INT4, FMT_FP8E4M3_ROW, FMT_FP16 = 0, 1, 2, 3
 
 _lock = threading.Lock()
