@@ -199,6 +199,24 @@ NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_log
                              uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
                              size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Greedy acceptance that allocates nothing and takes no workspace: the same
+ * computation and results as spec_accept_greedy, for callers that cannot
+ * allocate device memory where they decide tokens (their device memory is
+ * owned by another component, such as a serving runtime with a fixed budget,
+ * or an allocation must not fail or block inside the decode loop).  The pages
+ * have no counterpart; this is a deployment variant.
+ * Scratch: a fixed 1 MiB array inside the library, held on every GPU that
+ * loads the library until the process exits.  Sizes needing more than that,
+ * 256 + B*(k+1)*ceil(V/4096)*8 bytes > 1 MiB, return NQ_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call clears the part of the array that must start at zero.  All calls share
+ * the one array: calls that overlap on the GPU race and give wrong results.
+ */
+NQ_API nq_status spec_accept_greedy_noalloc(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
+                                            int32_t *out_tok, int32_t *out_cnt, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 NQ_API const char *nq_status_string(int status);
 

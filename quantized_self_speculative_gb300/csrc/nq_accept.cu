@@ -16,6 +16,7 @@
 // L2.  All fp32 arithmetic of the sampled path follows the fixed recipe
 // documented in nq.h so that decisions are reproducible bit for bit.
 #include <algorithm>
+#include <mutex>
 
 #include "nq_internal.cuh"
 
@@ -536,5 +537,64 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     dim3 grid(nq::n_chunks(V), 2 * k + 1, B);
     nq::sample_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
                                                          out_tok, out_cnt, counters, part, status);
+    return nq::cuda_status(cudaGetLastError());
+}
+
+// ------------------------------------------------------------------ allocation-free greedy acceptance
+//
+// For callers that cannot allocate device memory at the call site (their
+// device memory is owned by another component -- e.g. a serving runtime whose
+// allocator holds a fixed budget -- or they must not risk a failing or
+// blocking allocation in the decode loop): the workspace of the greedy
+// acceptance lives in a fixed array compiled into this file.  Every GPU that
+// loads the library holds it until the process exits.  All calls share it.
+
+namespace nq {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;   // 1 MiB
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (host code may not use the symbol).
+void *noalloc_scratch()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace nq
+
+extern "C" nq_status spec_accept_greedy_noalloc(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
+                                                int32_t *out_tok, int32_t *out_cnt, cudaStream_t stream)
+{
+    if (B < 1 || B > 65535 || k < 1 || k > nq::kMaxK || V < 1 || V > nq::kMaxChunks * nq::kChunk) return NQ_ERR_ARG;
+    if (!draft || !tgt_logits || !out_tok || !out_cnt) return NQ_ERR_ARG;
+    if (!nq::aligned16(draft) || !nq::aligned16(tgt_logits) || !nq::aligned16(out_tok) || !nq::aligned16(out_cnt))
+        return NQ_ERR_ALIGN;
+    const size_t counters = nq::counters_bytes(B);
+    const size_t need = counters + static_cast<size_t>(B) * (k + 1) * nq::n_chunks(V) * sizeof(float2);
+    if (need > nq::kNoAllocScratchBytes) return NQ_ERR_WORKSPACE;
+    unsigned char *scratch = static_cast<unsigned char *>(nq::noalloc_scratch());
+    unsigned int *status = nq::device_status_ptr();
+    if (!scratch || !status) return NQ_ERR_CUDA;
+    // the per-row tickets must start at zero; the partials are overwritten
+    if (cudaMemsetAsync(scratch, 0, counters, stream) != cudaSuccess) return NQ_ERR_CUDA;
+    dim3 grid(nq::n_chunks(V), k + 1, B);
+    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
+                                                         reinterpret_cast<unsigned int *>(scratch),
+                                                         reinterpret_cast<float2 *>(scratch + counters), status);
     return nq::cuda_status(cudaGetLastError());
 }
