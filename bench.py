@@ -265,6 +265,164 @@ def accept_sweep(device, iters=20):
     return out
 
 
+# ------------------------------------------------------------------ whole-pass sweeps (configs 3 and 4)
+def _pass_layers(device, shapes, fmt, group, seed, w16=False):
+    """Pack every linear of a pass in one format (weights drawn on the GPU)."""
+    import torch
+    from quantized_self_speculative_gb300 import nq
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    layers = []
+    for n, k in shapes:
+        w = torch.randn((n, k), generator=gen, device=device, dtype=torch.float32).mul_(0.02)
+        if w16:
+            w = w.half().float()          # the tiers derive from one fp16 base
+        layers.append(nq.pack_weights(w, fmt, group))
+        del w
+    torch.cuda.synchronize()
+    return layers
+
+
+def _time_pass(device, layers, M, verify, iters=10):
+    """Device time of one batched launch over all layers at M activation rows."""
+    import torch
+    from quantized_self_speculative_gb300 import nq
+    gen = torch.Generator(device=device)
+    gen.manual_seed(123)
+    xs = [torch.randn((M, L.k_in), generator=gen, device=device).to(torch.bfloat16) for L in layers]
+    ys = [torch.empty((M, L.n_out), dtype=torch.float32, device=device) for L in layers]
+    b = nq.LinearBatch(verify, layers, xs, ys)
+    for _ in range(3):
+        b()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        b()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    per_w = {nq.FMT_NESTED44: (1.0 if verify else 0.5), nq.FMT_INT4: 0.5, nq.FMT_FP8E4M3_ROW: 1.0, nq.FMT_FP16: 2.0}
+    byts = 0
+    for L in layers:
+        wb = per_w[L.fmt] * L.n_out * L.k_in
+        sb = (2 * L.n_out * L.k_in // L.group) if L.fmt in (nq.FMT_NESTED44, nq.FMT_INT4) else (4 * L.n_out if L.fmt == nq.FMT_FP8E4M3_ROW else 0)
+        byts += wb + sb + 2 * M * L.k_in + 4 * M * L.n_out
+    hbm, _ = peaks()
+    return {"M": M, "us": round(us, 1), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+            "frac": round(byts / (us * 1e-6) / 1e9 / hbm, 4), "bytes": int(byts),
+            "tflops": round(2.0 * M * sum(L.n_out * L.k_in for L in layers) / (us * 1e-6) / 1e12, 2)}
+
+
+def _shapes(spec):
+    layer, lm, n_layers = spec()
+    return [(n, k) for _ in range(n_layers) for _, n, k in layer] + [(lm[1], lm[2])]
+
+
+def config3_sweep(device):
+    """LLaMA-3-8B-shaped linears, batch 16, k = 8: draft M = 16 (base plane),
+    verify M = 144 (both planes), groups 64 and 128."""
+    import torch
+    from quantized_self_speculative_gb300 import nq, synth
+    out = {}
+    shapes = _shapes(synth.llama3_8b_linears)
+    for g in (128, 64):
+        layers = _pass_layers(device, shapes, nq.FMT_NESTED44, g, 31 + g)
+        out[f"g{g}"] = {"draft_M16": _time_pass(device, layers, 16, False),
+                        "verify_M144": _time_pass(device, layers, 144, True, iters=3)}
+        del layers
+        torch.cuda.empty_cache()
+    return out
+
+
+def config4_sweep(device):
+    """Qwen2.5-7B-shaped linears (28 layers), three tiers of one fp16 base:
+    INT4 g128 draft at M = 1; FP8 (row scale) and FP16 verify at M = k+1."""
+    import torch
+    from quantized_self_speculative_gb300 import nq, synth
+    shapes = _shapes(synth.qwen25_7b_linears)
+    out = {}
+    int4 = _pass_layers(device, shapes, nq.FMT_INT4, 128, 41, w16=True)
+    out["int4_draft_M1"] = _time_pass(device, int4, 1, False)
+    del int4
+    for name, fmt in (("fp8_verify", nq.FMT_FP8E4M3_ROW), ("fp16_verify", nq.FMT_FP16)):
+        layers = _pass_layers(device, shapes, fmt, 0, 41, w16=True)
+        out[name] = {f"k{k}": _time_pass(device, layers, k + 1, True) for k in (2, 4, 6, 8)}
+        del layers
+        torch.cuda.empty_cache()
+    return out
+
+
+def config5_tokens(device, rounds=200):
+    """Acceptance sweep semantics: mean tokens per round vs Eq. (1) at the
+    measured acceptance rate, greedy and sampled (T = 1), B = 64, V = 152064."""
+    import torch
+    from quantized_self_speculative_gb300 import nq
+    B, V = 64, 152064
+    gen = torch.Generator(device=device)
+    out = {}
+    for sigma in (0.3, 1.5):
+        for k in (2, 4, 6, 8):
+            gen.manual_seed(1000 * k + int(sigma * 10))
+            ws = nq.accept_workspace(B, k, V, device)
+            seeds = torch.arange(B, dtype=torch.int64, device=device) + 1000 * k
+            tot_s, acc_pos, tested = 0, 0, 0
+            tot_g = 0
+            for r in range(rounds):
+                tl = torch.randn((B, k + 1, V), generator=gen, device=device).mul_(3.0)
+                dl = (tl[:, :k] + sigma * torch.randn((B, k, V), generator=gen, device=device)).contiguous()
+                p = torch.softmax(dl.double(), -1).view(-1, V)
+                d = torch.multinomial(p, 1, generator=gen).view(B, k).to(torch.int32)
+                _, cnt = nq.accept_sample(d, dl, tl, 1.0, seeds, r, ws=ws)
+                _, cntg = nq.accept_greedy(dl.argmax(-1).to(torch.int32), tl, ws=ws)
+                c = cnt.to(torch.int64)
+                tot_s += int(c.sum())
+                tot_g += int(cntg.sum())
+                acc_pos += int((c - 1).sum())
+                tested += int(torch.minimum(c, torch.full_like(c, k)).sum())
+            alpha = acc_pos / max(1, tested)
+            e1 = (1 - alpha ** (k + 1)) / (1 - alpha) if alpha < 1 else k + 1
+            out[f"sigma{sigma}_k{k}"] = {"alpha_hat": round(alpha, 4),
+                                         "tokens_per_round_sampled": round(tot_s / (rounds * B), 4),
+                                         "eq1_at_alpha_hat": round(e1, 4),
+                                         "tokens_per_round_greedy": round(tot_g / (rounds * B), 4),
+                                         "rounds": rounds * B}
+    return out
+
+
+def profile_case(case, layers=8):
+    """Small fixed workloads for ncu captures: a few launches of one kernel."""
+    import torch
+    from quantized_self_speculative_gb300 import build, nq, synth
+    build.build()
+    device = torch.device("cuda")
+    if case in ("draft", "verify", "draft16", "verify144", "int4", "fp8", "fp16"):
+        spec = synth.llama3_8b_linears if case in ("draft16", "verify144") else (
+            synth.qwen25_7b_linears if case in ("int4", "fp8", "fp16") else synth.llama2_7b_linears)
+        layer, _, _ = spec()
+        shapes = [(n, k) for _ in range(layers) for _, n, k in layer]
+        fmt = {"int4": nq.FMT_INT4, "fp8": nq.FMT_FP8E4M3_ROW, "fp16": nq.FMT_FP16}.get(case, nq.FMT_NESTED44)
+        L = _pass_layers(device, shapes, fmt, 128 if fmt in (nq.FMT_NESTED44, nq.FMT_INT4) else 0, 1)
+        M = {"draft": 1, "verify": 5, "draft16": 16, "verify144": 144, "int4": 1, "fp8": 5, "fp16": 5}[case]
+        print(json.dumps({"case": case, **_time_pass(device, L, M, case not in ("draft", "draft16", "int4"), iters=2)}))
+    else:
+        B, k, V = 64, 4, 152064
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1)
+        tl = torch.randn((B, k + 1, V), generator=gen, device=device).mul_(3.0)
+        dl = (tl[:, :k] + 0.3 * torch.randn((B, k, V), generator=gen, device=device)).contiguous()
+        d = dl.argmax(-1).to(torch.int32)
+        seeds = torch.arange(B, dtype=torch.int64, device=device)
+        ws = nq.accept_workspace(B, k, V)
+        for r in range(4):
+            if case == "greedy":
+                nq.accept_greedy(d, tl, ws=ws)
+            else:
+                nq.accept_sample(d, dl, tl, 1.0, seeds, r, ws=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": case, "B": B, "k": k, "V": V}))
+
+
 # ------------------------------------------------------------------ CPU oracle baseline
 def oracle_sample_step(state):
     """A bounded sample of the round on the CPU oracle: draft (M=1) and verify
@@ -400,9 +558,6 @@ def run_ours(args):
     v_avg = statistics.mean(verify_ms)
     draft_gbs = R.bytes_draft_pass / (d_avg * 1e-3) / 1e9
     verify_gbs = R.bytes_verify / (v_avg * 1e-3) / 1e9
-    extras = {}
-    if not args.no_extras:
-        extras["accept_sweep_B64_V152064"] = accept_sweep(device)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
@@ -426,7 +581,14 @@ def run_ours(args):
                 "h2d_bytes_per_step": R.h2d_bytes, "d2h_bytes_per_step": R.d2h_bytes},
         "gpu_launches": R.launches_per_round * args.steps,
     }
-    line.update(extras)
+    if not args.no_extras:
+        line["accept_sweep_B64_V152064"] = accept_sweep(device)
+    if args.extras == "full":
+        del R
+        torch.cuda.empty_cache()
+        line["config3_llama3_8b_b16_k8"] = config3_sweep(device)
+        line["config4_qwen25_7b_tiers"] = config4_sweep(device)
+        line["config5_tokens_per_round"] = config5_tokens(device)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -441,7 +603,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--extras", choices=["quick", "full"], default="quick",
+                    help="full: also the LLaMA-3-8B (M=16/144), Qwen2.5-7B tier and acceptance-sweep passes")
+    ap.add_argument("--case", default=None,
+                    help="profiling workload: draft|verify|draft16|verify144|int4|fp8|fp16|greedy|sample")
+    ap.add_argument("--layers", type=int, default=8)
     args = ap.parse_args()
+    if args.case:
+        profile_case(args.case, args.layers)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

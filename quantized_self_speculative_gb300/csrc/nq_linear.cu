@@ -8,11 +8,12 @@
 // parents of the same base.
 //
 // Design (GB300, HBM-bound at M <= 16):
-//  * Persistent CTAs walk a flat list of row units over all linears of a
-//    batch, so one launch streams a whole model pass with no inter-kernel gaps.
-//  * Each warp owns 16 output rows and streams them with 128-bit
-//    non-allocating loads, several quantisation groups ahead in a register
-//    ring (each slot is refilled right after it is consumed: no copies).
+//  * One persistent launch streams every linear of a batch (e.g. a whole
+//    model pass): each CTA takes a contiguous, cost-balanced range of 16-row
+//    units, and each warp walks the flat (unit, group) sequence of its rows
+//    with 128-bit non-allocating loads several quantisation groups ahead in a
+//    register ring that continues across unit boundaries (no drain, no copies;
+//    a step costs one compare for unit and segment bookkeeping).
 //  * Dequantisation costs 5 integer ops per 8 weights: a nibble pair masked to
 //    bits 0-3 (or 4-7) of each half and XOR-ed with 8 is, read as an fp16x2,
 //    exactly (code + 8) * 2^-24 (or 16x that) -- fp16 subnormals.  The x16
@@ -25,12 +26,11 @@
 //    short accumulator chains per plane; the scale is applied once per group.
 //  * The K order inside every group is fixed, so an output element is
 //    computed by the same operations whatever M is (batch invariance).
-//  * Activations are staged once per unit in shared memory, converted to
-//    fp16, permuted into operand order and interleaved so that B-fragment
-//    loads are conflict-free.
+//  * Activations are staged in shared memory only when the problem (or the
+//    staged K segment) changes, converted to fp16, permuted into operand
+//    order and interleaved so that B-fragment loads are conflict-free.
 #include <algorithm>
 #include <atomic>
-#include <cstdlib>
 
 #include "nq_internal.cuh"
 
@@ -39,7 +39,12 @@ namespace {
 
 constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
 constexpr int kMaxM = 16;             // activation rows per launch (two 8-column MMA tiles)
-constexpr int kXsMax = 48 * 1024;     // dynamic shared memory cap per CTA
+constexpr int kXsMax = 112 * 1024;    // dynamic shared memory cap per CTA (two CTAs fit one SM)
+// Staging cap of the nibble kernels: the whole activation matrix at M = 1
+// (K <= 11008), segments beyond.  Measured on GB300: a larger buffer shrinks
+// L1 and slows the verify pass (4.5 TB/s at 48 KB, 2.5 TB/s at 112 KB vs 4.9
+// TB/s at 40 KB), a smaller one forces restaging at M = 1.
+constexpr int kXsNib = 40 * 1024;
 
 enum Kind { kNib = 0, kFp8 = 1, kFp16 = 2 };
 
@@ -49,11 +54,13 @@ struct Prob {
     const void *scales;
     const uint16_t *x;
     float *y;
+    long long cost_begin;   // sum over earlier problems of units * k (load balancing)
     int n, k, unit_begin, pad;
 };
 
 template <int MAXP>
 struct Batch {
+    long long total_cost;
     int count, total_units, M, xs_bytes;
     Prob p[MAXP];
 };
@@ -89,14 +96,17 @@ __device__ __forceinline__ void mma_f16_c(float (&d)[4], uint32_t a0, uint32_t a
 // lo16 = (k1, k5) and hi16 = (k3, k7) as 16 (code + 8) * 2^-24.
 struct NibPairs { uint32_t lo1, hi1, lo16, hi16; };
 
+// One XOR turns the eight signed nibbles into offset binary (code + 8); each
+// pair is then a single AND with one immediate.
 __device__ __forceinline__ NibPairs nib_pairs(uint32_t w)
 {
-    const uint32_t w8 = w >> 8;
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t u8 = u >> 8;
     NibPairs r;
-    r.lo1 = (w & 0x000F000Fu) ^ 0x00080008u;
-    r.lo16 = (w & 0x00F000F0u) ^ 0x00800080u;
-    r.hi1 = (w8 & 0x000F000Fu) ^ 0x00080008u;
-    r.hi16 = (w8 & 0x00F000F0u) ^ 0x00800080u;
+    r.lo1 = u & 0x000F000Fu;
+    r.lo16 = u & 0x00F000F0u;
+    r.hi1 = u8 & 0x000F000Fu;
+    r.hi16 = u8 & 0x00F000F0u;
     return r;
 }
 
@@ -117,6 +127,31 @@ struct NibSlot {
     unsigned short s[2];             // fp16 scales of rows g, g+8
 };
 
+// First unit whose cost-prefix is >= target (units of one problem cost K each).
+template <int MAXP>
+__device__ __forceinline__ int unit_at_cost(const Batch<MAXP> &B, long long target)
+{
+    if (target >= B.total_cost) return B.total_units;
+    int lo = 0, hi = B.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (B.p[mid].cost_begin <= target) lo = mid; else hi = mid - 1;
+    }
+    const Prob &P = B.p[lo];
+    const long long off = target - P.cost_begin;
+    return P.unit_begin + static_cast<int>((off + P.k - 1) / P.k);
+}
+
+template <int MAXP>
+__device__ __forceinline__ int units_of(const Batch<MAXP> &B, int pi)
+{
+    return (pi + 1 < B.count ? B.p[pi + 1].unit_begin : B.total_units) - B.p[pi].unit_begin;
+}
+
+// Each CTA streams a contiguous, cost-balanced range of row units; every warp
+// walks the flat (unit, group) sequence of its 16 rows with a prefetch ring
+// that continues across unit boundaries.  Activations are restaged only when
+// the problem (or the staged K segment) changes.
 template <int PLANES, int G, int NT, int WARPS, int MAXP>
 __global__ void __launch_bounds__(WARPS * 32)
 nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
@@ -136,180 +171,249 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
 
-    for (int u = blockIdx.x; u < B.total_units; u += gridDim.x) {
-        const Prob &P = B.p[find_problem(B, u)];
-        const int N = P.n, K = P.k, NG = K / G;
-        const int rg = (u - P.unit_begin) * ROWS + warp * 16 + g, rg8 = rg + 8;
-        const bool vg = rg < N, vg8 = rg8 < N;
-        const size_t rowb = static_cast<size_t>(K) / 2;
-        const uint8_t *pw[PLANES][2];
-        pw[0][0] = P.base + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t;
-        pw[0][1] = P.base + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t;
+    const int ub = unit_at_cost(B, B.total_cost * blockIdx.x / gridDim.x);
+    const int ue = unit_at_cost(B, B.total_cost * (blockIdx.x + 1) / gridDim.x);
+    if (ub >= ue) return;
+
+    // total steps (groups) of this CTA's range
+    int first_pi = find_problem(B, ub);
+    long long steps_ll = 0;
+    for (int pi = first_pi; pi < B.count && B.p[pi].unit_begin < ue; ++pi) {
+        const int a = max(ub, B.p[pi].unit_begin), b = min(ue, B.p[pi].unit_begin + units_of(B, pi));
+        steps_ll += static_cast<long long>(b - a) * (B.p[pi].k / G);
+    }
+    const int steps = static_cast<int>(steps_ll);
+
+    // ---- load cursor (runs R-1 steps ahead of the compute cursor)
+    int l_u = ub, l_pi = first_pi, l_c = 0, l_ng = 0;
+    const uint8_t *lw[PLANES][2];
+    const unsigned short *ls[2];
+    auto l_setup = [&]() {
+        const Prob &P = B.p[l_pi];
+        const int N = P.n;
+        l_ng = P.k / G;
+        const size_t rowb = static_cast<size_t>(P.k) / 2;
+        const int rg = (l_u - P.unit_begin) * ROWS + warp * 16 + g;
+        const int r0 = rg < N ? rg : 0, r1 = rg + 8 < N ? rg + 8 : 0;
+        lw[0][0] = P.base + static_cast<size_t>(r0) * rowb + VB * t;
+        lw[0][1] = P.base + static_cast<size_t>(r1) * rowb + VB * t;
         if constexpr (PLANES == 2) {
-            pw[1][0] = P.resid + static_cast<size_t>(vg ? rg : 0) * rowb + VB * t;
-            pw[1][1] = P.resid + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + VB * t;
+            lw[1][0] = P.resid + static_cast<size_t>(r0) * rowb + VB * t;
+            lw[1][1] = P.resid + static_cast<size_t>(r1) * rowb + VB * t;
         }
-        const unsigned short *ps0 = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg ? rg : 0) * NG;
-        const unsigned short *ps1 = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(vg8 ? rg8 : 0) * NG;
-
-        auto load = [&](NibSlot<PLANES, G> &S, int c) {
+        ls[0] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r0) * l_ng;
+        ls[1] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r1) * l_ng;
+    };
+    auto issue = [&](NibSlot<PLANES, G> &S) {
+        const size_t off = static_cast<size_t>(l_c) * (G / 2);
 #pragma unroll
-            for (int p = 0; p < PLANES; ++p)
+        for (int p = 0; p < PLANES; ++p)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if constexpr (VB == 16) {
-                        const uint4 v = ld_stream_v4(pw[p][r] + static_cast<size_t>(c) * (G / 2));
-                        S.w[p][r][0] = v.x; S.w[p][r][1] = v.y; S.w[p][r][2] = v.z; S.w[p][r][3] = v.w;
-                    } else {
-                        const uint2 v = ld_stream_v2(pw[p][r] + static_cast<size_t>(c) * (G / 2));
-                        S.w[p][r][0] = v.x; S.w[p][r][1] = v.y;
-                    }
-                }
-            S.s[0] = ld_nc_u16(ps0 + c);
-            S.s[1] = ld_nc_u16(ps1 + c);
-        };
-
-        // groups per staged activation segment (a multiple of R unless all of K fits)
-        int cps = (B.xs_bytes - M * kRowPad) / (M * CHB + MT * 4);
-        if (cps >= NG) cps = NG;
-        else cps = max(R, cps / R * R);
-        const int RS = cps * CHB + kRowPad;
-        unsigned char *xs = smem;
-        float *corr = reinterpret_cast<float *>(smem + M * RS);
-
-        NibSlot<PLANES, G> ring[R];
-#pragma unroll
-        for (int i = 0; i < R - 1; ++i)
-            if (i < NG) load(ring[i], i);
-
-        // Stage activations of groups [c_begin, c_begin + cps): fp16, operand
-        // order (x0,x4)(x2,x6)(x1/16,x5/16)(x3/16,x7/16) per 8 inputs, plus
-        // the offset correction -8 * 2^-24 * sum(x) per (group, row).
-        auto stage = [&](int c_begin) {
-            const int nch = min(cps, NG - c_begin);
-            const int items_row = nch * (G / 8);
-            const int total = M * items_row;
-            const int total_pad = (total + THREADS - 1) / THREADS * THREADS;
-            bool range = false;
-            for (int i = threadIdx.x; i < total_pad; i += THREADS) {
-                const bool valid = i < total;
-                const int m = valid ? i / items_row : 0, it = valid ? i % items_row : 0;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (valid)
-                    v = *reinterpret_cast<const uint4 *>(P.x + static_cast<size_t>(m) * K +
-                                                         static_cast<size_t>(c_begin) * G + it * 8);
-                const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-                const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-                const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
-                const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
-                uint4 o;
-                o.x = pack_h2(x0, x4);
-                o.y = pack_h2(x2, x6);
-                o.z = pack_h2(__fmul_rn(x1, 0.0625f), __fmul_rn(x5, 0.0625f));
-                o.w = pack_h2(__fmul_rn(x3, 0.0625f), __fmul_rn(x7, 0.0625f));
-                const float amax = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
-                                         fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
-                range |= amax > 65504.0f;
-                const int cl = it / (G / 8), kk = (it % (G / 8)) * 8;
-                const int tl = kk / (2 * VB), wd = (kk % (2 * VB)) / 8;
-                if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
-                // sum of the staged values as the MMA sees them: x~ at even k, 16 * (x/16)~ at odd k
-                const float se = __fadd_rn(__fadd_rn(h_lo(o.x), h_hi(o.x)), __fadd_rn(h_lo(o.y), h_hi(o.y)));
-                const float so = __fadd_rn(__fadd_rn(h_lo(o.z), h_hi(o.z)), __fadd_rn(h_lo(o.w), h_hi(o.w)));
-                float s = __fmaf_rn(16.0f, so, se);
-#pragma unroll
-                for (int o2 = 1; o2 < G / 8; o2 <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o2));
-                if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(kNeg8Ulp, s);
-            }
-            for (int i = threadIdx.x; i < nch * (MT - M); i += THREADS)
-                corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
-            if (range) set_status(status, NQ_DEV_ACT_RANGE);
-        };
-
-        __syncthreads();   // the previous unit is done with shared memory
-        stage(0);
-        __syncthreads();
-
-        // per-lane activation rows: rows >= M read a zero-stride dummy (their
-        // columns are never stored)
-        const unsigned char *xrow[NT];
-        int xstep[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int m = nt * 8 + g;
-            xrow[nt] = xs + (m < M ? m : 0) * RS + t * 16;
-            xstep[nt] = m < M ? CHB : 0;
-        }
-
-        float y[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) y[nt][i] = 0.0f;
-
-        for (int c0 = 0; c0 < NG; c0 += R) {
-            if (c0 > 0 && c0 % cps == 0) {
-                __syncthreads();
-                stage(c0);
-                __syncthreads();
-            }
-            const int cbase = c0 % cps;
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int c = c0 + i;
-                if (c < NG) {
-                    if (c + R - 1 < NG) load(ring[(i + R - 1) % R], c + R - 1);
-                    const NibSlot<PLANES, G> &S = ring[i];
-                    const int cl = cbase + i;
-                    float accA[NT][PLANES][4], accB[NT][PLANES][4];
-#pragma unroll
-                    for (int wd = 0; wd < WORDS; ++wd) {
-                        uint4 bq[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt] + wd * 64);
-#pragma unroll
-                        for (int p = 0; p < PLANES; ++p) {
-                            const NibPairs a = nib_pairs(S.w[p][0][wd]), b = nib_pairs(S.w[p][1][wd]);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                if (wd == 0) {
-                                    const float2 cc = *reinterpret_cast<const float2 *>(corr + cl * MT + nt * 8 + 2 * t);
-                                    mma_f16_c(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y, cc.x, cc.y, cc.x, cc.y);
-                                    mma_f16_c(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w, 0.f, 0.f, 0.f, 0.f);
-                                } else {
-                                    mma_f16(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y);
-                                    mma_f16(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w);
-                                }
-                            }
-                        }
-                    }
-                    // group scale x 2^24 (undoes the subnormal encoding); refinement plane at s/16
-                    const float s0 = __fmul_rn(__half2float(__ushort_as_half(S.s[0])), 16777216.0f);
-                    const float s1 = __fmul_rn(__half2float(__ushort_as_half(S.s[1])), 16777216.0f);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float sc = e < 2 ? s0 : s1;
-                            y[nt][e] = __fmaf_rn(sc, __fadd_rn(accA[nt][0][e], accB[nt][0][e]), y[nt][e]);
-                            if constexpr (PLANES == 2)
-                                y[nt][e] = __fmaf_rn(__fmul_rn(sc, 0.0625f), __fadd_rn(accA[nt][1][e], accB[nt][1][e]), y[nt][e]);
-                        }
-                    }
+            for (int r = 0; r < 2; ++r) {
+                if constexpr (VB == 16) {
+                    const uint4 v = ld_stream_v4(lw[p][r] + off);
+                    S.w[p][r][0] = v.x; S.w[p][r][1] = v.y; S.w[p][r][2] = v.z; S.w[p][r][3] = v.w;
+                } else {
+                    const uint2 v = ld_stream_v2(lw[p][r] + off);
+                    S.w[p][r][0] = v.x; S.w[p][r][1] = v.y;
                 }
             }
+        S.s[0] = ld_nc_u16(ls[0] + l_c);
+        S.s[1] = ld_nc_u16(ls[1] + l_c);
+        if (++l_c == l_ng) {
+            l_c = 0;
+            if (++l_u < ue) {
+                if (l_pi + 1 < B.count && l_u >= B.p[l_pi + 1].unit_begin) ++l_pi;
+                l_setup();
+            }
         }
+    };
 
+    // ---- compute cursor: the next group to compute is (c_u, c_grp); an
+    // "event" (unit end / unit start / new activation segment) happens when
+    // c_grp reaches seg_end, so a step costs one compare.
+    int c_u = ub, c_pi = first_pi, c_grp = 0, seg_end = 0;
+    int c_N = 0, c_ng = 0, c_K = 0, c_rg = 0;
+    bool in_unit = false;
+    int staged_pi = -1, staged_begin = -1, cps = 1, RS = 0;
+    const uint16_t *c_x = nullptr;
+    float *c_y = nullptr;
+    unsigned char *xs = smem;
+    float *corr = reinterpret_cast<float *>(smem);
+
+    // Stage activations of groups [c_begin, c_begin + nch) of the compute
+    // cursor's problem: fp16, operand order (x0,x4)(x2,x6)(x1/16,x5/16)
+    // (x3/16,x7/16) per 8 inputs, plus the offset correction -8 * 2^-24 *
+    // sum(x) per (group, row).
+    auto stage = [&](int c_begin, int nch) {
+        const int items_row = nch * (G / 8);
+        const int total = M * items_row;
+        const int total_pad = (total + THREADS - 1) / THREADS * THREADS;
+        bool range = false;
+        for (int i = threadIdx.x; i < total_pad; i += THREADS) {
+            const bool valid = i < total;
+            const int m = valid ? i / items_row : 0, it = valid ? i % items_row : 0;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (valid)
+                v = *reinterpret_cast<const uint4 *>(c_x + static_cast<size_t>(m) * c_K +
+                                                     static_cast<size_t>(c_begin) * G + it * 8);
+            const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+            const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+            const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
+            const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
+            uint4 o;
+            o.x = pack_h2(x0, x4);
+            o.y = pack_h2(x2, x6);
+            o.z = pack_h2(__fmul_rn(x1, 0.0625f), __fmul_rn(x5, 0.0625f));
+            o.w = pack_h2(__fmul_rn(x3, 0.0625f), __fmul_rn(x7, 0.0625f));
+            const float amax = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
+                                     fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
+            range |= amax > 65504.0f;
+            const int cl = it / (G / 8), kk = (it % (G / 8)) * 8;
+            const int tl = kk / (2 * VB), wd = (kk % (2 * VB)) / 8;
+            if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
+            // sum of the staged values as the MMA sees them: x~ at even k, 16 * (x/16)~ at odd k
+            const float se = __fadd_rn(__fadd_rn(h_lo(o.x), h_hi(o.x)), __fadd_rn(h_lo(o.y), h_hi(o.y)));
+            const float so = __fadd_rn(__fadd_rn(h_lo(o.z), h_hi(o.z)), __fadd_rn(h_lo(o.w), h_hi(o.w)));
+            float sum = __fmaf_rn(16.0f, so, se);
+#pragma unroll
+            for (int o2 = 1; o2 < G / 8; o2 <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o2));
+            if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(kNeg8Ulp, sum);
+        }
+        for (int i = threadIdx.x; i < nch * (MT - M); i += THREADS)
+            corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
+        if (range) set_status(status, NQ_DEV_ACT_RANGE);
+    };
+
+    const unsigned char *xrow[NT];   // row base of each 8-column tile in the staged segment
+    int xstep[NT];
+    const unsigned char *xp[NT];     // current group
+    const float *cp = corr;          // current group's offset corrections
+    float y[NT][4];
+
+    auto store_unit = [&]() {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int m = nt * 8 + 2 * t + (e & 1);
-                const bool top = e < 2;
-                if (m < M && (top ? vg : vg8)) P.y[static_cast<size_t>(m) * N + (top ? rg : rg8)] = y[nt][e];
+                const int row = e < 2 ? c_rg : c_rg + 8;
+                if (m < M && row < c_N) c_y[static_cast<size_t>(m) * c_N + row] = y[nt][e];
+            }
+        }
+    };
+
+    auto event = [&]() {
+        if (in_unit && c_grp == c_ng) {
+            store_unit();
+            in_unit = false;
+            ++c_u;
+            if (c_pi + 1 < B.count && c_u >= B.p[c_pi + 1].unit_begin) ++c_pi;
+        }
+        if (!in_unit) {
+            const Prob &P = B.p[c_pi];
+            c_N = P.n; c_K = P.k; c_ng = c_K / G; c_x = P.x; c_y = P.y;
+            c_rg = (c_u - P.unit_begin) * ROWS + warp * 16 + g;
+            c_grp = 0;
+            in_unit = true;
+            if (staged_pi != c_pi) {
+                cps = (B.xs_bytes - M * kRowPad) / (M * CHB + MT * 4);
+                cps = cps >= c_ng ? c_ng : max(1, cps);
+                RS = cps * CHB + kRowPad;
+                corr = reinterpret_cast<float *>(smem + M * RS);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int m = nt * 8 + g;
+                    xrow[nt] = xs + (m < M ? m : 0) * RS + t * 16;
+                    xstep[nt] = m < M ? CHB : 0;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[nt][e] = 0.0f;
+        }
+        seg_end = min(c_ng, c_grp + cps);
+        if (staged_pi != c_pi || staged_begin != c_grp) {
+            __syncthreads();
+            stage(c_grp, seg_end - c_grp);
+            __syncthreads();
+            staged_pi = c_pi;
+            staged_begin = c_grp;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xp[nt] = xrow[nt];
+        cp = corr + 2 * t;
+    };
+
+    // one quantisation group of this warp's 16 rows
+    auto compute = [&](const NibSlot<PLANES, G> &S) {
+        if (c_grp == seg_end) event();
+        float accA[NT][PLANES][4], accB[NT][PLANES][4];
+#pragma unroll
+        for (int wd = 0; wd < WORDS; ++wd) {
+            uint4 bq[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xp[nt] + wd * 64);
+#pragma unroll
+            for (int p = 0; p < PLANES; ++p) {
+                const NibPairs a = nib_pairs(S.w[p][0][wd]), b = nib_pairs(S.w[p][1][wd]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (wd == 0) {
+                        const float2 cc = *reinterpret_cast<const float2 *>(cp + nt * 8);
+                        mma_f16_c(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y, cc.x, cc.y, cc.x, cc.y);
+                        mma_f16_c(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w, 0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        mma_f16(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y);
+                        mma_f16(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w);
+                    }
+                }
+            }
+        }
+        // group scale x 2^24 (undoes the subnormal encoding); refinement plane at s/16
+        const float s0f = __fmul_rn(__half2float(__ushort_as_half(S.s[0])), 16777216.0f);
+        const float s1f = __fmul_rn(__half2float(__ushort_as_half(S.s[1])), 16777216.0f);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float sc = e < 2 ? s0f : s1f;
+                y[nt][e] = __fmaf_rn(sc, __fadd_rn(accA[nt][0][e], accB[nt][0][e]), y[nt][e]);
+                if constexpr (PLANES == 2)
+                    y[nt][e] = __fmaf_rn(__fmul_rn(sc, 0.0625f), __fadd_rn(accA[nt][1][e], accB[nt][1][e]), y[nt][e]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xp[nt] += xstep[nt];
+        cp += MT;
+        ++c_grp;
+    };
+
+    NibSlot<PLANES, G> ring[R];
+    l_setup();
+#pragma unroll
+    for (int i = 0; i < R - 1; ++i)
+        if (i < steps) issue(ring[i]);
+
+    int s0 = 0;
+    for (; s0 + 2 * R - 2 < steps; s0 += R) {     // every load of the block is in range
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            issue(ring[(i + R - 1) % R]);
+            compute(ring[i]);
+        }
+    }
+    for (; s0 < steps; s0 += R) {                  // tail
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if (s0 + i < steps) {
+                if (s0 + i + R - 1 < steps) issue(ring[(i + R - 1) % R]);
+                compute(ring[i]);
             }
         }
     }
+    if (in_unit) store_unit();
 }
 
 // ------------------------------------------------------------------ FP8 / FP16 tier kernel
@@ -496,11 +600,24 @@ int cached_occupancy(F kernel, int threads, int smem, std::atomic<int> (&cache)[
     return o;
 }
 
+// Opt a kernel into the large dynamic shared memory size, once per process.
+template <typename F>
+cudaError_t allow_large_smem(F kernel, std::atomic<int> &done)
+{
+    if (done.load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXsMax);
+    if (e == cudaSuccess) done.store(1, std::memory_order_release);
+    return e;
+}
+
 template <int PLANES, int G, int NT, int WARPS, int MAXP>
 cudaError_t launch_nib(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
 {
     auto k = nib_kernel<PLANES, G, NT, WARPS, MAXP>;
+    static std::atomic<int> attr{0};
     static std::atomic<int> occ[kXsMax / 1024 + 1];
+    const cudaError_t e = allow_large_smem(k, attr);
+    if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(b.total_units, sm_count() * cached_occupancy(k, WARPS * 32, b.xs_bytes, occ)));
     k<<<grid, WARPS * 32, b.xs_bytes, s>>>(b, status);
     return cudaGetLastError();
@@ -510,7 +627,10 @@ template <int KIND, int NT, int MAXP>
 cudaError_t launch_fp(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
 {
     auto k = fp_kernel<KIND, NT, MAXP>;
+    static std::atomic<int> attr{0};
     static std::atomic<int> occ[kXsMax / 1024 + 1];
+    const cudaError_t e = allow_large_smem(k, attr);
+    if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(b.total_units, sm_count() * cached_occupancy(k, kFpWarps * 32, b.xs_bytes, occ)));
     k<<<grid, kFpWarps * 32, b.xs_bytes, s>>>(b, status);
     return cudaGetLastError();
@@ -562,17 +682,6 @@ nq_status check_layer(const nq_weights &w, bool verify, int &kind, int &planes)
     return NQ_OK;
 }
 
-// Tuning override of the CTA width of batched nibble launches (NQ_LINEAR_WARPS = 4 or 8).
-int linear_warps_override()
-{
-    static const int v = [] {
-        const char *e = std::getenv("NQ_LINEAR_WARPS");
-        const int w = e ? std::atoi(e) : 0;
-        return (w == 4 || w == 8) ? w : 0;
-    }();
-    return v;
-}
-
 // Dynamic shared memory for a launch: all activation rows of the widest layer
 // (in fp16, padded rows, plus offset corrections), capped at kXsMax.
 int xs_bytes_for(int kind, int M, int kmax, int group)
@@ -582,7 +691,7 @@ int xs_bytes_for(int kind, int M, int kmax, int group)
     const int mt = M > 8 ? 16 : 8;
     const long long need = static_cast<long long>(M) * (chunks * 2 * ch + kRowPad) +
                            (kind == kNib ? static_cast<long long>(chunks) * mt * 4 : 0);
-    return static_cast<int>(std::min<long long>(need, kXsMax));
+    return static_cast<int>(std::min<long long>(need, kind == kNib ? kXsNib : kXsMax));
 }
 
 template <int MAXP>
@@ -603,10 +712,9 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
                 rows16 += (w[i0 + i].n_out + 15) / 16;
             }
             // 8-warp units when there are enough of them to fill the GPU twice
-            int warps = (kind == kNib && MAXP == kLargeBatch && rows16 / 8 >= 2LL * sm_count()) ? 8 : 4;
-            if (kind == kNib && MAXP == kLargeBatch && linear_warps_override() != 0) warps = linear_warps_override();
+            const int warps = (kind == kNib && MAXP == kLargeBatch && rows16 / 8 >= 2LL * sm_count()) ? 8 : 4;
             const int rows_per_unit = kind == kNib ? 16 * warps : 16 * kFpWarps;
-            long long units = 0;
+            long long units = 0, cost = 0;
             for (int i = 0; i < cnt; ++i) {
                 const nq_weights &L = w[i0 + i];
                 Prob &p = b.p[i];
@@ -618,10 +726,14 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
                 p.n = L.n_out;
                 p.k = L.k_in;
                 p.unit_begin = static_cast<int>(units);
+                p.cost_begin = cost;
                 p.pad = 0;
-                units += (L.n_out + rows_per_unit - 1) / rows_per_unit;
+                const long long nu = (L.n_out + rows_per_unit - 1) / rows_per_unit;
+                units += nu;
+                cost += nu * L.k_in;
             }
             if (units > 0x7fffffffLL) return NQ_ERR_SHAPE;
+            b.total_cost = cost;
             b.count = cnt;
             b.total_units = static_cast<int>(units);
             b.M = Mc;
