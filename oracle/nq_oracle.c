@@ -378,12 +378,18 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  * on the same fp32 values, computed by this fixed recipe:
  *
  *   c      = fp32(log2(e)) / T                       (IEEE division)
- *   leaf   = 16 consecutive vocabulary entries; mx = max raw logit of the leaf
+ *   leaf   = the vocabulary is cut into blocks of 16384 entries of 1024
+ *            leaves; leaf 4T + q (T = 0..255, q = 0..3) of block b holds the
+ *            16 entries b*16384 + 4096*q + 1024*r + 4*T + j (r, j = 0..3) in
+ *            that (r, j) order -- thread T of a 256-thread block reads its four
+ *            consecutive leaves with sixteen coalesced 16-byte loads -- and has
+ *            global index 1024*b + 4T + q; entries >= V are absent, a leaf with
+ *            none is a pad; mx = max raw logit of the leaf
  *   mz     = RN(mx * c);  t(x) = fma(l(x), c, -mz)    (base-2 exponent, <= ~0)
  *   e2(t)  = 0 if t < -125, else P(f) * 2^n with n = rint(t), f = t - n and
  *            P the degree-6 Taylor polynomial of 2^f (coefficients
  *            RN(ln2^i / i!)), evaluated by Horner with fma
- *   leaf s = serial fp32 sum, in index order, of e2(t(x))
+ *   leaf s = serial fp32 sum, in leaf order, of e2(t(x))
  *   merge  (m1,s1),(m2,s2): the larger m survives; s = fma(s_small,
  *            e2(m_small - m_large), s_large); a (-inf, 0) pad is the identity
  *   valid  = every logit finite and every leaf's mz finite (a logit whose
@@ -444,19 +450,36 @@ static ms_t ms_merge(ms_t a, ms_t b)
     return r;
 }
 
-static int n_leaves(int V) { return (V + ORC_LEAF - 1) / ORC_LEAF; }
+#define ORC_BLOCK 16384
+
+/* Number of leaf slots (1024 per 16384-entry block) and the entry held at
+ * position e (0..15) of leaf i; -1 if that entry lies at or beyond V. */
+static int n_leaves(int V) { return 1024 * ((V + ORC_BLOCK - 1) / ORC_BLOCK); }
+static int leaf_entry(int V, int i, int e)
+{
+    int blk = i / 1024, T = (i % 1024) / 4, q = i % 4;
+    int x = blk * ORC_BLOCK + 4096 * q + 1024 * (e / 4) + 4 * T + (e % 4);
+    return x < V ? x : -1;
+}
 static int pow2_at_least(int n) { int p = 1; while (p < n) p *= 2; return p; }
 
-/* Per-leaf (mz, s) for one logits vector; returns the number of leaves. */
+/* Per-leaf (mz, s) for one logits vector; returns the number of leaf slots. */
 static int leaf_stats(const float *l, int V, float c, ms_t *leaf)
 {
     int L = n_leaves(V);
     for (int i = 0; i < L; i++) {
-        int x0 = i * ORC_LEAF, x1 = x0 + ORC_LEAF < V ? x0 + ORC_LEAF : V;
-        float mx = l[x0];
-        for (int x = x0 + 1; x < x1; x++) if (l[x] > mx) mx = l[x];
+        float mx = -INFINITY;
+        int any = 0;
+        for (int e = 0; e < ORC_LEAF; e++) {
+            int x = leaf_entry(V, i, e);
+            if (x >= 0 && (!any || l[x] > mx)) { mx = l[x]; any = 1; }
+        }
+        if (!any) { leaf[i].m = -INFINITY; leaf[i].s = 0.0f; continue; }
         float mz = mx * c, s = 0.0f;
-        for (int x = x0; x < x1; x++) s = s + orc_exp2c(fmaf(l[x], c, -mz));
+        for (int e = 0; e < ORC_LEAF; e++) {
+            int x = leaf_entry(V, i, e);
+            if (x >= 0) s = s + orc_exp2c(fmaf(l[x], c, -mz));
+        }
         leaf[i].m = mz; leaf[i].s = s;
     }
     return L;
@@ -485,13 +508,17 @@ int orc_softmax_canonical(const float *l, int V, float T, float *p)
     for (int x = 0; x < V; x++) if (!isfinite(l[x])) return -1;
     ms_t *leaf = malloc(sizeof(ms_t) * n_leaves(V));
     int L = leaf_stats(l, V, c, leaf);
-    for (int i = 0; i < L; i++) if (!isfinite(leaf[i].m)) { free(leaf); return -1; }
+    for (int i = 0; i < L; i++)
+        if (leaf_entry(V, i, 0) >= 0 && !isfinite(leaf[i].m)) { free(leaf); return -1; }
     ms_t root = ms_tree(leaf, L);
     float inv_s = 1.0f / root.s;
     for (int i = 0; i < L; i++) {
+        if (leaf_entry(V, i, 0) < 0) continue;
         float F = orc_exp2c(leaf[i].m - root.m) * inv_s;
-        int x0 = i * ORC_LEAF, x1 = x0 + ORC_LEAF < V ? x0 + ORC_LEAF : V;
-        for (int x = x0; x < x1; x++) p[x] = orc_exp2c(fmaf(l[x], c, -leaf[i].m)) * F;
+        for (int e = 0; e < ORC_LEAF; e++) {
+            int x = leaf_entry(V, i, e);
+            if (x >= 0) p[x] = orc_exp2c(fmaf(l[x], c, -leaf[i].m)) * F;
+        }
     }
     free(leaf);
     return 0;
@@ -509,7 +536,10 @@ int orc_tree_sample(const float *w, int V, float u)
     for (int l = 0; l <= levels; l++) level[l] = calloc((size_t)(P >> l), sizeof(float));
     for (int i = 0; i < L; i++) {
         float s = 0.0f;
-        for (int x = i * ORC_LEAF; x < (i + 1) * ORC_LEAF && x < V; x++) s = s + w[x];
+        for (int e = 0; e < ORC_LEAF; e++) {
+            int x = leaf_entry(V, i, e);
+            if (x >= 0) s = s + w[x];
+        }
         level[0][i] = s;
     }
     for (int l = 1; l <= levels; l++)
@@ -525,13 +555,16 @@ int orc_tree_sample(const float *w, int V, float u)
             else { t = t - left; node = 2 * node + 1; }
         }
         float run = 0.0f;
-        int x0 = node * ORC_LEAF, x1 = x0 + ORC_LEAF < V ? x0 + ORC_LEAF : V;
-        for (int x = x0; x < x1 && result < 0; x++) {
+        for (int e = 0; e < ORC_LEAF && result < 0; e++) {
+            int x = leaf_entry(V, node, e);
+            if (x < 0) continue;
             run = run + w[x];
             if (t < run) result = x;
         }
-        for (int x = x1 - 1; x >= x0 && result < 0; x--)
-            if (w[x] > 0.0f) result = x;
+        for (int e = ORC_LEAF - 1; e >= 0 && result < 0; e--) {
+            int x = leaf_entry(V, node, e);
+            if (x >= 0 && w[x] > 0.0f) result = x;
+        }
     }
     for (int l = 0; l <= levels; l++) free(level[l]);
     free(level);
@@ -599,23 +632,30 @@ static void softmax_f64(const float *l, int V, double T, double *p)
     for (int x = 0; x < V; x++) p[x] /= s;
 }
 
+/* Inverse CDF in fp64, walking the entries in the recipe's leaf order. */
 static int cdf_sample_f64(const double *w, int V, double u, double *margin)
 {
+    int L = n_leaves(V);
     double tot = 0.0;
     for (int x = 0; x < V; x++) tot += w[x];
     if (!(tot > 0.0)) return -1;
     double t = u * tot, run = 0.0;
-    int pick = -1;
-    for (int x = 0; x < V; x++) {
-        double prev = run;
-        run += w[x];
-        if (w[x] > 0.0 && pick < 0 && t < run) {
-            pick = x;
-            double d0 = (t - prev) / tot, d1 = (run - t) / tot;
-            *margin = d0 < d1 ? d0 : d1;
+    int pick = -1, last = -1;
+    for (int i = 0; i < L; i++) {
+        for (int e = 0; e < ORC_LEAF; e++) {
+            int x = leaf_entry(V, i, e);
+            if (x < 0) continue;
+            double prev = run;
+            run += w[x];
+            if (w[x] > 0.0) last = x;
+            if (w[x] > 0.0 && pick < 0 && t < run) {
+                pick = x;
+                double d0 = (t - prev) / tot, d1 = (run - t) / tot;
+                *margin = d0 < d1 ? d0 : d1;
+            }
         }
     }
-    if (pick < 0) { for (int x = V - 1; x >= 0; x--) if (w[x] > 0.0) { pick = x; break; } *margin = 0.0; }
+    if (pick < 0) { pick = last; *margin = 0.0; }
     return pick;
 }
 

@@ -25,12 +25,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLeaf = 16;
-constexpr int kChunk = kThreads * kLeaf;     // vocabulary entries per CTA
+constexpr int kChunk = kThreads * kLeaf;     // vocabulary entries per greedy CTA
 constexpr int kMaxChunks = 128;              // V <= 524288
+constexpr int kBlock = 4 * kChunk;           // vocabulary entries per sampling CTA (1024 leaves)
+constexpr int kMaxBlocks = kMaxChunks / 4;   // 32
 constexpr int kMaxK = 16;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 inline int n_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+inline int n_blocks(int V) { return (V + kBlock - 1) / kBlock; }
 inline size_t counters_bytes(int B) { return (static_cast<size_t>(B) * 4 + 255) / 256 * 256; }
 
 // ------------------------------------------------------------------ greedy
@@ -134,43 +137,83 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 }
 
 // ------------------------------------------------------------------ sampled
+//
+// Leaves of the recipe: the vocabulary is cut into blocks of 16384 entries of
+// 1024 leaves; leaf 4T + q (T = 0..255, q = 0..3) of block b holds the entries
+// b*16384 + 4096*q + 1024*r + 4*T + j (r, j = 0..3), in (r, j) order, and has
+// global index 1024*b + 4T + q.  Thread T of a 256-thread CTA owns the four
+// consecutive leaves 4T..4T+3 of a block and reads them with sixteen coalesced
+// 16-byte loads.  Absent entries (>= V) are read as -inf: they cannot raise a
+// maximum and contribute an exact zero to every sum.
 
-// Load the (up to) 16 logits of leaf L of a vector; entries past V are -inf.
-__device__ __forceinline__ void load_leaf(const float *vec, int V, int L, float (&l)[kLeaf])
+struct SampleRec {      // per-row decision, written by pass A, read by pass B
+    int js;             // first rejected position, or k if all accepted
+    int resid;          // 1: draw from max(0, p_js - q_js); 0: draw from p_js
+    float u;            // the draw's uniform
+    float Mp, invSp, Mq, invSq;
+    int pad;
+};
+
+// Workspace layout shared by the greedy and sampled calls.
+struct WsLayout {
+    size_t counters_a, counters_b, part, rec, csum, lsum, total;
+};
+
+inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Every section starts on a 256-byte boundary (the kernels use 16-byte
+// vector accesses on some of them).
+inline WsLayout ws_layout(int B, int k, int V)
 {
-    const int x0 = L * kLeaf;
-    if ((V & 3) == 0 && x0 + kLeaf <= V) {
-        const float4 *p = reinterpret_cast<const float4 *>(vec + x0);
+    const size_t C = static_cast<size_t>(n_chunks(V));   // greedy partials per vector (>= blocks)
+    const size_t NB = static_cast<size_t>(n_blocks(V));
+    WsLayout L;
+    L.counters_a = 0;
+    L.counters_b = align256(static_cast<size_t>(B) * 4);
+    L.part = L.counters_b + align256(static_cast<size_t>(B) * 4);
+    L.rec = L.part + align256(static_cast<size_t>(B) * (2 * k + 1) * C * sizeof(float2));
+    L.csum = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));
+    L.lsum = L.csum + align256(static_cast<size_t>(B) * NB * sizeof(float));
+    L.total = L.lsum + static_cast<size_t>(B) * NB * 4 * kThreads * sizeof(float);
+    return L;
+}
+
+__device__ __forceinline__ int leaf_entry(int blk, int T, int q, int e)
+{
+    return blk * kBlock + 4096 * q + 1024 * (e >> 2) + 4 * T + (e & 3);
+}
+
+// Leaf (blk, 4T + q); `full` means the whole block lies inside [0, V).
+__device__ __forceinline__ void load_leaf(const float *vec, int V, bool full, int blk, int T, int q, float (&l)[kLeaf])
+{
+    const int base = leaf_entry(blk, T, q, 0);
+    if (full) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = __ldcg(p + q);
-            l[4 * q] = v.x; l[4 * q + 1] = v.y; l[4 * q + 2] = v.z; l[4 * q + 3] = v.w;
+        for (int r = 0; r < 4; ++r) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(vec + base + 1024 * r));
+            l[4 * r] = v.x; l[4 * r + 1] = v.y; l[4 * r + 2] = v.z; l[4 * r + 3] = v.w;
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < kLeaf; ++e) l[e] = x0 + e < V ? __ldcg(vec + x0 + e) : -INFINITY;
+        for (int e = 0; e < kLeaf; ++e) {
+            const int x = base + 1024 * (e >> 2) + (e & 3);
+            l[e] = x < V ? __ldcg(vec + x) : -INFINITY;
+        }
     }
 }
 
-// Leaf statistics of the recipe: raw max -> mz = RN(max * c); s = serial sum
-// of exp2(fma(l, c, -mz)).  Returns (-inf, 0) for a leaf wholly past V.
-__device__ __forceinline__ MaxSum leaf_stats(const float (&l)[kLeaf], int n_valid, float c, float &finite)
+__device__ __forceinline__ bool block_full(int V, int blk) { return (V & 3) == 0 && (blk + 1) * kBlock <= V; }
+
+// (mz, s) of a leaf with at least one present entry.
+__device__ __forceinline__ MaxSum leaf_ms(const float (&l)[kLeaf], float c)
 {
-    if (n_valid <= 0) return MaxSum{-INFINITY, 0.0f};
     float mx = l[0];
 #pragma unroll
-    for (int e = 0; e < kLeaf; ++e) {
-        if (e < n_valid) {
-            mx = fmaxf(mx, l[e]);
-            finite = __fmaf_rn(0.0f, l[e], finite);
-        }
-    }
+    for (int e = 1; e < kLeaf; ++e) mx = fmaxf(mx, l[e]);
     const float mz = __fmul_rn(mx, c);
-    finite = __fmaf_rn(0.0f, mz, finite);
     float s = 0.0f;
 #pragma unroll
-    for (int e = 0; e < kLeaf; ++e)
-        if (e < n_valid) s = __fadd_rn(s, exp2_canon(__fmaf_rn(l[e], c, -mz)));
+    for (int e = 0; e < kLeaf; ++e) s = __fadd_rn(s, exp2_canon(__fmaf_rn(l[e], c, -mz)));
     return MaxSum{mz, s};
 }
 
@@ -193,176 +236,84 @@ __device__ __forceinline__ float warp_tree_sum(float a, int levels)
 
 struct RowRoots { float M, inv_s; };
 
-// Probability of entry x (leaf max mz recomputed from the leaf's logits).
-__device__ __forceinline__ float prob_of(float lx, float mz_leaf, float c, RowRoots r)
+__device__ __forceinline__ float leaf_factor(float mz_leaf, float M, float inv_s)
 {
-    const float F = __fmul_rn(exp2_canon(__fsub_rn(mz_leaf, r.M)), r.inv_s);
-    return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz_leaf)), F);
+    return __fmul_rn(exp2_canon(__fsub_rn(mz_leaf, M)), inv_s);
 }
 
-// Weights of the sampling distribution for one leaf: the residual
-// max(0, p - q) (resid == true) or the target probabilities p.
-__device__ __forceinline__ void leaf_weights(const float *pv, const float *qv, bool resid, int V, int L, float c,
-                                             RowRoots rp, RowRoots rq, float (&w)[kLeaf], int &n_valid)
-{
-    n_valid = min(kLeaf, V - L * kLeaf);
-    if (n_valid <= 0) {
-#pragma unroll
-        for (int e = 0; e < kLeaf; ++e) w[e] = 0.0f;
-        return;
-    }
-    float lp[kLeaf];
-    load_leaf(pv, V, L, lp);
-    float mx = lp[0];
-#pragma unroll
-    for (int e = 0; e < kLeaf; ++e) if (e < n_valid) mx = fmaxf(mx, lp[e]);
-    const float mzp = __fmul_rn(mx, c);
-#pragma unroll
-    for (int e = 0; e < kLeaf; ++e) w[e] = e < n_valid ? prob_of(lp[e], mzp, c, rp) : 0.0f;
-    if (resid) {
-        float lq[kLeaf];
-        load_leaf(qv, V, L, lq);
-        float mq = lq[0];
-#pragma unroll
-        for (int e = 0; e < kLeaf; ++e) if (e < n_valid) mq = fmaxf(mq, lq[e]);
-        const float mzq = __fmul_rn(mq, c);
-#pragma unroll
-        for (int e = 0; e < kLeaf; ++e) {
-            if (e < n_valid) {
-                const float d = __fsub_rn(w[e], prob_of(lq[e], mzq, c, rq));
-                w[e] = d > 0.0f ? d : 0.0f;
-            }
-        }
-    }
-}
-
-struct SampleSmem {
-    MaxSum red[kThreads / 32];
-    RowRoots roots[2 * kMaxK + 1];
-    float chunk_sum[2 * kMaxChunks];     // chunk-level tree (levels stacked)
-    float leaf_sum[2 * kThreads];        // leaf-level tree of one chunk (levels stacked)
-    float warp_sum[kThreads / 32];
-    int jstar;
-    int pick;
-    bool last;
-};
-
-// Sum of the sampling weights of every leaf of chunk cc, reduced to the chunk
-// total by a fixed pairwise tree; optionally keeps the leaf-level tree.
-__device__ float chunk_weight_sum(SampleSmem &sm, const float *pv, const float *qv, bool resid, int V, int cc,
-                                  float c, RowRoots rp, RowRoots rq, bool keep_levels)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float w[kLeaf];
-    int nv;
-    leaf_weights(pv, qv, resid, V, cc * kThreads + threadIdx.x, c, rp, rq, w, nv);
-    float s = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kLeaf; ++e) if (e < nv) s = __fadd_rn(s, w[e]);
-    if (keep_levels) sm.leaf_sum[threadIdx.x] = s;
-    s = warp_tree_sum(s, 5);
-    if (lane == 0) sm.warp_sum[warp] = s;
-    __syncthreads();
-    float tot = 0.0f;
-    if (threadIdx.x < 32) {
-        float v = lane < kThreads / 32 ? sm.warp_sum[lane] : 0.0f;
-        v = warp_tree_sum(v, 3);
-        tot = v;
-    }
-    if (keep_levels) {
-        // levels 1..8 of the 256-leaf tree, stacked after level 0
-        int in = 0, width = kThreads;
-        while (width > 1) {
-            const int out = in + width;
-            for (int i = threadIdx.x; i < width / 2; i += kThreads)
-                sm.leaf_sum[out + i] = __fadd_rn(sm.leaf_sum[in + 2 * i], sm.leaf_sum[in + 2 * i + 1]);
-            __syncthreads();
-            in = out;
-            width >>= 1;
-        }
-    }
-    __syncthreads();
-    return tot;   // valid in thread 0 (warp 0)
-}
-
+// ---- pass A: one block of one vector; the last CTA of a row decides.
 __global__ void __launch_bounds__(kThreads)
-sample_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
-              int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
-              int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
-              unsigned int *__restrict__ counters, float2 *__restrict__ part, unsigned int *status)
+sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
+                int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
+                unsigned int *__restrict__ counters, float2 *__restrict__ part, SampleRec *__restrict__ rec,
+                unsigned int *status)
 {
-    __shared__ SampleSmem sm;
-    const int C = gridDim.x, cidx = blockIdx.x, v = blockIdx.y, b = blockIdx.z;
+    __shared__ MaxSum red[kThreads / 32];
+    __shared__ RowRoots roots[2 * kMaxK + 1];
+    __shared__ bool last;
+    const int NBK = gridDim.x, blk = blockIdx.x, v = blockIdx.y, b = blockIdx.z;
     const int NV = 2 * k + 1;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, T = threadIdx.x;
     // vectors 0..k: target positions 0..k; k+1..2k: draft positions 0..k-1
     const float *vec = v <= k ? tlog + (static_cast<size_t>(b) * (k + 1) + v) * V
                               : dlog + (static_cast<size_t>(b) * k + (v - k - 1)) * V;
-
-    // ---- pass A: (max, sum) of this chunk's 256 leaves
     {
-        const int L = cidx * kThreads + threadIdx.x;
-        float l[kLeaf];
-        const int nv = min(kLeaf, V - L * kLeaf);
-        float finite = 0.0f;
-        MaxSum ms{-INFINITY, 0.0f};
-        if (nv > 0) {
-            const int x0 = L * kLeaf;
-            if ((V & 3) == 0 && nv == kLeaf) {
-                const float4 *p = reinterpret_cast<const float4 *>(vec + x0);
+        const bool full = block_full(V, blk);
+        float finite = 0.0f;   // becomes NaN if a present entry is not finite
+        MaxSum ms[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 t4 = __ldcg(p + q);
-                    l[4 * q] = t4.x; l[4 * q + 1] = t4.y; l[4 * q + 2] = t4.z; l[4 * q + 3] = t4.w;
-                }
+        for (int q = 0; q < 4; ++q) {
+            float l[kLeaf];
+            load_leaf(vec, V, full, blk, T, q, l);
+            if (full) {
+#pragma unroll
+                for (int e = 0; e < kLeaf; ++e) finite = __fmaf_rn(0.0f, l[e], finite);
+                ms[q] = leaf_ms(l, c);
+            } else if (leaf_entry(blk, T, q, 0) < V) {
+#pragma unroll
+                for (int e = 0; e < kLeaf; ++e)
+                    if (leaf_entry(blk, T, q, e) < V) finite = __fmaf_rn(0.0f, l[e], finite);
+                ms[q] = leaf_ms(l, c);
             } else {
-#pragma unroll
-                for (int e = 0; e < kLeaf; ++e) l[e] = e < nv ? vec[x0 + e] : 0.0f;
+                ms[q] = MaxSum{-INFINITY, 0.0f};
             }
-            ms = leaf_stats(l, nv, c, finite);
+            finite = __fmaf_rn(0.0f, ms[q].m == -INFINITY ? 0.0f : ms[q].m, finite);
         }
         if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
-        ms = warp_tree_ms(ms, lane, 5);
-        if (lane == 0) sm.red[warp] = ms;
+        MaxSum a = ms_merge(ms_merge(ms[0], ms[1]), ms_merge(ms[2], ms[3]));
+        a = warp_tree_ms(a, lane, 5);
+        if (lane == 0) red[warp] = a;
         __syncthreads();
         if (warp == 0) {
-            MaxSum a = lane < kThreads / 32 ? sm.red[lane] : MaxSum{-INFINITY, 0.0f};
-            a = warp_tree_ms(a, lane, 3);
+            MaxSum w8 = lane < kThreads / 32 ? red[lane] : MaxSum{-INFINITY, 0.0f};
+            w8 = warp_tree_ms(w8, lane, 3);
             if (lane == 0) {
-                part[(static_cast<size_t>(b) * NV + v) * C + cidx] = make_float2(a.m, a.s);
+                part[(static_cast<size_t>(b) * NV + v) * NBK + blk] = make_float2(w8.m, w8.s);
                 __threadfence();
                 const unsigned int prev = atomicAdd(&counters[b], 1u);
-                sm.last = prev == static_cast<unsigned int>(NV * C - 1);
+                last = prev == static_cast<unsigned int>(NV * NBK - 1);
             }
         }
         __syncthreads();
-        if (!sm.last) return;
+        if (!last) return;
         __threadfence();
     }
 
-    // ---- last CTA of row b: roots (M, 1/S) of all 2k+1 vectors
+    // ---- last CTA of row b: roots (M, 1/S) of the 2k+1 vectors (lane = block)
     for (int vv = warp; vv < NV; vv += kThreads / 32) {
-        // lane holds chunks 4*lane .. 4*lane+3 (levels 9, 10 locally, then 11.. across lanes)
-        MaxSum n4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int cc = 4 * lane + q;
-            if (cc < C) {
-                const float2 p = __ldcg(part + (static_cast<size_t>(b) * NV + vv) * C + cc);
-                n4[q] = MaxSum{p.x, p.y};
-            } else {
-                n4[q] = MaxSum{-INFINITY, 0.0f};
-            }
+        MaxSum a{-INFINITY, 0.0f};
+        if (lane < NBK) {
+            const float2 p = __ldcg(part + (static_cast<size_t>(b) * NV + vv) * NBK + lane);
+            a = MaxSum{p.x, p.y};
         }
-        MaxSum a = ms_merge(ms_merge(n4[0], n4[1]), ms_merge(n4[2], n4[3]));
         a = warp_tree_ms(a, lane, 5);
-        if (lane == 0) sm.roots[vv] = RowRoots{a.m, __frcp_rn(a.s)};
+        if (lane == 0) roots[vv] = RowRoots{a.m, __frcp_rn(a.s)};
     }
     __syncthreads();
 
-    // ---- decisions: accept d_j iff u_j < p_j(d_j) / q_j(d_j), first rejection j*
-    const uint64_t seed = seeds[b];
+    // ---- decisions: accept d_j iff u_j < p_j(d_j) / q_j(d_j); first rejection j*
     if (warp == 0) {
+        const uint64_t seed = seeds[b];
         bool reject = false;
         if (lane < k) {
             const int j = lane;
@@ -373,109 +324,239 @@ sample_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog,
             } else {
                 const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + j) * V;
                 const float *qv = dlog + (static_cast<size_t>(b) * k + j) * V;
-                const int L = d / kLeaf;
+                const int bd = d / kBlock, o = d - bd * kBlock;
+                const int qd = o >> 12, o2 = o & 4095;
+                const int Td = (o2 & 1023) >> 2, ed = 4 * (o2 >> 10) + (o2 & 3);
+                const bool fd = block_full(V, bd);
                 float lp[kLeaf], lq[kLeaf];
-                load_leaf(pv, V, L, lp);
-                load_leaf(qv, V, L, lq);
-                const int nv = min(kLeaf, V - L * kLeaf);
+                load_leaf(pv, V, fd, bd, Td, qd, lp);
+                load_leaf(qv, V, fd, bd, Td, qd, lq);
                 float mp = lp[0], mq = lq[0];
 #pragma unroll
-                for (int e = 0; e < kLeaf; ++e) if (e < nv) { mp = fmaxf(mp, lp[e]); mq = fmaxf(mq, lq[e]); }
-                const float p = prob_of(lp[d - L * kLeaf], __fmul_rn(mp, c), c, sm.roots[j]);
-                const float q = prob_of(lq[d - L * kLeaf], __fmul_rn(mq, c), c, sm.roots[k + 1 + j]);
+                for (int e = 1; e < kLeaf; ++e) { mp = fmaxf(mp, lp[e]); mq = fmaxf(mq, lq[e]); }
+                const float mzp = __fmul_rn(mp, c), mzq = __fmul_rn(mq, c);
+                float ld_p = lp[0], ld_q = lq[0];
+#pragma unroll
+                for (int e = 1; e < kLeaf; ++e) if (e == ed) { ld_p = lp[e]; ld_q = lq[e]; }
+                const float p = __fmul_rn(exp2_canon(__fmaf_rn(ld_p, c, -mzp)), leaf_factor(mzp, roots[j].M, roots[j].inv_s));
+                const float q = __fmul_rn(exp2_canon(__fmaf_rn(ld_q, c, -mzq)),
+                                          leaf_factor(mzq, roots[k + 1 + j].M, roots[k + 1 + j].inv_s));
                 const float ratio = __fdiv_rn(p, q);
                 const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
                 reject = !(u < ratio);
             }
         }
         const unsigned int rej = __ballot_sync(0xffffffffu, reject);
-        if (lane == 0) sm.jstar = rej ? __ffs(rej) - 1 : k;
+        if (lane == 0) {
+            const int js = rej ? __ffs(rej) - 1 : k;
+            SampleRec r;
+            r.js = js;
+            r.resid = js < k;
+            r.u = philox_uniform(seed, static_cast<uint32_t>(js), js < k ? 1u : 2u, round);
+            r.Mp = roots[js].M;
+            r.invSp = roots[js].inv_s;
+            r.Mq = js < k ? roots[k + 1 + js].M : 0.0f;
+            r.invSq = js < k ? roots[k + 1 + js].inv_s : 0.0f;
+            r.pad = 0;
+            rec[b] = r;
+            counters[b] = 0;   // ready for the next call
+        }
     }
-    __syncthreads();
-    const int js = sm.jstar;
+}
 
-    // ---- draw the replacement (residual at j*) or the bonus token (p_k)
-    const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + js) * V;
-    const float *qv = js < k ? dlog + (static_cast<size_t>(b) * k + js) * V : pv;
-    const RowRoots rp = sm.roots[js];
-    const RowRoots rq = js < k ? sm.roots[k + 1 + js] : sm.roots[js];
-    bool resid = js < k;
-    const float u = philox_uniform(seed, static_cast<uint32_t>(js), resid ? 1u : 2u, round);
-    int Cp = 1;
-    while (Cp < C) Cp <<= 1;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        for (int cc = 0; cc < Cp; ++cc) {
-            const float s = cc < C ? chunk_weight_sum(sm, pv, qv, resid, V, cc, c, rp, rq, false) : 0.0f;
-            if (threadIdx.x == 0) sm.chunk_sum[cc] = s;
+// Sampling weights of leaf (blk, 4T + q) of row b's chosen position and their
+// serial sum: max(0, p - q) (resid) or p.  The logits are loaded separately
+// (load_pq) so that the next leaf's loads can overlap this leaf's arithmetic.
+__device__ __forceinline__ void load_pq(const float *pv, const float *qv, bool resid, int V, int blk, int T, int q,
+                                        float (&lp)[kLeaf], float (&lq)[kLeaf])
+{
+    if (leaf_entry(blk, T, q, 0) >= V) return;
+    const bool full = block_full(V, blk);
+    load_leaf(pv, V, full, blk, T, q, lp);
+    if (resid) load_leaf(qv, V, full, blk, T, q, lq);
+}
+
+template <bool KEEP>
+__device__ __forceinline__ float leaf_weights(const float (&lp)[kLeaf], const float (&lq)[kLeaf], bool resid, int V,
+                                              int blk, int T, int q, float c, const SampleRec &R, float (&w)[kLeaf])
+{
+    if (leaf_entry(blk, T, q, 0) >= V) {
+        if (KEEP) {
+#pragma unroll
+            for (int e = 0; e < kLeaf; ++e) w[e] = 0.0f;
         }
-        __syncthreads();
-        // chunk-level levels stacked: level 0 at [0, Cp), level l after
-        {
-            int in = 0, width = Cp;
-            while (width > 1) {
-                const int out = in + width;
-                for (int i = threadIdx.x; i < width / 2; i += kThreads)
-                    sm.chunk_sum[out + i] = __fadd_rn(sm.chunk_sum[in + 2 * i], sm.chunk_sum[in + 2 * i + 1]);
-                __syncthreads();
-                in = out;
-                width >>= 1;
-            }
-        }
-        const float R = sm.chunk_sum[2 * Cp - 2];
-        if (R > 0.0f || !resid) break;
-        resid = false;   // all-zero residual: draw from p_j* instead
-        __syncthreads();
+        return 0.0f;
     }
-    const float R = sm.chunk_sum[2 * Cp - 2];
-    // descend the chunk-level tree (every thread follows the same path)
-    float t = __fmul_rn(u, R);
-    int node = 0;
-    {
-        // level offsets: level l (width Cp >> l) starts at Cp*(2 - 2^(1-l)) = sum of wider levels
-        int levels = 0;
-        while ((1 << levels) < Cp) ++levels;
-        for (int lv = levels; lv >= 1; --lv) {
-            int off_child = 0;
-            for (int q = 0; q < lv - 1; ++q) off_child += Cp >> q;
-            const float left = sm.chunk_sum[off_child + 2 * node], right = sm.chunk_sum[off_child + 2 * node + 1];
-            if (t < left || !(right > 0.0f)) node = 2 * node;
-            else { t = __fsub_rn(t, left); node = 2 * node + 1; }
+    float mp = lp[0];
+#pragma unroll
+    for (int e = 1; e < kLeaf; ++e) mp = fmaxf(mp, lp[e]);
+    const float mzp = __fmul_rn(mp, c);
+    const float Fp = leaf_factor(mzp, R.Mp, R.invSp);
+    float s = 0.0f;
+    if (resid) {
+        float mq = lq[0];
+#pragma unroll
+        for (int e = 1; e < kLeaf; ++e) mq = fmaxf(mq, lq[e]);
+        const float mzq = __fmul_rn(mq, c);
+        const float Fq = leaf_factor(mzq, R.Mq, R.invSq);
+#pragma unroll
+        for (int e = 0; e < kLeaf; ++e) {
+            const float pe = __fmul_rn(exp2_canon(__fmaf_rn(lp[e], c, -mzp)), Fp);
+            const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq[e], c, -mzq)), Fq);
+            const float d = __fsub_rn(pe, qe);
+            const float we = d > 0.0f ? d : 0.0f;
+            s = __fadd_rn(s, we);
+            if (KEEP) w[e] = we;
         }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kLeaf; ++e) {
+            const float we = __fmul_rn(exp2_canon(__fmaf_rn(lp[e], c, -mzp)), Fp);
+            s = __fadd_rn(s, we);
+            if (KEEP) w[e] = we;
+        }
+    }
+    return s;
+}
+
+// Sum over the 1024 leaves of block blk by the fixed pairwise tree (valid in
+// thread 0); optionally stores the 1024 leaf sums (index 4T + q) at lsum.
+__device__ float block_sum(float *warp_sum, float *lsum, const float *pv, const float *qv, bool resid, int V,
+                           int blk, float c, const SampleRec &R)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, T = threadIdx.x;
+    float w[kLeaf];
+    float lp[2][kLeaf], lq[2][kLeaf];
+    float ls[4];
+    load_pq(pv, qv, resid, V, blk, T, 0, lp[0], lq[0]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q + 1 < 4) load_pq(pv, qv, resid, V, blk, T, q + 1, lp[(q + 1) & 1], lq[(q + 1) & 1]);
+        ls[q] = leaf_weights<false>(lp[q & 1], lq[q & 1], resid, V, blk, T, q, c, R, w);
+    }
+    if (lsum) *reinterpret_cast<float4 *>(lsum + 4 * T) = make_float4(ls[0], ls[1], ls[2], ls[3]);
+    float s = __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3]));
+    s = warp_tree_sum(s, 5);
+    if (lane == 0) warp_sum[warp] = s;
+    __syncthreads();
+    float tot = 0.0f;
+    if (warp == 0) tot = warp_tree_sum(lane < kThreads / 32 ? warp_sum[lane] : 0.0f, 3);
+    __syncthreads();
+    return tot;
+}
+
+// Levels of a power-of-two sum tree stacked in one array: level 0 = [0, P),
+// level l starts after the wider levels.  Returns the root.
+__device__ float build_levels(float *tree, int P)
+{
+    int in = 0, width = P;
+    while (width > 1) {
+        const int out = in + width;
+        for (int i = threadIdx.x; i < width / 2; i += kThreads)
+            tree[out + i] = __fadd_rn(tree[in + 2 * i], tree[in + 2 * i + 1]);
+        __syncthreads();
+        in = out;
+        width >>= 1;
+    }
+    return tree[in];
+}
+
+// Descend a stacked power-of-two tree: left if t < left or the right sum is 0.
+__device__ __forceinline__ int descend(const float *tree, int P, float &t)
+{
+    int levels = 0;
+    while ((1 << levels) < P) ++levels;
+    int node = 0;
+    for (int lv = levels; lv >= 1; --lv) {
+        int off = 0;
+        for (int q = 0; q < lv - 1; ++q) off += P >> q;
+        const float left = tree[off + 2 * node], right = tree[off + 2 * node + 1];
+        if (t < left || !(right > 0.0f)) node = 2 * node;
+        else { t = __fsub_rn(t, left); node = 2 * node + 1; }
+    }
+    return node;
+}
+
+// ---- pass B: one block of the chosen position of one row; the last CTA of
+// the row descends the sum tree and writes the row's tokens.
+__global__ void __launch_bounds__(kThreads)
+sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
+                int k, int V, float c, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
+                unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ csum,
+                float *__restrict__ lsum)
+{
+    __shared__ float warp_sum[kThreads / 32];
+    __shared__ __align__(16) float btree[2 * kMaxBlocks];
+    __shared__ __align__(16) float ltree[2 * 4 * kThreads];
+    __shared__ bool last;
+    __shared__ int pick;
+    const int NBK = gridDim.x, blk = blockIdx.x, b = blockIdx.y;
+    const SampleRec R = rec[b];
+    const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + R.js) * V;
+    const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
+    bool resid = R.resid != 0;
+
+    float *my_lsum = lsum + (static_cast<size_t>(b) * NBK + blk) * (4 * kThreads);
+    const float tot = block_sum(warp_sum, my_lsum, pv, qv, resid, V, blk, c, R);
+    if (threadIdx.x == 0) {
+        csum[static_cast<size_t>(b) * NBK + blk] = tot;
+        __threadfence();
+        const unsigned int prev = atomicAdd(&counters[b], 1u);
+        last = prev == static_cast<unsigned int>(NBK - 1);
     }
     __syncthreads();
-    const int cstar = node;
-    chunk_weight_sum(sm, pv, qv, resid, V, cstar, c, rp, rq, true);
-    // descend the 256-leaf tree of chunk c*
+    if (!last) return;
+    __threadfence();
+
+    int P = 1;
+    while (P < NBK) P <<= 1;
+    for (int i = threadIdx.x; i < P; i += kThreads) btree[i] = i < NBK ? __ldcg(csum + static_cast<size_t>(b) * NBK + i) : 0.0f;
+    __syncthreads();
+    float root = build_levels(btree, P);
+    if (!(root > 0.0f) && resid) {
+        // all-zero residual (rounding): draw from p_js instead
+        resid = false;
+        for (int bb = 0; bb < NBK; ++bb) {
+            const float s = block_sum(warp_sum, lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads), pv, qv,
+                                      false, V, bb, c, R);
+            if (threadIdx.x == 0) btree[bb] = s;
+        }
+        __syncthreads();
+        root = build_levels(btree, P);
+    }
+    float t = __fmul_rn(R.u, root);
+    const int bstar = descend(btree, P, t);
     {
-        int leaf = 0;
-        for (int lv = 8; lv >= 1; --lv) {
-            int off_child = 0;
-            for (int q = 0; q < lv - 1; ++q) off_child += kThreads >> q;
-            const float left = sm.leaf_sum[off_child + 2 * leaf], right = sm.leaf_sum[off_child + 2 * leaf + 1];
-            if (t < left || !(right > 0.0f)) leaf = 2 * leaf;
-            else { t = __fsub_rn(t, left); leaf = 2 * leaf + 1; }
+        const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * (4 * kThreads)) + threadIdx.x);
+        *reinterpret_cast<float4 *>(ltree + 4 * threadIdx.x) = v4;
+    }
+    __syncthreads();
+    build_levels(ltree, 4 * kThreads);
+    const int lstar = descend(ltree, 4 * kThreads, t);
+    if (threadIdx.x == 0) {
+        const int Ts = lstar >> 2, qs = lstar & 3;
+        float w[kLeaf], lp[kLeaf], lq[kLeaf];
+        load_pq(pv, qv, resid, V, bstar, Ts, qs, lp, lq);
+        leaf_weights<true>(lp, lq, resid, V, bstar, Ts, qs, c, R, w);
+        int pk = -1;
+        float run = 0.0f;
+        for (int e = 0; e < kLeaf && pk < 0; ++e) {
+            const int x = leaf_entry(bstar, Ts, qs, e);
+            if (x >= V) continue;
+            run = __fadd_rn(run, w[e]);
+            if (t < run) pk = x;
         }
-        if (threadIdx.x == 0) {
-            const int L = cstar * kThreads + leaf;
-            float w[kLeaf];
-            int nv;
-            leaf_weights(pv, qv, resid, V, L, c, rp, rq, w, nv);
-            int pick = -1;
-            float run = 0.0f;
-            for (int e = 0; e < nv && pick < 0; ++e) {
-                run = __fadd_rn(run, w[e]);
-                if (t < run) pick = e;
-            }
-            for (int e = nv - 1; e >= 0 && pick < 0; --e)
-                if (w[e] > 0.0f) pick = e;
-            sm.pick = pick < 0 ? -1 : L * kLeaf + pick;
+        for (int e = kLeaf - 1; e >= 0 && pk < 0; --e) {
+            const int x = leaf_entry(bstar, Ts, qs, e);
+            if (x < V && w[e] > 0.0f) pk = x;
         }
+        pick = pk;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int tok = sm.pick;
+        const int js = R.js;
         for (int jj = 0; jj <= k; ++jj)
-            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? tok : -1);
+            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? pick : -1);
         out_cnt[b] = js + 1;
         counters[b] = 0;
     }
@@ -486,7 +567,7 @@ nq_status check_accept(int B, int k, int V, const void *ws, size_t ws_bytes)
     if (B < 1 || B > 65535 || k < 1 || k > kMaxK || V < 1 || V > kMaxChunks * kChunk) return NQ_ERR_ARG;
     if (!ws) return NQ_ERR_ARG;
     if (!aligned16(ws)) return NQ_ERR_ALIGN;
-    if (ws_bytes < spec_accept_workspace_bytes(B, k, V)) return NQ_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(B, k, V).total) return NQ_ERR_WORKSPACE;
     return NQ_OK;
 }
 
@@ -496,7 +577,7 @@ nq_status check_accept(int B, int k, int V, const void *ws, size_t ws_bytes)
 extern "C" size_t spec_accept_workspace_bytes(int B, int k, int V)
 {
     if (B < 1 || B > 65535 || k < 1 || k > nq::kMaxK || V < 1 || V > nq::kMaxChunks * nq::kChunk) return 0;
-    return nq::counters_bytes(B) + static_cast<size_t>(B) * (2 * k + 1) * nq::n_chunks(V) * sizeof(float2);
+    return nq::ws_layout(B, k, V).total;
 }
 
 extern "C" nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
@@ -510,10 +591,12 @@ extern "C" nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_l
         return NQ_ERR_ALIGN;
     unsigned int *status = nq::device_status_ptr();
     if (!status) return NQ_ERR_CUDA;
-    unsigned int *counters = static_cast<unsigned int *>(ws);
-    float2 *part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + nq::counters_bytes(B));
+    const nq::WsLayout L = nq::ws_layout(B, k, V);
+    char *w = static_cast<char *>(ws);
     dim3 grid(nq::n_chunks(V), k + 1, B);
-    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt, counters, part, status);
+    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
+                                                         reinterpret_cast<unsigned int *>(w + L.counters_a),
+                                                         reinterpret_cast<float2 *>(w + L.part), status);
     return nq::cuda_status(cudaGetLastError());
 }
 
@@ -532,11 +615,18 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     unsigned int *status = nq::device_status_ptr();
     if (!status) return NQ_ERR_CUDA;
     const float c = nq::kLog2e / temperature;   // IEEE division on the host (round to nearest)
-    unsigned int *counters = static_cast<unsigned int *>(ws);
-    float2 *part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + nq::counters_bytes(B));
-    dim3 grid(nq::n_chunks(V), 2 * k + 1, B);
-    nq::sample_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
-                                                         out_tok, out_cnt, counters, part, status);
+    const nq::WsLayout L = nq::ws_layout(B, k, V);
+    char *w = static_cast<char *>(ws);
+    auto *rec = reinterpret_cast<nq::SampleRec *>(w + L.rec);
+    dim3 grid_a(nq::n_blocks(V), 2 * k + 1, B);
+    nq::sample_a_kernel<<<grid_a, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
+                                                             reinterpret_cast<unsigned int *>(w + L.counters_a),
+                                                             reinterpret_cast<float2 *>(w + L.part), rec, status);
+    dim3 grid_b(nq::n_blocks(V), B);
+    nq::sample_b_kernel<<<grid_b, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
+                                                             reinterpret_cast<unsigned int *>(w + L.counters_b), rec,
+                                                             reinterpret_cast<float *>(w + L.csum),
+                                                             reinterpret_cast<float *>(w + L.lsum));
     return nq::cuda_status(cudaGetLastError());
 }
 

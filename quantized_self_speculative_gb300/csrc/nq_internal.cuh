@@ -92,36 +92,42 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint
 // base-2 exponential of t <= 0.5: 0 below -125, else P(f) 2^n with n =
 // rint(t), f = t - n (exact) and P the degree-6 Taylor polynomial of 2^f,
 // coefficients ln2^i / i! rounded to fp32, Horner with fused multiply-add.
+// rint is taken by adding 1.5 * 2^23 (round to nearest even; the integer
+// lands in the low mantissa bits of the sum) and 2^n is applied by adding n
+// to the exponent field, so no conversion instructions are needed.
 __device__ __forceinline__ float exp2_canon(float t)
 {
     const float c0 = 1.0f, c1 = 0.693147180559945309417f, c2 = 0.240226506959100712333f,
                 c3 = 0.0555041086648215799531f, c4 = 0.00961812910762847716197f,
                 c5 = 0.00133335581464284434234f, c6 = 0.000154035303933816099545f;
-    float tc = fmaxf(t, -125.0f);
-    float n = rintf(tc);
-    float f = __fsub_rn(tc, n);
+    const float tc = fmaxf(t, -125.0f);
+    const float big = __fadd_rn(tc, 12582912.0f);
+    const float n = __fsub_rn(big, 12582912.0f);
+    const float f = __fsub_rn(tc, n);
     float p = __fmaf_rn(c6, f, c5);
     p = __fmaf_rn(p, f, c4);
     p = __fmaf_rn(p, f, c3);
     p = __fmaf_rn(p, f, c2);
     p = __fmaf_rn(p, f, c1);
     p = __fmaf_rn(p, f, c0);
-    float r = __int_as_float(__float_as_int(p) + (static_cast<int>(n) << 23));
+    const float r = __int_as_float(__float_as_int(p) + (__float_as_int(big) << 23));
     return t < -125.0f ? 0.0f : r;
 }
 
 struct MaxSum { float m, s; };
 
 // Merge two (max, sum) nodes; the larger max survives, the other sum is
-// rescaled by 2^(m_small - m_large); a (-inf, 0) pad is the identity.
+// rescaled by 2^(m_small - m_large) with one fma; ties keep `a` as the larger.
+// Branch-free (lanes of a warp merging different pairs never diverge).  A
+// (-inf, 0) pad is the identity: its rescale factor is exp2(-inf) = 0 and
+// fma(0, 0, s) = s; two pads give a pad.
 __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b)
 {
-    if (b.m == -INFINITY) return a;
-    if (a.m == -INFINITY) return b;
-    MaxSum r;
-    if (a.m >= b.m) { r.m = a.m; r.s = __fmaf_rn(b.s, exp2_canon(__fsub_rn(b.m, a.m)), a.s); }
-    else            { r.m = b.m; r.s = __fmaf_rn(a.s, exp2_canon(__fsub_rn(a.m, b.m)), b.s); }
-    return r;
+    const bool a_big = a.m >= b.m || b.m != b.m;
+    const float big_m = a_big ? a.m : b.m, small_m = a_big ? b.m : a.m;
+    const float big_s = a_big ? a.s : b.s, small_s = a_big ? b.s : a.s;
+    const float d = small_m == -INFINITY ? -INFINITY : __fsub_rn(small_m, big_m);
+    return MaxSum{big_m, __fmaf_rn(small_s, exp2_canon(d), big_s)};
 }
 
 // Philox4x32-10 (Salmon et al., SC'11).

@@ -99,29 +99,63 @@ def test_canonical_softmax_underflow_is_exact_zero():
     assert p[1] == 0 and p[3] == 0 and p[0] > 0 and p[2] > p[0]
 
 
+def sampling_order(V):
+    """The recipe's leaf order: blocks of 16384 entries; within a block, leaf
+    4T + q (T = 0..255, q = 0..3) holds entries 4096 q + 1024 r + 4 T + j for
+    r, j = 0..3 in that order."""
+    order = []
+    for b in range((V + 16383) // 16384):
+        for T in range(256):
+            for q in range(4):
+                for r in range(4):
+                    for j in range(4):
+                        x = 16384 * b + 4096 * q + 1024 * r + 4 * T + j
+                        if x < V:
+                            order.append(x)
+    assert sorted(order) == list(range(V))
+    return np.array(order)
+
+
 def test_tree_sample_is_inverse_cdf_away_from_boundaries():
     g = synth.rng(91)
-    for V in (1, 7, 16, 33, 1000, 4096):
+    for V in (1, 7, 16, 33, 1000, 4096, 5000, 20000):
         w = g.random(V).astype(np.float32) * (g.random(V) < 0.7)
         if w.sum() == 0:
             w[0] = 1
-        us = g.random(400).astype(np.float32)
-        cdf = np.cumsum(w.astype(np.float64))
+        us = g.random(150).astype(np.float32)
+        order = sampling_order(V)
+        cdf = np.cumsum(w[order].astype(np.float64))
         tot = cdf[-1]
         for u in us:
             got = O.tree_sample(w, float(u))
             t = float(u) * tot
             if np.min(np.abs(cdf - t)) < 1e-5 * tot:
                 continue
-            want = int(np.searchsorted(cdf, t, side="right"))
+            want = int(order[np.searchsorted(cdf, t, side="right")])
             assert got == want, (V, u)
             assert w[got] > 0
+
+
+def test_tree_sample_distribution_chi_square():
+    g = synth.rng(92)
+    V = 40000                                      # three blocks, the last one partial
+    w = np.zeros(V, np.float32)
+    hot = g.choice(V, 12, replace=False)
+    w[hot] = g.random(12).astype(np.float32) + 0.2
+    us = ((np.arange(12000) + 0.5) / 12000).astype(np.float32)
+    got = np.array([O.tree_sample(w, float(u)) for u in us])
+    assert np.all(np.isin(got, hot))
+    obs = np.array([(got == h).sum() for h in hot])
+    wh = w[hot].astype(np.float64)
+    exp = wh / wh.sum() * us.size
+    assert stats.chisquare(obs, exp).pvalue > 1e-3
 
 
 def test_tree_sample_zero_total_and_extreme_u():
     assert O.tree_sample(np.zeros(20, np.float32), 0.5) == -1
     w = np.zeros(40, np.float32)
     w[[3, 37]] = [1.0, 2.0]
+    # entry 3 sits in leaf 0, entry 37 in leaf 36 of block 0: index order here
     assert O.tree_sample(w, 0.0) == 3
     assert O.tree_sample(w, float(np.float32(1 - 2**-24))) == 37
 
