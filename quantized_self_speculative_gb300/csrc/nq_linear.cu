@@ -40,11 +40,11 @@ namespace {
 constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
 constexpr int kMaxM = 16;             // activation rows per launch (two 8-column MMA tiles)
 constexpr int kXsMax = 112 * 1024;    // dynamic shared memory cap per CTA (two CTAs fit one SM)
-// Staging cap of the nibble kernels: the whole activation matrix at M = 1
-// (K <= 11008), segments beyond.  Measured on GB300: a larger buffer shrinks
-// L1 and slows the verify pass (4.5 TB/s at 48 KB, 2.5 TB/s at 112 KB vs 4.9
-// TB/s at 40 KB), a smaller one forces restaging at M = 1.
-constexpr int kXsNib = 40 * 1024;
+// Activation staging cap: the whole activation matrix at M = 1 (K <= 11008),
+// segments beyond.  Measured on GB300: a larger buffer shrinks L1 and slows
+// the verify pass (4.5 TB/s at 48 KB, 2.5 TB/s at 112 KB vs 4.9 TB/s at
+// 40 KB), a smaller one forces restaging at M = 1.
+constexpr int kXsStage = 40 * 1024;
 
 enum Kind { kNib = 0, kFp8 = 1, kFp16 = 2 };
 
@@ -119,12 +119,29 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 __device__ __forceinline__ float h_lo(uint32_t v) { return __half2float(__ushort_as_half(static_cast<unsigned short>(v))); }
 __device__ __forceinline__ float h_hi(uint32_t v) { return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16))); }
 
-// ------------------------------------------------------------------ nibble kernel
+// ------------------------------------------------------------------ streaming kernel
 
-template <int PLANES, int G>
-struct NibSlot {
-    uint32_t w[PLANES][2][G / 32];   // [plane][row g / g+8][word]
-    unsigned short s[2];             // fp16 scales of rows g, g+8
+// Geometry of one chunk of K (the unit of the prefetch ring) per weight kind:
+// nibbles use one quantisation group per chunk; E4M3 and fp16 rows give each
+// lane 16 contiguous bytes per row per chunk.
+template <int KIND, int G>
+struct Geo {
+    static constexpr int CH = KIND == kNib ? G : (KIND == kFp8 ? 64 : 32);   // inputs per chunk
+    static constexpr int VB = KIND == kNib ? G / 8 : 16;                     // bytes per lane per row per plane
+    static constexpr int WORDS = VB / 4;
+    static constexpr int IPL = CH / 4;                                       // inputs per lane per chunk
+    static constexpr int CHB = 2 * CH;                                       // staged fp16 bytes per chunk per row
+    static constexpr int PIECES = CHB / 64;                                  // 16-byte activation pieces per lane
+    __host__ __device__ static constexpr size_t row_bytes(int k)
+    {
+        return KIND == kNib ? static_cast<size_t>(k) / 2 : (KIND == kFp8 ? static_cast<size_t>(k) : 2 * static_cast<size_t>(k));
+    }
+};
+
+template <int KIND, int PLANES, int G>
+struct Slot {
+    uint32_t w[PLANES][2][Geo<KIND, G>::WORDS];   // [plane][row g / g+8][word]
+    unsigned short s[2];                           // nibbles: fp16 group scales of rows g, g+8
 };
 
 // First unit whose cost-prefix is >= target (units of one problem cost K each).
@@ -149,20 +166,20 @@ __device__ __forceinline__ int units_of(const Batch<MAXP> &B, int pi)
 }
 
 // Each CTA streams a contiguous, cost-balanced range of row units; every warp
-// walks the flat (unit, group) sequence of its 16 rows with a prefetch ring
+// walks the flat (unit, chunk) sequence of its 16 rows with a prefetch ring
 // that continues across unit boundaries.  Activations are restaged only when
 // the problem (or the staged K segment) changes.
-template <int PLANES, int G, int NT, int WARPS, int MAXP>
+template <int KIND, int PLANES, int G, int NT, int WARPS, int MAXP>
 __global__ void __launch_bounds__(WARPS * 32)
-nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
+stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
 {
+    using Gm = Geo<KIND, G>;
     constexpr int THREADS = WARPS * 32;
-    constexpr int VB = G / 8;                  // bytes per lane per row per plane per group
-    constexpr int WORDS = VB / 4;
-    constexpr int CHB = 2 * G;                 // staged fp16 activation bytes per group per row
+    constexpr int CH = Gm::CH, VB = Gm::VB, WORDS = Gm::WORDS, CHB = Gm::CHB, IPL = Gm::IPL;
     constexpr int MT = 8 * NT;
+    constexpr int CORR = KIND == kNib ? MT * 4 : 0;   // offset-correction bytes per chunk
     constexpr int LANE_BYTES = 2 * PLANES * VB;
-    constexpr int R = LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8);   // ring slots (R-1 groups in flight)
+    constexpr int R = LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8);   // ring slots (R-1 chunks in flight)
     constexpr int ROWS = 16 * WARPS;
     constexpr float kNeg8Ulp = -4.76837158203125e-07f;   // -8 * 2^-24
 
@@ -175,24 +192,24 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     const int ue = unit_at_cost(B, B.total_cost * (blockIdx.x + 1) / gridDim.x);
     if (ub >= ue) return;
 
-    // total steps (groups) of this CTA's range
-    int first_pi = find_problem(B, ub);
+    // total steps (chunks) of this CTA's range
+    const int first_pi = find_problem(B, ub);
     long long steps_ll = 0;
     for (int pi = first_pi; pi < B.count && B.p[pi].unit_begin < ue; ++pi) {
         const int a = max(ub, B.p[pi].unit_begin), b = min(ue, B.p[pi].unit_begin + units_of(B, pi));
-        steps_ll += static_cast<long long>(b - a) * (B.p[pi].k / G);
+        steps_ll += static_cast<long long>(b - a) * (B.p[pi].k / CH);
     }
     const int steps = static_cast<int>(steps_ll);
 
     // ---- load cursor (runs R-1 steps ahead of the compute cursor)
     int l_u = ub, l_pi = first_pi, l_c = 0, l_ng = 0;
     const uint8_t *lw[PLANES][2];
-    const unsigned short *ls[2];
+    const unsigned short *ls[2] = {nullptr, nullptr};
     auto l_setup = [&]() {
         const Prob &P = B.p[l_pi];
         const int N = P.n;
-        l_ng = P.k / G;
-        const size_t rowb = static_cast<size_t>(P.k) / 2;
+        l_ng = P.k / CH;
+        const size_t rowb = Gm::row_bytes(P.k);
         const int rg = (l_u - P.unit_begin) * ROWS + warp * 16 + g;
         const int r0 = rg < N ? rg : 0, r1 = rg + 8 < N ? rg + 8 : 0;
         lw[0][0] = P.base + static_cast<size_t>(r0) * rowb + VB * t;
@@ -201,11 +218,13 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
             lw[1][0] = P.resid + static_cast<size_t>(r0) * rowb + VB * t;
             lw[1][1] = P.resid + static_cast<size_t>(r1) * rowb + VB * t;
         }
-        ls[0] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r0) * l_ng;
-        ls[1] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r1) * l_ng;
+        if constexpr (KIND == kNib) {
+            ls[0] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r0) * l_ng;
+            ls[1] = static_cast<const unsigned short *>(P.scales) + static_cast<size_t>(r1) * l_ng;
+        }
     };
-    auto issue = [&](NibSlot<PLANES, G> &S) {
-        const size_t off = static_cast<size_t>(l_c) * (G / 2);
+    auto issue = [&](Slot<KIND, PLANES, G> &S) {
+        const size_t off = static_cast<size_t>(l_c) * (4 * VB);
 #pragma unroll
         for (int p = 0; p < PLANES; ++p)
 #pragma unroll
@@ -218,8 +237,10 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
                     S.w[p][r][0] = v.x; S.w[p][r][1] = v.y;
                 }
             }
-        S.s[0] = ld_nc_u16(ls[0] + l_c);
-        S.s[1] = ld_nc_u16(ls[1] + l_c);
+        if constexpr (KIND == kNib) {
+            S.s[0] = ld_nc_u16(ls[0] + l_c);
+            S.s[1] = ld_nc_u16(ls[1] + l_c);
+        }
         if (++l_c == l_ng) {
             l_c = 0;
             if (++l_u < ue) {
@@ -229,7 +250,7 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         }
     };
 
-    // ---- compute cursor: the next group to compute is (c_u, c_grp); an
+    // ---- compute cursor: the next chunk to compute is (c_u, c_grp); an
     // "event" (unit end / unit start / new activation segment) happens when
     // c_grp reaches seg_end, so a step costs one compare.
     int c_u = ub, c_pi = first_pi, c_grp = 0, seg_end = 0;
@@ -238,15 +259,16 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     int staged_pi = -1, staged_begin = -1, cps = 1, RS = 0;
     const uint16_t *c_x = nullptr;
     float *c_y = nullptr;
+    const float *c_rs = nullptr;   // FP8 row scales
     unsigned char *xs = smem;
     float *corr = reinterpret_cast<float *>(smem);
 
-    // Stage activations of groups [c_begin, c_begin + nch) of the compute
-    // cursor's problem: fp16, operand order (x0,x4)(x2,x6)(x1/16,x5/16)
-    // (x3/16,x7/16) per 8 inputs, plus the offset correction -8 * 2^-24 *
-    // sum(x) per (group, row).
+    // Stage activations of chunks [c_begin, c_begin + nch) of the compute
+    // cursor's problem in fp16.  Nibbles: operand order (x0,x4)(x2,x6)
+    // (x1/16,x5/16)(x3/16,x7/16) per 8 inputs plus the offset correction
+    // -8 * 2^-24 * sum(x) per (chunk, row); E4M3 / fp16: natural order.
     auto stage = [&](int c_begin, int nch) {
-        const int items_row = nch * (G / 8);
+        const int items_row = nch * (CH / 8);
         const int total = M * items_row;
         const int total_pad = (total + THREADS - 1) / THREADS * THREADS;
         bool range = false;
@@ -256,49 +278,65 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
             uint4 v = make_uint4(0, 0, 0, 0);
             if (valid)
                 v = *reinterpret_cast<const uint4 *>(c_x + static_cast<size_t>(m) * c_K +
-                                                     static_cast<size_t>(c_begin) * G + it * 8);
+                                                     static_cast<size_t>(c_begin) * CH + it * 8);
             const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
             const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
             const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
             const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
-            uint4 o;
-            o.x = pack_h2(x0, x4);
-            o.y = pack_h2(x2, x6);
-            o.z = pack_h2(__fmul_rn(x1, 0.0625f), __fmul_rn(x5, 0.0625f));
-            o.w = pack_h2(__fmul_rn(x3, 0.0625f), __fmul_rn(x7, 0.0625f));
             const float amax = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
                                      fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
             range |= amax > 65504.0f;
-            const int cl = it / (G / 8), kk = (it % (G / 8)) * 8;
-            const int tl = kk / (2 * VB), wd = (kk % (2 * VB)) / 8;
-            if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
-            // sum of the staged values as the MMA sees them: x~ at even k, 16 * (x/16)~ at odd k
-            const float se = __fadd_rn(__fadd_rn(h_lo(o.x), h_hi(o.x)), __fadd_rn(h_lo(o.y), h_hi(o.y)));
-            const float so = __fadd_rn(__fadd_rn(h_lo(o.z), h_hi(o.z)), __fadd_rn(h_lo(o.w), h_hi(o.w)));
-            float sum = __fmaf_rn(16.0f, so, se);
+            const int cl = it / (CH / 8), kk = (it % (CH / 8)) * 8;
+            if constexpr (KIND == kNib) {
+                uint4 o;
+                o.x = pack_h2(x0, x4);
+                o.y = pack_h2(x2, x6);
+                o.z = pack_h2(__fmul_rn(x1, 0.0625f), __fmul_rn(x5, 0.0625f));
+                o.w = pack_h2(__fmul_rn(x3, 0.0625f), __fmul_rn(x7, 0.0625f));
+                const int tl = kk / IPL, wd = (kk % IPL) / 8;
+                if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * wd + tl) * 16) = o;
+                // sum of the staged values as the MMA sees them: x~ at even k, 16 * (x/16)~ at odd k
+                const float se = __fadd_rn(__fadd_rn(h_lo(o.x), h_hi(o.x)), __fadd_rn(h_lo(o.y), h_hi(o.y)));
+                const float so = __fadd_rn(__fadd_rn(h_lo(o.z), h_hi(o.z)), __fadd_rn(h_lo(o.w), h_hi(o.w)));
+                float sum = __fmaf_rn(16.0f, so, se);
 #pragma unroll
-            for (int o2 = 1; o2 < G / 8; o2 <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o2));
-            if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(kNeg8Ulp, sum);
+                for (int o2 = 1; o2 < CH / 8; o2 <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o2));
+                if (valid && kk == 0) corr[cl * MT + m] = __fmul_rn(kNeg8Ulp, sum);
+            } else {
+                const uint4 o = make_uint4(pack_h2(x0, x1), pack_h2(x2, x3), pack_h2(x4, x5), pack_h2(x6, x7));
+                // lane kk / IPL reads its IPL inputs as PIECES 16-byte pieces, interleaved across lanes
+                const int tl = kk / IPL, pc = (kk % IPL) / 8;
+                if (valid) *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + (4 * pc + tl) * 16) = o;
+            }
         }
-        for (int i = threadIdx.x; i < nch * (MT - M); i += THREADS)
-            corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
+        if constexpr (KIND == kNib)
+            for (int i = threadIdx.x; i < nch * (MT - M); i += THREADS)
+                corr[(i / (MT - M)) * MT + M + i % (MT - M)] = 0.0f;
         if (range) set_status(status, NQ_DEV_ACT_RANGE);
     };
 
     const unsigned char *xrow[NT];   // row base of each 8-column tile in the staged segment
     int xstep[NT];
-    const unsigned char *xp[NT];     // current group
-    const float *cp = corr;          // current group's offset corrections
-    float y[NT][4];
+    const unsigned char *xp[NT];     // current chunk
+    const float *cp = corr;          // current chunk's offset corrections (nibbles)
+    float y[NT][4], y2[NT][4];
 
     auto store_unit = [&]() {
+        float rs0 = 1.0f, rs1 = 1.0f;
+        if constexpr (KIND == kFp8) {
+            rs0 = c_rg < c_N ? c_rs[c_rg] : 0.0f;
+            rs1 = c_rg + 8 < c_N ? c_rs[c_rg + 8] : 0.0f;
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int m = nt * 8 + 2 * t + (e & 1);
                 const int row = e < 2 ? c_rg : c_rg + 8;
-                if (m < M && row < c_N) c_y[static_cast<size_t>(m) * c_N + row] = y[nt][e];
+                float val = y[nt][e];
+                if constexpr (KIND != kNib) val = __fadd_rn(val, y2[nt][e]);
+                if constexpr (KIND == kFp8) val = __fmul_rn(e < 2 ? rs0 : rs1, val);
+                if (m < M && row < c_N) c_y[static_cast<size_t>(m) * c_N + row] = val;
             }
         }
     };
@@ -312,12 +350,13 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         }
         if (!in_unit) {
             const Prob &P = B.p[c_pi];
-            c_N = P.n; c_K = P.k; c_ng = c_K / G; c_x = P.x; c_y = P.y;
+            c_N = P.n; c_K = P.k; c_ng = c_K / CH; c_x = P.x; c_y = P.y;
+            c_rs = static_cast<const float *>(P.scales);
             c_rg = (c_u - P.unit_begin) * ROWS + warp * 16 + g;
             c_grp = 0;
             in_unit = true;
             if (staged_pi != c_pi) {
-                cps = (B.xs_bytes - M * kRowPad) / (M * CHB + MT * 4);
+                cps = (B.xs_bytes - M * kRowPad) / (M * CHB + CORR);
                 cps = cps >= c_ng ? c_ng : max(1, cps);
                 RS = cps * CHB + kRowPad;
                 corr = reinterpret_cast<float *>(smem + M * RS);
@@ -331,7 +370,7 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) y[nt][e] = 0.0f;
+                for (int e = 0; e < 4; ++e) { y[nt][e] = 0.0f; y2[nt][e] = 0.0f; }
         }
         seg_end = min(c_ng, c_grp + cps);
         if (staged_pi != c_pi || staged_begin != c_grp) {
@@ -346,51 +385,82 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         cp = corr + 2 * t;
     };
 
-    // one quantisation group of this warp's 16 rows
-    auto compute = [&](const NibSlot<PLANES, G> &S) {
-        if (c_grp == seg_end) event();
-        float accA[NT][PLANES][4], accB[NT][PLANES][4];
+    // E4M3 / fp16 chunk: lane t holds IPL consecutive inputs of rows g, g+8;
+    // each 16-byte activation piece covers words 2 pc and 2 pc + 1
+    auto fp_chunk = [&](const Slot<KIND, PLANES, G> &S, float (&acc)[NT][4]) {
 #pragma unroll
-        for (int wd = 0; wd < WORDS; ++wd) {
+        for (int pc = 0; pc < Gm::PIECES; ++pc) {
             uint4 bq[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xp[nt] + wd * 64);
+            for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xp[nt] + pc * 64);
+            // this piece covers words 2 pc and 2 pc + 1 of each row (4 inputs per word)
 #pragma unroll
-            for (int p = 0; p < PLANES; ++p) {
-                const NibPairs a = nib_pairs(S.w[p][0][wd]), b = nib_pairs(S.w[p][1][wd]);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a0, a1, a2, a3;
+                if constexpr (KIND == kFp8) {
+                    e4m3x4_to_f16x2x2(S.w[0][0][2 * pc + h], a0, a2);
+                    e4m3x4_to_f16x2x2(S.w[0][1][2 * pc + h], a1, a3);
+                } else {
+                    a0 = S.w[0][0][2 * h]; a2 = S.w[0][0][2 * h + 1];
+                    a1 = S.w[0][1][2 * h]; a3 = S.w[0][1][2 * h + 1];
+                }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (wd == 0) {
-                        const float2 cc = *reinterpret_cast<const float2 *>(cp + nt * 8);
-                        mma_f16_c(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y, cc.x, cc.y, cc.x, cc.y);
-                        mma_f16_c(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w, 0.f, 0.f, 0.f, 0.f);
-                    } else {
-                        mma_f16(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y);
-                        mma_f16(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w);
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16(acc[nt], a0, a1, a2, a3, h ? bq[nt].z : bq[nt].x, h ? bq[nt].w : bq[nt].y);
+            }
+        }
+    };
+
+    // one chunk of this warp's 16 rows; `odd` picks the accumulator set of the
+    // E4M3 / fp16 kinds (two independent chains, summed at the unit end)
+    auto compute = [&](const Slot<KIND, PLANES, G> &S, bool odd) {
+        if (c_grp == seg_end) event();
+        if constexpr (KIND == kNib) {
+            float accA[NT][PLANES][4], accB[NT][PLANES][4];
+#pragma unroll
+            for (int wd = 0; wd < WORDS; ++wd) {
+                uint4 bq[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xp[nt] + wd * 64);
+#pragma unroll
+                for (int p = 0; p < PLANES; ++p) {
+                    const NibPairs a = nib_pairs(S.w[p][0][wd]), b = nib_pairs(S.w[p][1][wd]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (wd == 0) {
+                            const float2 cc = *reinterpret_cast<const float2 *>(cp + nt * 8);
+                            mma_f16_c(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y, cc.x, cc.y, cc.x, cc.y);
+                            mma_f16_c(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w, 0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            mma_f16(accA[nt][p], a.lo1, b.lo1, a.hi1, b.hi1, bq[nt].x, bq[nt].y);
+                            mma_f16(accB[nt][p], a.lo16, b.lo16, a.hi16, b.hi16, bq[nt].z, bq[nt].w);
+                        }
                     }
                 }
             }
-        }
-        // group scale x 2^24 (undoes the subnormal encoding); refinement plane at s/16
-        const float s0f = __fmul_rn(__half2float(__ushort_as_half(S.s[0])), 16777216.0f);
-        const float s1f = __fmul_rn(__half2float(__ushort_as_half(S.s[1])), 16777216.0f);
+            // group scale x 2^24 (undoes the subnormal encoding); refinement plane at s/16
+            const float s0f = __fmul_rn(__half2float(__ushort_as_half(S.s[0])), 16777216.0f);
+            const float s1f = __fmul_rn(__half2float(__ushort_as_half(S.s[1])), 16777216.0f);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float sc = e < 2 ? s0f : s1f;
-                y[nt][e] = __fmaf_rn(sc, __fadd_rn(accA[nt][0][e], accB[nt][0][e]), y[nt][e]);
-                if constexpr (PLANES == 2)
-                    y[nt][e] = __fmaf_rn(__fmul_rn(sc, 0.0625f), __fadd_rn(accA[nt][1][e], accB[nt][1][e]), y[nt][e]);
+                for (int e = 0; e < 4; ++e) {
+                    const float sc = e < 2 ? s0f : s1f;
+                    y[nt][e] = __fmaf_rn(sc, __fadd_rn(accA[nt][0][e], accB[nt][0][e]), y[nt][e]);
+                    if constexpr (PLANES == 2)
+                        y[nt][e] = __fmaf_rn(__fmul_rn(sc, 0.0625f), __fadd_rn(accA[nt][1][e], accB[nt][1][e]), y[nt][e]);
+                }
             }
+            cp += MT;
+        } else {
+            if (odd) fp_chunk(S, y2); else fp_chunk(S, y);
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) xp[nt] += xstep[nt];
-        cp += MT;
         ++c_grp;
     };
 
-    NibSlot<PLANES, G> ring[R];
+    Slot<KIND, PLANES, G> ring[R];
     l_setup();
 #pragma unroll
     for (int i = 0; i < R - 1; ++i)
@@ -401,7 +471,7 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             issue(ring[(i + R - 1) % R]);
-            compute(ring[i]);
+            compute(ring[i], (i & 1) != 0);
         }
     }
     for (; s0 < steps; s0 += R) {                  // tail
@@ -409,170 +479,11 @@ nib_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         for (int i = 0; i < R; ++i) {
             if (s0 + i < steps) {
                 if (s0 + i + R - 1 < steps) issue(ring[(i + R - 1) % R]);
-                compute(ring[i]);
+                compute(ring[i], (i & 1) != 0);
             }
         }
     }
     if (in_unit) store_unit();
-}
-
-// ------------------------------------------------------------------ FP8 / FP16 tier kernel
-
-template <int KIND>
-struct FpGeom {
-    static constexpr int CH = KIND == kFp8 ? 64 : 32;   // inputs per chunk
-    static constexpr int ROWB_NUM = KIND == kFp8 ? 1 : 2;   // row bytes = k * ROWB_NUM
-};
-
-constexpr int kFpWarps = 4;
-
-template <int KIND, int NT, int MAXP>
-__global__ void __launch_bounds__(kFpWarps * 32)
-fp_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
-{
-    constexpr int THREADS = kFpWarps * 32;
-    constexpr int CH = FpGeom<KIND>::CH, CHB = CH * 2;
-    constexpr int R = 5;          // ring slots: 4 chunks (2 rows x 16 B) in flight
-    constexpr int ROWS = 16 * kFpWarps;
-
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int M = B.M;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-
-    for (int u = blockIdx.x; u < B.total_units; u += gridDim.x) {
-        const Prob &P = B.p[find_problem(B, u)];
-        const int N = P.n, K = P.k, NCH = K / CH;
-        const int rg = (u - P.unit_begin) * ROWS + warp * 16 + g, rg8 = rg + 8;
-        const bool vg = rg < N, vg8 = rg8 < N;
-        const size_t rowb = static_cast<size_t>(K) * FpGeom<KIND>::ROWB_NUM;
-        const uint8_t *p0 = P.base + static_cast<size_t>(vg ? rg : 0) * rowb + 16 * t;
-        const uint8_t *p1 = P.base + static_cast<size_t>(vg8 ? rg8 : 0) * rowb + 16 * t;
-
-        int cps = (B.xs_bytes - M * kRowPad) / (M * CHB);
-        if (cps >= NCH) cps = NCH;
-        else cps = max(R, cps / R * R);
-        const int RS = cps * CHB + kRowPad;
-        unsigned char *xs = smem;
-
-        uint4 ring[R][2];
-#pragma unroll
-        for (int i = 0; i < R - 1; ++i)
-            if (i < NCH) {
-                ring[i][0] = ld_stream_v4(p0 + static_cast<size_t>(i) * 64);
-                ring[i][1] = ld_stream_v4(p1 + static_cast<size_t>(i) * 64);
-            }
-
-        auto stage = [&](int c_begin) {
-            const int nch = min(cps, NCH - c_begin);
-            const int items_row = nch * (CH / 8);
-            const int total = M * items_row;
-            bool range = false;
-            for (int i = threadIdx.x; i < total; i += THREADS) {
-                const int m = i / items_row, it = i % items_row;
-                const uint4 v = *reinterpret_cast<const uint4 *>(P.x + static_cast<size_t>(m) * K +
-                                                                 static_cast<size_t>(c_begin) * CH + it * 8);
-                const uint32_t src[4] = {v.x, v.y, v.z, v.w};
-                uint32_t h[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float lo = __uint_as_float(src[q] << 16), hi = __uint_as_float(src[q] & 0xFFFF0000u);
-                    range |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.0f;
-                    h[q] = pack_h2(lo, hi);
-                }
-                const int cl = it / (CH / 8), kk = (it % (CH / 8)) * 8;
-                const int pos = KIND == kFp8 ? 4 * ((kk % 16) / 8) + kk / 16 : kk / 8;
-                *reinterpret_cast<uint4 *>(xs + m * RS + cl * CHB + pos * 16) = make_uint4(h[0], h[1], h[2], h[3]);
-            }
-            if (range) set_status(status, NQ_DEV_ACT_RANGE);
-        };
-
-        __syncthreads();
-        stage(0);
-        __syncthreads();
-
-        const unsigned char *xrow[NT];
-        int xstep[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int m = nt * 8 + g;
-            xrow[nt] = xs + (m < M ? m : 0) * RS + t * 16;
-            xstep[nt] = m < M ? CHB : 0;
-        }
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-
-        for (int c0 = 0; c0 < NCH; c0 += R) {
-            if (c0 > 0 && c0 % cps == 0) {
-                __syncthreads();
-                stage(c0);
-                __syncthreads();
-            }
-            const int cbase = c0 % cps;
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int c = c0 + i;
-                if (c < NCH) {
-                    if (c + R - 1 < NCH) {
-                        ring[(i + R - 1) % R][0] = ld_stream_v4(p0 + static_cast<size_t>(c + R - 1) * 64);
-                        ring[(i + R - 1) % R][1] = ld_stream_v4(p1 + static_cast<size_t>(c + R - 1) * 64);
-                    }
-                    const uint4 wa = ring[i][0], wb = ring[i][1];
-                    const int cl = cbase + i;
-                    if constexpr (KIND == kFp8) {
-                        const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, Bw[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            uint4 bq[NT];
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt] + q * 64);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint32_t a0, a2, a1, a3;
-                                e4m3x4_to_f16x2x2(A[2 * q + h], a0, a2);
-                                e4m3x4_to_f16x2x2(Bw[2 * q + h], a1, a3);
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    mma_f16(acc[nt], a0, a1, a2, a3, h ? bq[nt].z : bq[nt].x, h ? bq[nt].w : bq[nt].y);
-                            }
-                        }
-                    } else {
-                        uint4 bq[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) bq[nt] = lds128(xrow[nt] + cl * xstep[nt]);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            mma_f16(acc[nt], wa.x, wb.x, wa.y, wb.y, bq[nt].x, bq[nt].y);
-                            mma_f16(acc[nt], wa.z, wb.z, wa.w, wb.w, bq[nt].z, bq[nt].w);
-                        }
-                    }
-                }
-            }
-        }
-
-        float rs0 = 1.0f, rs1 = 1.0f;
-        if constexpr (KIND == kFp8) {
-            const float *rsc = static_cast<const float *>(P.scales);
-            rs0 = vg ? rsc[rg] : 0.0f;
-            rs1 = vg8 ? rsc[rg8] : 0.0f;
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = nt * 8 + 2 * t + (e & 1);
-                const bool top = e < 2;
-                if (m < M && (top ? vg : vg8)) {
-                    float v = acc[nt][e];
-                    if constexpr (KIND == kFp8) v = __fmul_rn(top ? rs0 : rs1, v);
-                    P.y[static_cast<size_t>(m) * N + (top ? rg : rg8)] = v;
-                }
-            }
-        }
-    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -610,10 +521,10 @@ cudaError_t allow_large_smem(F kernel, std::atomic<int> &done)
     return e;
 }
 
-template <int PLANES, int G, int NT, int WARPS, int MAXP>
-cudaError_t launch_nib(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
+template <int KIND, int PLANES, int G, int NT, int WARPS, int MAXP>
+cudaError_t launch_stream(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
 {
-    auto k = nib_kernel<PLANES, G, NT, WARPS, MAXP>;
+    auto k = stream_kernel<KIND, PLANES, G, NT, WARPS, MAXP>;
     static std::atomic<int> attr{0};
     static std::atomic<int> occ[kXsMax / 1024 + 1];
     const cudaError_t e = allow_large_smem(k, attr);
@@ -623,26 +534,14 @@ cudaError_t launch_nib(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
     return cudaGetLastError();
 }
 
-template <int KIND, int NT, int MAXP>
-cudaError_t launch_fp(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
-{
-    auto k = fp_kernel<KIND, NT, MAXP>;
-    static std::atomic<int> attr{0};
-    static std::atomic<int> occ[kXsMax / 1024 + 1];
-    const cudaError_t e = allow_large_smem(k, attr);
-    if (e != cudaSuccess) return e;
-    const int grid = std::max(1, std::min(b.total_units, sm_count() * cached_occupancy(k, kFpWarps * 32, b.xs_bytes, occ)));
-    k<<<grid, kFpWarps * 32, b.xs_bytes, s>>>(b, status);
-    return cudaGetLastError();
-}
-
-template <int PLANES, int G, int NT, int MAXP>
-cudaError_t dispatch_nib_w(Batch<MAXP> &b, int warps, cudaStream_t s, unsigned int *st)
+template <int KIND, int PLANES, int G, int NT, int MAXP>
+cudaError_t dispatch_w(Batch<MAXP> &b, int warps, cudaStream_t s, unsigned int *st)
 {
     if constexpr (MAXP == kSmallBatch) {
-        return launch_nib<PLANES, G, NT, 4, MAXP>(b, s, st);
+        return launch_stream<KIND, PLANES, G, NT, 4, MAXP>(b, s, st);
     } else {
-        return warps == 8 ? launch_nib<PLANES, G, NT, 8, MAXP>(b, s, st) : launch_nib<PLANES, G, NT, 4, MAXP>(b, s, st);
+        return warps == 8 ? launch_stream<KIND, PLANES, G, NT, 8, MAXP>(b, s, st)
+                          : launch_stream<KIND, PLANES, G, NT, 4, MAXP>(b, s, st);
     }
 }
 
@@ -652,14 +551,14 @@ cudaError_t launch_kind(int kind, int planes, int group, int nt, int warps, Batc
 {
     if (kind == kNib) {
         if (planes == 1) {
-            if (group == 128) return nt == 1 ? dispatch_nib_w<1, 128, 1>(b, warps, s, st) : dispatch_nib_w<1, 128, 2>(b, warps, s, st);
-            return nt == 1 ? dispatch_nib_w<1, 64, 1>(b, warps, s, st) : dispatch_nib_w<1, 64, 2>(b, warps, s, st);
+            if (group == 128) return nt == 1 ? dispatch_w<kNib, 1, 128, 1>(b, warps, s, st) : dispatch_w<kNib, 1, 128, 2>(b, warps, s, st);
+            return nt == 1 ? dispatch_w<kNib, 1, 64, 1>(b, warps, s, st) : dispatch_w<kNib, 1, 64, 2>(b, warps, s, st);
         }
-        if (group == 128) return nt == 1 ? dispatch_nib_w<2, 128, 1>(b, warps, s, st) : dispatch_nib_w<2, 128, 2>(b, warps, s, st);
-        return nt == 1 ? dispatch_nib_w<2, 64, 1>(b, warps, s, st) : dispatch_nib_w<2, 64, 2>(b, warps, s, st);
+        if (group == 128) return nt == 1 ? dispatch_w<kNib, 2, 128, 1>(b, warps, s, st) : dispatch_w<kNib, 2, 128, 2>(b, warps, s, st);
+        return nt == 1 ? dispatch_w<kNib, 2, 64, 1>(b, warps, s, st) : dispatch_w<kNib, 2, 64, 2>(b, warps, s, st);
     }
-    if (kind == kFp8) return nt == 1 ? launch_fp<kFp8, 1>(b, s, st) : launch_fp<kFp8, 2>(b, s, st);
-    return nt == 1 ? launch_fp<kFp16, 1>(b, s, st) : launch_fp<kFp16, 2>(b, s, st);
+    if (kind == kFp8) return nt == 1 ? dispatch_w<kFp8, 1, 0, 1>(b, warps, s, st) : dispatch_w<kFp8, 1, 0, 2>(b, warps, s, st);
+    return nt == 1 ? dispatch_w<kFp16, 1, 0, 1>(b, warps, s, st) : dispatch_w<kFp16, 1, 0, 2>(b, warps, s, st);
 }
 
 // Validate one layer for the given pass; returns the kernel family.
@@ -691,7 +590,7 @@ int xs_bytes_for(int kind, int M, int kmax, int group)
     const int mt = M > 8 ? 16 : 8;
     const long long need = static_cast<long long>(M) * (chunks * 2 * ch + kRowPad) +
                            (kind == kNib ? static_cast<long long>(chunks) * mt * 4 : 0);
-    return static_cast<int>(std::min<long long>(need, kind == kNib ? kXsNib : kXsMax));
+    return static_cast<int>(std::min<long long>(need, kXsStage));
 }
 
 template <int MAXP>
@@ -712,8 +611,8 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
                 rows16 += (w[i0 + i].n_out + 15) / 16;
             }
             // 8-warp units when there are enough of them to fill the GPU twice
-            const int warps = (kind == kNib && MAXP == kLargeBatch && rows16 / 8 >= 2LL * sm_count()) ? 8 : 4;
-            const int rows_per_unit = kind == kNib ? 16 * warps : 16 * kFpWarps;
+            const int warps = (MAXP == kLargeBatch && rows16 / 8 >= 2LL * sm_count()) ? 8 : 4;
+            const int rows_per_unit = 16 * warps;
             long long units = 0, cost = 0;
             for (int i = 0; i < cnt; ++i) {
                 const nq_weights &L = w[i0 + i];
