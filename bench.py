@@ -283,15 +283,17 @@ def _pass_layers(device, shapes, fmt, group, seed, w16=False):
     return layers
 
 
-def _time_pass(device, layers, M, verify, iters=10):
-    """Device time of one batched launch over all layers at M activation rows."""
+def _time_pass(device, layers, M, verify, iters=10, tensor_cores=False):
+    """Device time of one batched call over all layers at M activation rows
+    (tensor_cores: the *_ws entry point, tensor-memory kernel at M >= 16,
+    including its activation pre-pass)."""
     import torch
     from quantized_self_speculative_gb300 import nq
     gen = torch.Generator(device=device)
     gen.manual_seed(123)
     xs = [torch.randn((M, L.k_in), generator=gen, device=device).to(torch.bfloat16) for L in layers]
     ys = [torch.empty((M, L.n_out), dtype=torch.float32, device=device) for L in layers]
-    b = nq.LinearBatch(verify, layers, xs, ys)
+    b = nq.LinearBatch(verify, layers, xs, ys, tensor_cores=tensor_cores)
     for _ in range(3):
         b()
     torch.cuda.synchronize()
@@ -321,15 +323,18 @@ def _shapes(spec):
 
 def config3_sweep(device):
     """LLaMA-3-8B-shaped linears, batch 16, k = 8: draft M = 16 (base plane),
-    verify M = 144 (both planes), groups 64 and 128."""
+    verify M = 144 (both planes), groups 64 and 128; the tensor-memory kernel
+    (the *_ws entry points) and, for comparison, the streaming kernel."""
     import torch
     from quantized_self_speculative_gb300 import nq, synth
     out = {}
     shapes = _shapes(synth.llama3_8b_linears)
     for g in (128, 64):
         layers = _pass_layers(device, shapes, nq.FMT_NESTED44, g, 31 + g)
-        out[f"g{g}"] = {"draft_M16": _time_pass(device, layers, 16, False),
-                        "verify_M144": _time_pass(device, layers, 144, True, iters=3)}
+        out[f"g{g}"] = {"draft_M16": _time_pass(device, layers, 16, False, tensor_cores=True),
+                        "verify_M144": _time_pass(device, layers, 144, True, tensor_cores=True),
+                        "draft_M16_stream_kernel": _time_pass(device, layers, 16, False),
+                        "verify_M144_stream_kernel": _time_pass(device, layers, 144, True, iters=2)}
         del layers
         torch.cuda.empty_cache()
     return out
@@ -404,7 +409,8 @@ def profile_case(case, layers=8):
         fmt = {"int4": nq.FMT_INT4, "fp8": nq.FMT_FP8E4M3_ROW, "fp16": nq.FMT_FP16}.get(case, nq.FMT_NESTED44)
         L = _pass_layers(device, shapes, fmt, 128 if fmt in (nq.FMT_NESTED44, nq.FMT_INT4) else 0, 1)
         M = {"draft": 1, "verify": 5, "draft16": 16, "verify144": 144, "int4": 1, "fp8": 5, "fp16": 5}[case]
-        print(json.dumps({"case": case, **_time_pass(device, L, M, case not in ("draft", "draft16", "int4"), iters=2)}))
+        print(json.dumps({"case": case, **_time_pass(device, L, M, case not in ("draft", "draft16", "int4"), iters=2,
+                                                      tensor_cores=case in ("draft16", "verify144"))}))
     else:
         B, k, V = 64, 4, 152064
         gen = torch.Generator(device=device)

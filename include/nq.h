@@ -61,7 +61,7 @@ typedef enum {
     NQ_ERR_CUDA = 4,       /* a CUDA runtime call failed (launch error, bad device) */
     NQ_ERR_NONFINITE = 5,  /* reported by nq_get_device_status(): non-finite logits */
     NQ_ERR_TIMEOUT = 6,    /* reserved: a bounded device wait gave up */
-    NQ_ERR_WORKSPACE = 7,  /* workspace smaller than spec_accept_workspace_bytes() */
+    NQ_ERR_WORKSPACE = 7,  /* workspace NULL or smaller than the *_workspace_bytes() size */
     NQ_ERR_TOKEN = 8       /* reported by nq_get_device_status(): draft id outside [0, V) */
 } nq_status;
 
@@ -155,6 +155,34 @@ NQ_API nq_status nq_draft_gemv_batch(int count, const nq_weights *w, const uint1
                               float *const *y, cudaStream_t stream);
 NQ_API nq_status nq_verify_gemm_batch(int count, const nq_weights *w, const uint16_t *const *x, int M,
                                float *const *y, cudaStream_t stream);
+
+/*
+ * Batched speculative rounds (many sequences, M = B (k+1) of a few tens to
+ * hundreds of rows) turn the same linears into dense contractions.  These two
+ * calls take a device workspace and, when M >= 16 and every layer is NESTED44
+ * (or INT4 for the draft) with k_in % 128 == 0, run the contraction on the
+ * tensor cores with the decoded weights in tensor memory: one pre-pass writes
+ * the activations as fp16 into the workspace, then each CTA decodes 128
+ * weight rows to fp16(q8 * s/16) (verify) or fp16(q4 * s) (draft), each
+ * weight rounded once to fp16, and accumulates in fp32 (activations rounded
+ * bf16 -> fp16 as above).  Results agree with nq_*_batch to fp16 weight
+ * rounding (well inside the 2e-3 normwise bound) but are not bit-identical
+ * to them, and M >= 16 rows are not batch-invariant with respect to M < 16.
+ * Other cases run exactly as nq_draft_gemv_batch / nq_verify_gemm_batch and
+ * ignore ws.  M > 256 is processed in chunks of 256 rows.
+ *
+ * nq_linear_workspace_bytes() gives the workspace size in bytes (host-only;
+ * 0 when the tensor-core path is not taken or the arguments are invalid).
+ * The workspace is caller-owned device memory, 16-byte aligned, needs no
+ * initialisation and must not be used by another call that may run at the
+ * same time.  NQ_ERR_WORKSPACE if ws is NULL or smaller than that size.
+ * A bounded internal wait that gives up sets NQ_DEV_TIMEOUT.
+ */
+NQ_API size_t nq_linear_workspace_bytes(int count, const nq_weights *w, int M, int verify);
+NQ_API nq_status nq_draft_gemv_batch_ws(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                                 float *const *y, void *ws, size_t ws_bytes, cudaStream_t stream);
+NQ_API nq_status nq_verify_gemm_batch_ws(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                                  float *const *y, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Device workspace for the acceptance calls, in bytes (host-only).  The

@@ -35,6 +35,14 @@
 #include "nq_internal.cuh"
 
 namespace nq {
+// Tensor-memory path for M >= 16 (nq_tc.cu).
+bool tc_route(int count, const nq_weights *w, int M, bool verify);
+size_t tc_workspace_bytes(int count, const nq_weights *w, int M);
+nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M, float *const *y, bool verify,
+                 void *ws, cudaStream_t stream);
+}  // namespace nq
+
+namespace nq {
 namespace {
 
 constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
@@ -645,7 +653,8 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
 }
 
 nq_status linear_entry(int count, const nq_weights *w, const uint16_t *const *x, int M, float *const *y,
-                       bool verify, cudaStream_t stream)
+                       bool verify, cudaStream_t stream, bool with_ws = false, void *ws = nullptr,
+                       size_t ws_bytes = 0)
 {
     if (count < 1 || !w || !x || !y) return NQ_ERR_ARG;
     if (M < 1 || M > 4096) return NQ_ERR_ARG;
@@ -659,6 +668,11 @@ nq_status linear_entry(int count, const nq_weights *w, const uint16_t *const *x,
         else if (k2 != kind || p2 != planes || g2 != group) return NQ_ERR_ARG;   // one kernel family per call
         if (!x[i] || !y[i]) return NQ_ERR_ARG;
         if (!aligned16(x[i]) || !aligned16(y[i])) return NQ_ERR_ALIGN;
+    }
+    if (with_ws && tc_route(count, w, M, verify)) {
+        if (!ws || ws_bytes < tc_workspace_bytes(count, w, M)) return NQ_ERR_WORKSPACE;
+        if (!aligned16(ws)) return NQ_ERR_ALIGN;
+        return tc_run(count, w, x, M, y, verify, ws, stream);
     }
     return count <= kSmallBatch ? run_batch<kSmallBatch>(count, w, x, M, y, kind, planes, group, stream)
                                 : run_batch<kLargeBatch>(count, w, x, M, y, kind, planes, group, stream);
@@ -689,4 +703,26 @@ extern "C" nq_status nq_verify_gemm_batch(int count, const nq_weights *w, const 
                                           float *const *y, cudaStream_t stream)
 {
     return nq::linear_entry(count, w, x, M, y, true, stream);
+}
+
+extern "C" size_t nq_linear_workspace_bytes(int count, const nq_weights *w, int M, int verify)
+{
+    if (count < 1 || !w || M < 1 || M > 4096) return 0;
+    for (int i = 0; i < count; ++i) {
+        int k2, p2;
+        if (nq::check_layer(w[i], verify != 0, k2, p2) != NQ_OK) return 0;
+    }
+    return nq::tc_route(count, w, M, verify != 0) ? nq::tc_workspace_bytes(count, w, M) : 0;
+}
+
+extern "C" nq_status nq_draft_gemv_batch_ws(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                                            float *const *y, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return nq::linear_entry(count, w, x, M, y, false, stream, true, ws, ws_bytes);
+}
+
+extern "C" nq_status nq_verify_gemm_batch_ws(int count, const nq_weights *w, const uint16_t *const *x, int M,
+                                             float *const *y, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return nq::linear_entry(count, w, x, M, y, true, stream, true, ws, ws_bytes);
 }

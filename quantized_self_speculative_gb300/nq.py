@@ -55,6 +55,11 @@ def lib():
                 getattr(L, name).argtypes = [W, vp, i32, vp, vp]
             for name in ("nq_draft_gemv_batch", "nq_verify_gemm_batch"):
                 getattr(L, name).argtypes = [i32, W, C.POINTER(vp), i32, C.POINTER(vp), vp]
+            for name in ("nq_draft_gemv_batch_ws", "nq_verify_gemm_batch_ws"):
+                getattr(L, name).argtypes = [i32, W, C.POINTER(vp), i32, C.POINTER(vp), vp, sz, vp]
+                getattr(L, name).restype = i32
+            L.nq_linear_workspace_bytes.argtypes = [i32, W, i32, i32]
+            L.nq_linear_workspace_bytes.restype = sz
             L.spec_accept_workspace_bytes.argtypes = [i32, i32, i32]
             L.spec_accept_workspace_bytes.restype = sz
             L.spec_accept_greedy.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
@@ -167,12 +172,21 @@ def verify_gemm(w: PackedLinear, x: torch.Tensor, y=None, stream=None) -> torch.
     return _linear("nq_verify_gemm", w, x, y, stream)
 
 
+def linear_workspace_bytes(verify: bool, layers: Sequence[PackedLinear], M: int) -> int:
+    """Workspace of nq_{draft_gemv,verify_gemm}_batch_ws (0: the tensor-core
+    path is not taken for these layers and M)."""
+    w = (nq_weights * len(layers))(*[L.struct() for L in layers])
+    return lib().nq_linear_workspace_bytes(len(layers), w, M, int(verify))
+
+
 class LinearBatch:
     """Prebuilt argument arrays for nq_{draft_gemv,verify_gemm}_batch: one
-    persistent launch over many independent linears at the same M."""
+    persistent launch over many independent linears at the same M.  With
+    tensor_cores=True the *_batch_ws entry point is used with a workspace
+    allocated here (the tensor-memory kernel for M >= 16)."""
 
     def __init__(self, verify: bool, layers: Sequence[PackedLinear], xs: Sequence[torch.Tensor],
-                 ys: Sequence[torch.Tensor]):
+                 ys: Sequence[torch.Tensor], tensor_cores: bool = False):
         n = len(layers)
         assert n == len(xs) == len(ys) and n > 0
         self.fn = "nq_verify_gemm_batch" if verify else "nq_draft_gemv_batch"
@@ -185,10 +199,19 @@ class LinearBatch:
         self.w = (nq_weights * n)(*[L.struct() for L in layers])
         self.x = (C.c_void_p * n)(*[x.data_ptr() for x in xs])
         self.y = (C.c_void_p * n)(*[y.data_ptr() for y in ys])
+        self.ws = None
+        if tensor_cores:
+            self.fn += "_ws"
+            nb = lib().nq_linear_workspace_bytes(n, self.w, self.M, int(verify))
+            self.ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=xs[0].device)
         self._keep = (list(layers), list(xs), list(ys))
 
     def __call__(self, stream=None):
-        _check(getattr(lib(), self.fn)(self.count, self.w, self.x, self.M, self.y, _stream(stream)), self.fn)
+        if self.ws is None:
+            _check(getattr(lib(), self.fn)(self.count, self.w, self.x, self.M, self.y, _stream(stream)), self.fn)
+        else:
+            _check(getattr(lib(), self.fn)(self.count, self.w, self.x, self.M, self.y, self.ws.data_ptr(),
+                                           self.ws.numel(), _stream(stream)), self.fn)
 
 
 # ---------------------------------------------------------------- acceptance

@@ -70,6 +70,40 @@ def test_workspace_bytes(L):
         assert nq.workspace_bytes(*bad) == 0
 
 
+def test_linear_workspace_bytes(L):
+    """Workspace of the tensor-core linears: fp16 activations of each layer
+    (N padded to a multiple of 16, at most 256 rows per launch), 1024-byte
+    regions, the largest launch of 128 layers; 0 where the path is not taken."""
+    from quantized_self_speculative_gb300 import nq
+    A = 0x10000
+    a1k = lambda n: (n + 1023) // 1024 * 1024
+
+    def layers(shapes, fmt=nq.FMT_NESTED44, g=128):
+        return (nq.nq_weights * len(shapes))(*[nq.nq_weights(n, k, g, fmt, A, A, A) for n, k in shapes])
+
+    one = layers([(4096, 4096)])
+    assert L.nq_linear_workspace_bytes(1, one, 144, 1) == a1k(2 * 144 * 4096)
+    assert L.nq_linear_workspace_bytes(1, one, 16, 0) == a1k(2 * 16 * 4096)
+    assert L.nq_linear_workspace_bytes(1, one, 17, 1) == a1k(2 * 32 * 4096)
+    assert L.nq_linear_workspace_bytes(1, one, 1000, 1) == a1k(2 * 256 * 4096)
+    assert L.nq_linear_workspace_bytes(1, one, 15, 1) == 0                  # streaming kernel
+    mix = layers([(1024, 4096), (4096, 14336), (333, 384)])
+    assert L.nq_linear_workspace_bytes(3, mix, 40, 1) == sum(a1k(2 * 48 * k) for k in (4096, 14336, 384))
+    many = layers([(512, 4096)] * 200)
+    assert L.nq_linear_workspace_bytes(200, many, 64, 1) == 128 * a1k(2 * 64 * 4096)
+    assert L.nq_linear_workspace_bytes(1, layers([(256, 192)], g=64), 64, 1) == 0   # k % 128 != 0
+    assert L.nq_linear_workspace_bytes(1, layers([(256, 512)], fmt=nq.FMT_INT4), 64, 0) == a1k(2 * 64 * 512)
+    assert L.nq_linear_workspace_bytes(1, layers([(256, 512)], fmt=nq.FMT_INT4), 64, 1) == 0   # invalid pair
+    assert L.nq_linear_workspace_bytes(1, layers([(256, 512)], fmt=nq.FMT_FP16, g=0), 64, 1) == 0
+    # a missing or short workspace is rejected before any launch
+    ptrs = (C.c_void_p * 1)(A)
+    need = L.nq_linear_workspace_bytes(1, one, 144, 1)
+    assert L.nq_verify_gemm_batch_ws(1, one, ptrs, 144, ptrs, None, need, None) == nq.NQ_ERR_WORKSPACE
+    assert L.nq_verify_gemm_batch_ws(1, one, ptrs, 144, ptrs, A, need - 16, None) == nq.NQ_ERR_WORKSPACE
+    assert L.nq_verify_gemm_batch_ws(1, one, ptrs, 144, ptrs, A + 8, need, None) == nq.NQ_ERR_ALIGN
+    assert L.nq_draft_gemv_batch_ws(1, one, ptrs, 0, ptrs, A, need, None) == nq.NQ_ERR_ARG
+
+
 def test_status_strings(L):
     from quantized_self_speculative_gb300 import nq
     assert nq.status_string(0) == "NQ_OK"
