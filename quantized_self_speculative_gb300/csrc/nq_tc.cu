@@ -8,18 +8,23 @@
 // does 288 FLOP per weight byte, beyond any warp-MMA path.  Here each CTA owns
 // a tile of 128 weight rows and streams its K:
 //
-//   * warps 0-3 (one thread per weight row = one tensor-memory lane) load the
-//     packed nibbles and the group scale straight from HBM into a register
-//     ring and write the decoded weights, fp16(q * s) exactly rounded, into a
-//     tensor-memory A stage (64 columns per 128 inputs) with tcgen05.st;
-//   * warp 8 copies the activations of the k-block (already fp16, in the
+//   * warp 22 loads the packed nibble planes of the tile's next k-blocks
+//     into shared-memory stages with TMA (one 128-row x 64-byte box per
+//     plane, 64-byte swizzle) and their group scales with cp.async, several
+//     k-blocks ahead;
+//   * warps 0-15 (one thread per weight row = one tensor-memory lane; two
+//     groups of eight take alternate k-blocks, two warps per row quarter
+//     each taking half of the k-block) decode the
+//     weights to fp16(q * s), exactly rounded, into a tensor-memory A stage
+//     (64 columns per 128 inputs) with tcgen05.st;
+//   * warp 20 copies the activations of the k-block (already fp16, in the
 //     MMA's 128-byte-swizzled K-major layout, written once per call by
 //     tc_stage_kernel into the caller's workspace) into a shared-memory B
 //     stage with one bulk copy;
-//   * warp 9 issues tcgen05.mma (M = 128, N = padded M, K = 16; A from tensor
+//   * warp 21 issues tcgen05.mma (M = 128, N = padded M, K = 16; A from tensor
 //     memory, B from shared memory, fp32 accumulators in tensor memory) and
 //     tcgen05.commit to release the stages;
-//   * warps 4-7 read the finished accumulators (tcgen05.ld) and store y.
+//   * warps 16-19 read the finished accumulators (tcgen05.ld) and store y.
 //
 // Decoding: offset-binary codes land in fp16 subnormals (code * 2^-24) with
 // integer masks only; one fma per pair, fma(code * 2^-24, s * 2^20, -8 s),
@@ -31,8 +36,12 @@
 // tensor memory and returns.
 #include "nq_internal.cuh"
 
+#include <cuda.h>           // CUtensorMap (types only; the encoder is fetched through the runtime)
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 namespace nq {
 namespace {
@@ -41,8 +50,8 @@ constexpr int kTcMinM = 16;            // smallest M routed here
 constexpr int kTcMaxN = 256;           // activation rows per launch (MMA N)
 constexpr int kTcTile = 128;           // weight rows per tile (MMA M)
 constexpr int kTcKB = 128;             // inputs per k-block (8 MMAs of K = 16)
-constexpr int kTcMaxP = 128;           // linears per launch
-constexpr int kTcThreads = 320;        // warps 0-3 decode, 4-7 epilogue, 8 copy, 9 MMA
+constexpr int kTcMaxP = 64;            // linears per launch (two 128-byte tensor maps each)
+constexpr int kTcThreads = 736;        // warps 0-15 decode, 16-19 epilogue, 20 B copy, 21 MMA, 22 weight loads
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 
@@ -53,13 +62,12 @@ struct TcProb {
     const uint16_t *x;     // bf16 [M][k] (rows of this M chunk)
     uint16_t *xs;          // staged fp16 activations in the workspace
     float *y;              // fp32 [M][n] (rows of this M chunk)
-    long long cost_begin;  // prefix of tiles * k over the batch
     int n, k, tile_begin, pad;
 };
 
 struct TcBatch {
-    long long total_cost;
-    int count, total_tiles, M, Npad, group, sb, sa, nd;
+    CUtensorMap maps[kTcMaxP][2];   // base / refinement plane: uint8 [n][k/2], box 64 B x 128 rows, 64-byte swizzle
+    int count, total_tiles, M, Npad, group, sb, sa, nd, ws;
     TcProb p[kTcMaxP];
 };
 
@@ -80,11 +88,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// try_wait with a suspend-time hint: a waiting warp sleeps (up to 10 ms) until
+// the phase completes instead of spinning and taking issue slots from the
+// warps that do the work.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(10000000u) : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ unsigned long long global_ns()
@@ -93,30 +104,47 @@ __device__ __forceinline__ unsigned long long global_ns()
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Wait for the phase of `bar` with the given parity.  Gives up after kWaitNs
 // (sets the CTA's abort flag and NQ_DEV_TIMEOUT) or when another role of the
 // CTA has given up; returns false then.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned int *status)
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            unsigned int *status)
 {
-    if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    for (unsigned int i = 1;; ++i) {
+    for (;;) {
         if (mbar_try(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitNs) {
-                *abort_flag = 1;
-                set_status(status, NQ_DEV_TIMEOUT);
-                return false;
-            }
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            set_status(status, NQ_DEV_TIMEOUT);
+            return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status)
+{
+    return mbar_test(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, status);
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// One lane of a converged warp (the warp's loop state stays warp-uniform, so
+// descriptors and addresses live in uniform registers for tcgen05 issue).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile("{ .reg .b32 r; .reg .pred p; elect.sync r|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(e));
+    return e != 0;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -187,19 +215,13 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b)
     return d;
 }
 __device__ __forceinline__ uint32_t dup_h(unsigned short h) { return static_cast<uint32_t>(h) * 0x10001u; }
-// 16-byte read-only load kept in L1: the 32 lanes of a warp read 32 rows, and
-// the second half of each 32-byte sector is used by the next load.
-__device__ __forceinline__ uint4 ld_nc_v4(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
 // Per-group decoding constants: fast = fma(code * 2^-24, F, C) with F = s 2^20,
 // C = -8 s (both exact in fp16 when s <= 0x2BFF); slow = (1024 + code) - bias,
-// times s16 (s/16 for the verify codes, s for the draft codes).
+// times S (s/16 for the verify codes, s for the draft codes).  For a normal s
+// the constants are exponent shifts of its bits (F: +20, C: +3 and negate,
+// s/16: -4); s = 0 gives zeros; subnormal s (below 2^-14) goes through fp32.
 struct GroupK {
     uint32_t F, C, S;
     bool fast;
@@ -208,59 +230,60 @@ template <int PLANES>
 __device__ __forceinline__ GroupK group_consts(unsigned short s_bits)
 {
     GroupK g;
-    const float s = __half2float(__ushort_as_half(s_bits));
-    g.fast = (s_bits & 0x7FFFu) <= 0x2BFFu;
-    g.F = dup_h(__half_as_ushort(__float2half_rn(__fmul_rn(s, 1048576.0f))));
-    g.C = dup_h(__half_as_ushort(__float2half_rn(__fmul_rn(s, -8.0f))));
-    g.S = dup_h(__half_as_ushort(__float2half_rn(PLANES == 2 ? __fmul_rn(s, 0.0625f) : s)));
+    const uint32_t sb = s_bits & 0x7FFFu;
+    g.fast = sb <= 0x2BFFu;
+    if (sb >= 0x0400u || sb == 0u) {
+        const uint32_t sign = s_bits & 0x8000u;
+        const uint32_t f = sb ? (sb + (20u << 10)) | sign : 0u;
+        const uint32_t c = sb ? ((sb + (3u << 10)) | 0x8000u) ^ sign : 0u;
+        const uint32_t sv = (PLANES == 2 ? (sb >= (5u << 10) ? sb - (4u << 10) : 0u) : sb) | sign;
+        g.F = f * 0x10001u;
+        g.C = c * 0x10001u;
+        g.S = sv * 0x10001u;
+        if (PLANES == 2 && sb != 0 && sb < (5u << 10)) {   // s/16 subnormal (s < 2^-10): exact via fp32
+            g.S = dup_h(__half_as_ushort(__float2half_rn(__fmul_rn(__half2float(__ushort_as_half(s_bits)), 0.0625f))));
+        }
+    } else {
+        const float s = __half2float(__ushort_as_half(s_bits));
+        g.F = dup_h(__half_as_ushort(__float2half_rn(__fmul_rn(s, 1048576.0f))));
+        g.C = dup_h(__half_as_ushort(__float2half_rn(__fmul_rn(s, -8.0f))));
+        g.S = dup_h(__half_as_ushort(__float2half_rn(PLANES == 2 ? __fmul_rn(s, 0.0625f) : s)));
+    }
     return g;
 }
 
 // Decode one 32-bit word per plane (8 consecutive inputs) into 4 fp16x2
-// registers in the MMA order (0,4)(1,5)(2,6)(3,7).
-template <int PLANES>
+// registers in the MMA order (0,4)(1,5)(2,6)(3,7).  FAST: one fma per pair;
+// otherwise the biased-integer path (any s).
+template <int PLANES, bool FAST>
 __device__ __forceinline__ void decode_word(uint32_t b, uint32_t r, const GroupK &g, uint32_t *o)
 {
-    uint32_t c0, c1, c2, c3;   // codes as fp16 subnormals: (q8 + 128) or 16 (q4 + 8), times 2^-24
+    uint32_t c[4];   // codes as fp16 subnormals: (q8 + 128) or 16 (q4 + 8), times 2^-24
     const uint32_t bx = b ^ 0x88888888u;
     if constexpr (PLANES == 2) {
         const uint32_t rx = r ^ 0x88888888u;
         // byte c of L: inputs 2c (base nibble high, refinement nibble low); H: inputs 2c+1
         const uint32_t L = (((bx << 4) & 0xF0F0F0F0u) | (rx & 0x0F0F0F0Fu)) - 0x08080808u;
         const uint32_t H = ((bx & 0xF0F0F0F0u) | ((rx >> 4) & 0x0F0F0F0Fu)) - 0x08080808u;
-        c0 = L & 0x00FF00FFu;
-        c1 = H & 0x00FF00FFu;
-        c2 = (L >> 8) & 0x00FF00FFu;
-        c3 = (H >> 8) & 0x00FF00FFu;
-        if (g.fast) {
-            o[0] = hfma2_u(c0, g.F, g.C);
-            o[1] = hfma2_u(c1, g.F, g.C);
-            o[2] = hfma2_u(c2, g.F, g.C);
-            o[3] = hfma2_u(c3, g.F, g.C);
-        } else {
-            const uint32_t bias = 0x64806480u;   // fp16 1152 = 1024 + 128
-            o[0] = hmul2_u(hsub2_u(c0 | 0x64006400u, bias), g.S);
-            o[1] = hmul2_u(hsub2_u(c1 | 0x64006400u, bias), g.S);
-            o[2] = hmul2_u(hsub2_u(c2 | 0x64006400u, bias), g.S);
-            o[3] = hmul2_u(hsub2_u(c3 | 0x64006400u, bias), g.S);
-        }
+        c[0] = L & 0x00FF00FFu;
+        c[1] = H & 0x00FF00FFu;
+        c[2] = (L >> 8) & 0x00FF00FFu;
+        c[3] = (H >> 8) & 0x00FF00FFu;
     } else {
         (void)r;
-        c0 = (bx << 4) & 0x00F000F0u;
-        c1 = bx & 0x00F000F0u;
-        c2 = (bx >> 4) & 0x00F000F0u;
-        c3 = (bx >> 8) & 0x00F000F0u;
-        if (g.fast) {
-            o[0] = hfma2_u(c0, g.F, g.C);
-            o[1] = hfma2_u(c1, g.F, g.C);
-            o[2] = hfma2_u(c2, g.F, g.C);
-            o[3] = hfma2_u(c3, g.F, g.C);
+        c[0] = (bx << 4) & 0x00F000F0u;
+        c[1] = bx & 0x00F000F0u;
+        c[2] = (bx >> 4) & 0x00F000F0u;
+        c[3] = (bx >> 8) & 0x00F000F0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (FAST) {
+            o[i] = hfma2_u(c[i], g.F, g.C);
         } else {
-            const uint32_t bias = 0x64086408u;   // fp16 1032 = 1024 + 8
-            o[0] = hmul2_u(hsub2_u((c0 >> 4) | 0x64006400u, bias), g.S);
-            o[1] = hmul2_u(hsub2_u((c1 >> 4) | 0x64006400u, bias), g.S);
-            o[2] = hmul2_u(hsub2_u((c2 >> 4) | 0x64006400u, bias), g.S);
-            o[3] = hmul2_u(hsub2_u((c3 >> 4) | 0x64006400u, bias), g.S);
+            const uint32_t slow = PLANES == 2 ? hmul2_u(hsub2_u(c[i] | 0x64006400u, 0x64806480u), g.S)    // 1152
+                                              : hmul2_u(hsub2_u((c[i] >> 4) | 0x64006400u, 0x64086408u), g.S);  // 1032
+            o[i] = g.fast ? hfma2_u(c[i], g.F, g.C) : slow;
         }
     }
 }
@@ -274,40 +297,6 @@ __device__ __forceinline__ int tile_problem(const TcBatch &B, int tile)
     }
     return lo;
 }
-// First tile whose cost prefix is >= target.
-__device__ __forceinline__ int tile_at_cost(const TcBatch &B, long long target)
-{
-    if (target >= B.total_cost) return B.total_tiles;
-    int lo = 0, hi = B.count - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (B.p[mid].cost_begin <= target) lo = mid; else hi = mid - 1;
-    }
-    const TcProb &P = B.p[lo];
-    return P.tile_begin + static_cast<int>((target - P.cost_begin + P.k - 1) / P.k);
-}
-
-// Walks the (tile, k-block) sequence of a CTA's tile range.
-struct Cursor {
-    int tile, pi, kb, nkb;
-    __device__ void init(const TcBatch &B, int t)
-    {
-        tile = t;
-        pi = tile_problem(B, t);
-        kb = 0;
-        nkb = B.p[pi].k / kTcKB;
-    }
-    __device__ void next(const TcBatch &B)
-    {
-        if (++kb == nkb) {
-            kb = 0;
-            ++tile;
-            while (pi + 1 < B.count && tile >= B.p[pi + 1].tile_begin) ++pi;
-            nkb = B.p[pi].k / kTcKB;
-        }
-    }
-};
-
 // ---------------------------------------------------------------- activation pre-pass
 // x (bf16, [M][k]) -> fp16 in the workspace, per k-block of 64 inputs a
 // [Npad][128 B] block: row m, 16-byte chunk c (inputs 8c..8c+7 in the order
@@ -344,13 +333,80 @@ __global__ void __launch_bounds__(256) tc_stage_kernel(const __grid_constant__ T
     if (range) set_status(status, NQ_DEV_ACT_RANGE);
 }
 
-// ---------------------------------------------------------------- main kernel
-template <int PLANES>
-struct DqSlot {
-    uint32_t b[16];
-    uint32_t r[PLANES == 2 ? 16 : 1];
-    unsigned short s[2];
+// Slot and phase parity of a ring of n mbarrier-guarded stages, advanced
+// incrementally (integer division by a runtime n is an emulated sequence).
+struct Ring {
+    int slot, phase, n;
+    __device__ explicit Ring(int n_, int start = 0) : slot(start % n_), phase((start / n_) & 1), n(n_) {}
+    __device__ void step(int by = 1)
+    {
+        slot += by;
+        if (slot >= n) { slot -= n; phase ^= 1; }
+    }
 };
+
+// ---------------------------------------------------------------- main kernel
+// Tiles are dealt round-robin (CTA c takes tiles c, c + grid, ...), so the
+// CTAs running at any moment work on neighbouring tiles of one or two linears
+// and share their staged activations in L2.
+struct TileSeq {
+    int tile, pi, kb, nkb;
+    __device__ void init(const TcBatch &B)
+    {
+        tile = blockIdx.x;
+        kb = 0;
+        if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / kTcKB; }
+        else { pi = 0; nkb = 1; }
+    }
+    __device__ void next(const TcBatch &B)
+    {
+        if (++kb == nkb) {
+            kb = 0;
+            tile += gridDim.x;
+            if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / kTcKB; }
+        }
+    }
+};
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async of this thread issued so far has landed
+// (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Weight stage: per plane 128 rows of 64 bytes as TMA writes them with the
+// 64-byte swizzle (address bits 4-5 XOR bits 7-8 of a 1024-byte aligned
+// stage): the 16-byte piece p of row r sits at piece position p ^ ((r >> 1) & 3),
+// so the 8 rows read by a quarter warp (same logical piece) fall in 8
+// different bank groups.
+constexpr int kWPitch = 64;
+__host__ __device__ constexpr uint32_t wpos(int row, int piece)
+{
+    return static_cast<uint32_t>(row * kWPitch + ((piece ^ ((row >> 1) & 3)) << 4));
+}
 
 template <int PLANES, int G>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ TcBatch B, unsigned int *status)
@@ -359,10 +415,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (sbase - raw);
-    const int Npad = B.Npad, SB = B.sb, SA = B.sa, ND = B.nd;
+    const int Npad = B.Npad, SB = B.sb, SA = B.sa, ND = B.nd, WS = B.ws;
     const uint32_t stage_bytes = 256u * static_cast<uint32_t>(Npad);
-    // barriers: a_full[4] a_empty[4] b_full[8] b_empty[8] d_full[2] d_empty[2] done
-    const uint32_t bars = sbase + static_cast<uint32_t>(SB) * stage_bytes;
+    constexpr uint32_t kPlaneBytes = kTcTile * kWPitch;
+    constexpr uint32_t kWStage = PLANES * kPlaneBytes + 1024;   // planes, 512 B of scales, pad to 1024
+    const uint32_t wbase = sbase + static_cast<uint32_t>(SB) * stage_bytes;
+    // barriers: a_full[4] a_empty[4] b_full[8] b_empty[8] d_full[2] d_empty[2] done w_full[12] w_empty[12]
+    const uint32_t bars = wbase + static_cast<uint32_t>(WS) * kWStage;
     auto A_FULL = [&](int i) { return bars + 8u * i; };
     auto A_EMPTY = [&](int i) { return bars + 8u * (4 + i); };
     auto B_FULL = [&](int i) { return bars + 8u * (8 + i); };
@@ -370,19 +429,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     auto D_FULL = [&](int i) { return bars + 8u * (24 + i); };
     auto D_EMPTY = [&](int i) { return bars + 8u * (26 + i); };
     const uint32_t DONE = bars + 8u * 28;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + static_cast<size_t>(SB) * stage_bytes + 8 * 32);
+    auto W_FULL = [&](int i) { return bars + 8u * (29 + i); };
+    auto W_EMPTY = [&](int i) { return bars + 8u * (41 + i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bars - sbase) + 8 * 56);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) { mbar_init(A_FULL(i), 4); mbar_init(A_EMPTY(i), 1); }
+        for (int i = 0; i < 4; ++i) { mbar_init(A_FULL(i), 8); mbar_init(A_EMPTY(i), 1); }
         for (int i = 0; i < 8; ++i) { mbar_init(B_FULL(i), 1); mbar_init(B_EMPTY(i), 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(D_FULL(i), 1); mbar_init(D_EMPTY(i), 4); }
         mbar_init(DONE, 1);
+        for (int i = 0; i < 12; ++i) { mbar_init(W_FULL(i), 33); mbar_init(W_EMPTY(i), 8); }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 8) {
+    if (warp == 20) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -392,115 +454,125 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int tb = tile_at_cost(B, B.total_cost * blockIdx.x / gridDim.x);
-    const int te = tile_at_cost(B, B.total_cost * (blockIdx.x + 1) / gridDim.x);
     int steps = 0;
-    if (tb < te) {
-        Cursor c;
-        c.init(B, tb);
-        for (int pi = c.pi; pi < B.count && B.p[pi].tile_begin < te; ++pi) {
-            const int t_end = pi + 1 < B.count ? B.p[pi + 1].tile_begin : B.total_tiles;
-            const int a = max(tb, B.p[pi].tile_begin), b = min(te, t_end);
-            steps += (b - a) * (B.p[pi].k / kTcKB);
-        }
-    }
+    for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) steps += B.p[tile_problem(B, t)].k / kTcKB;
     const uint32_t dcol0 = static_cast<uint32_t>(SA) * 64u;
 
-    if (warp < 4 && steps > 0) {
-        // ------------------------------------------------ decode warps
-        constexpr int R = PLANES == 2 ? 3 : 4;
-        const int row = threadIdx.x;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-        Cursor lc, cc;
-        lc.init(B, tb);
-        cc.init(B, tb);
-        DqSlot<PLANES> ring[R];
-        auto issue = [&](DqSlot<PLANES> &S) {
-            const TcProb &P = B.p[lc.pi];
-            const int n = (lc.tile - P.tile_begin) * kTcTile + row;
-            const size_t nn = static_cast<size_t>(n < P.n ? n : 0);
-            const size_t rowb = static_cast<size_t>(P.k) / 2;
-            const uint8_t *pb = P.base + nn * rowb + static_cast<size_t>(lc.kb) * 64;
+    if (warp == 22 && steps > 0) {
+        // ------------------------------------------------ weight loader: TMA boxes and scale words into stages
+        TileSeq q;
+        q.init(B);
+        int last_phase[12];
+        for (int i = 0; i < 12; ++i) last_phase[i] = -1;
+        Ring w(WS);
+        for (int it = 0; it < steps; ++it, w.step()) {
+            const int st = w.slot;
+            bool ok = mbar_wait(W_EMPTY(st), w.phase ^ 1, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const TcProb &P = B.p[q.pi];
+            const int r0 = (q.tile - P.tile_begin) * kTcTile;
+            const uint32_t dst = wbase + static_cast<uint32_t>(st) * kWStage;
+            if (lane == 0) {
+                // one arrival with the byte count; rows beyond n are zero-filled by TMA
+                mbar_expect_tx(W_FULL(st), PLANES * kPlaneBytes);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 v = ld_nc_v4(pb + 16 * q);
-                S.b[4 * q] = v.x; S.b[4 * q + 1] = v.y; S.b[4 * q + 2] = v.z; S.b[4 * q + 3] = v.w;
+                for (int p = 0; p < PLANES; ++p)
+                    tma_load_2d(dst + static_cast<uint32_t>(p) * kPlaneBytes, &B.maps[q.pi][p], q.kb * 64, r0, W_FULL(st));
             }
-            if constexpr (PLANES == 2) {
-                const uint8_t *pr = P.resid + nn * rowb + static_cast<size_t>(lc.kb) * 64;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 v = ld_nc_v4(pr + 16 * q);
-                    S.r[4 * q] = v.x; S.r[4 * q + 1] = v.y; S.r[4 * q + 2] = v.z; S.r[4 * q + 3] = v.w;
-                }
-            }
+            // group scales: the 4-byte word holding scale (n, kb * 128 / G) (G = 128: pick the half later)
             const int ng = P.k / G;
-            const uint16_t *ps = P.scales + nn * ng + static_cast<size_t>(lc.kb) * (kTcKB / G);
-            S.s[0] = ld_nc_u16(ps);
-            S.s[1] = G == 64 ? ld_nc_u16(ps + 1) : S.s[0];
-            lc.next(B);
-        };
-        int a_iter = 0;
-        bool ok = true;
-        auto compute = [&](const DqSlot<PLANES> &S) {
-            const int sa = a_iter % SA;
-            const uint32_t par = ((a_iter / SA) & 1) ^ 1;
-            bool w_ok = mbar_wait(A_EMPTY(sa), par, abort_flag, status);
-            w_ok = __all_sync(0xffffffffu, w_ok);
-            if (!w_ok) { ok = false; return; }
-            tc_fence_after();
-            const GroupK g0 = group_consts<PLANES>(S.s[0]);
-            const GroupK g1 = G == 64 ? group_consts<PLANES>(S.s[1]) : g0;
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                uint32_t v[16];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int wd = 4 * part + w;
-                    decode_word<PLANES>(S.b[wd], S.r[PLANES == 2 ? wd : 0], wd < 8 ? g0 : g1, &v[4 * w]);
-                }
-                tc_st16(lane_addr + static_cast<uint32_t>(64 * sa + 16 * part), v);
+            for (int j = 0; j < 4; ++j) {
+                const int row = 32 * j + lane;
+                const int n = r0 + row < P.n ? r0 + row : 0;
+                const size_t e = static_cast<size_t>(n) * ng + static_cast<size_t>(q.kb) * (kTcKB / G);
+                cp_async4(dst + PLANES * kPlaneBytes + row * 4, P.scales + (e & ~static_cast<size_t>(1)));
             }
+            cp_async_arrive(W_FULL(st));
+            last_phase[st] = w.phase;
+            q.next(B);
+        }
+        cp_async_wait_all();
+        // every TMA box issued has landed before the CTA may exit
+        if (lane == 0)
+            for (int i = 0; i < WS && i < 12; ++i)
+                if (last_phase[i] >= 0) {
+                    volatile int never = 0;
+                    mbar_wait(W_FULL(i), static_cast<uint32_t>(last_phase[i]), &never, status);
+                }
+    } else if (warp < 16 && steps > 0) {
+        // ------------------------------------------------ decode warps: two groups of eight take
+        // alternate k-blocks; in a group, warp w decodes rows 32 (w % 4) .. + 31 (its
+        // tensor-memory lane quarter) and inputs 64 h .. + 63 (h = (w / 4) % 2) of the
+        // k-block, i.e. A-stage columns 32 h .. + 31
+        const int grp = warp >> 3, half = (warp >> 2) & 1, row = 32 * (warp & 3) + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 32u * half;
+        TileSeq q;
+        q.init(B);
+        if (grp == 1) q.next(B);
+        Ring w(WS, grp), a(SA, grp);
+        for (int it = grp; it < steps; it += 2, w.step(2), a.step(2)) {
+            const int st = w.slot, sa = a.slot;
+            bool ok = mbar_wait(W_FULL(st), w.phase, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const uint32_t src = wbase + static_cast<uint32_t>(st) * kWStage;
+            uint32_t bw[8], rw[8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t at = src + wpos(row, 2 * half + j);
+                const uint4 v = lds128(at);
+                bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
+                const uint4 r = PLANES == 2 ? lds128(at + kPlaneBytes) : make_uint4(0, 0, 0, 0);
+                rw[4 * j] = r.x; rw[4 * j + 1] = r.y; rw[4 * j + 2] = r.z; rw[4 * j + 3] = r.w;
+            }
+            const uint32_t sw = lds32(wbase + static_cast<uint32_t>(st) * kWStage + PLANES * kPlaneBytes + row * 4);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(W_EMPTY(st));
+            // the scale word holds two consecutive scales: G = 64 -> this half's group is
+            // 2 kb + half; G = 128 -> group kb sits in the half given by its index parity
+            unsigned short sbits;
+            if (G == 64) {
+                sbits = static_cast<unsigned short>(half ? (sw >> 16) : (sw & 0xFFFFu));
+            } else {
+                const TcProb &P = B.p[q.pi];
+                const int n0 = (q.tile - P.tile_begin) * kTcTile + row;
+                const size_t e = static_cast<size_t>(n0 < P.n ? n0 : 0) * (P.k / G) + q.kb;
+                sbits = static_cast<unsigned short>((e & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+            }
+            const GroupK g = group_consts<PLANES>(sbits);
+            const bool all_fast = __all_sync(0xffffffffu, g.fast);
+            uint32_t v[32];
+            if (all_fast) {
+#pragma unroll
+                for (int w = 0; w < 8; ++w) decode_word<PLANES, true>(bw[w], rw[w], g, &v[4 * w]);
+            } else {
+#pragma unroll
+                for (int w = 0; w < 8; ++w) decode_word<PLANES, false>(bw[w], rw[w], g, &v[4 * w]);
+            }
+            ok = mbar_wait(A_EMPTY(sa), a.phase ^ 1, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            tc_st16(lane_addr + static_cast<uint32_t>(64 * sa), *reinterpret_cast<const uint32_t(*)[16]>(&v[0]));
+            tc_st16(lane_addr + static_cast<uint32_t>(64 * sa + 16), *reinterpret_cast<const uint32_t(*)[16]>(&v[16]));
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(A_FULL(sa));
-            ++a_iter;
-            cc.next(B);
-        };
-#pragma unroll
-        for (int i = 0; i < R - 1; ++i)
-            if (i < steps) issue(ring[i]);
-        int s0 = 0;
-        for (; ok && s0 + 2 * R - 2 < steps; s0 += R) {
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                issue(ring[(i + R - 1) % R]);
-                if (ok) compute(ring[i]);
-            }
+            q.next(B);
+            q.next(B);
         }
-        for (; ok && s0 < steps; s0 += R) {
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                if (s0 + i < steps && ok) {
-                    if (s0 + i + R - 1 < steps) issue(ring[(i + R - 1) % R]);
-                    compute(ring[i]);
-                }
-            }
-        }
-    } else if (warp < 8 && steps > 0) {
+    } else if (warp < 20 && steps > 0) {
         // ------------------------------------------------ epilogue warps
-        const int q = warp - 4;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        int d_iter = 0;
-        for (int tile = tb; tile < te; ++tile) {
-            const int db = d_iter % ND;
-            bool w_ok = mbar_wait(D_FULL(db), (d_iter / ND) & 1, abort_flag, status);
-            w_ok = __all_sync(0xffffffffu, w_ok);
-            if (!w_ok) break;
+        const int qd = warp - 16;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+        Ring d(ND);
+        for (int tile = blockIdx.x; tile < B.total_tiles; tile += gridDim.x, d.step()) {
+            const int db = d.slot;
+            bool w_ok = mbar_wait(D_FULL(db), d.phase, abort_flag, status);
+            if (!__all_sync(0xffffffffu, w_ok)) break;
             tc_fence_after();
             const TcProb &P = B.p[tile_problem(B, tile)];
-            const int n = (tile - P.tile_begin) * kTcTile + 32 * q + lane;
+            const int n = (tile - P.tile_begin) * kTcTile + 32 * qd + lane;
             const bool valid = n < P.n;
             for (int c0 = 0; c0 < Npad; c0 += 16) {
                 uint32_t v[16];
@@ -515,23 +587,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(D_EMPTY(db));
-            ++d_iter;
         }
-    } else if (warp == 8 && lane == 0 && steps > 0) {
+    } else if (warp == 20 && lane == 0 && steps > 0) {
         // ------------------------------------------------ activation copies
-        Cursor c;
-        c.init(B, tb);
+        TileSeq q;
+        q.init(B);
         int last_phase[8];
         for (int i = 0; i < 8; ++i) last_phase[i] = -1;
-        for (int it = 0; it < steps; ++it) {
-            const int sb = it % SB;
-            if (!mbar_wait(B_EMPTY(sb), ((it / SB) & 1) ^ 1, abort_flag, status)) break;
-            const TcProb &P = B.p[c.pi];
+        Ring r(SB);
+        for (int it = 0; it < steps; ++it, r.step()) {
+            const int sb = r.slot;
+            if (!mbar_wait(B_EMPTY(sb), r.phase ^ 1, abort_flag, status)) break;
+            const TcProb &P = B.p[q.pi];
             mbar_expect_tx(B_FULL(sb), stage_bytes);
             bulk_g2s(sbase + static_cast<uint32_t>(sb) * stage_bytes,
-                     P.xs + static_cast<size_t>(c.kb) * (stage_bytes / 2), stage_bytes, B_FULL(sb));
-            last_phase[sb] = (it / SB) & 1;
-            c.next(B);
+                     P.xs + static_cast<size_t>(q.kb) * (stage_bytes / 2), stage_bytes, B_FULL(sb));
+            last_phase[sb] = r.phase;
+            q.next(B);
         }
         // every copy issued has landed before the CTA may exit
         for (int i = 0; i < SB && i < 8; ++i)
@@ -539,40 +611,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 volatile int never = 0;
                 mbar_wait(B_FULL(i), static_cast<uint32_t>(last_phase[i]), &never, status);
             }
-    } else if (warp == 9 && lane == 0 && steps > 0) {
-        // ------------------------------------------------ MMA issue
+    } else if (warp == 21 && steps > 0) {
+        // ------------------------------------------------ MMA issue (the whole warp runs the
+        // loop and waits; one elected lane issues the MMAs and commits)
         const uint32_t idesc = f16_idesc(kTcTile, Npad);
-        int a_iter = 0, d_iter = 0, it = 0;
+        Ring a(SA), r(SB), d(ND);
         bool ok = true, issued = false;
-        for (int tile = tb; ok && tile < te; ++tile) {
+        for (int tile = blockIdx.x; ok && tile < B.total_tiles; tile += gridDim.x, d.step()) {
             const int nkb = B.p[tile_problem(B, tile)].k / kTcKB;
-            const int db = d_iter % ND;
-            if (!mbar_wait(D_EMPTY(db), ((d_iter / ND) & 1) ^ 1, abort_flag, status)) break;
+            const int db = d.slot;
+            if (!__all_sync(0xffffffffu, mbar_wait(D_EMPTY(db), d.phase ^ 1, abort_flag, status))) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + dcol0 + static_cast<uint32_t>(db * Npad);
-            for (int kb = 0; kb < nkb; ++kb, ++it, ++a_iter) {
-                const int sa = a_iter % SA, sb = it % SB;
-                if (!mbar_wait(A_FULL(sa), (a_iter / SA) & 1, abort_flag, status) ||
-                    !mbar_wait(B_FULL(sb), (it / SB) & 1, abort_flag, status)) { ok = false; break; }
+            for (int kb = 0; kb < nkb; ++kb, a.step(), r.step()) {
+                const int sa = a.slot, sb = r.slot;
+                bool w_ok = mbar_wait(A_FULL(sa), a.phase, abort_flag, status) &&
+                            mbar_wait(B_FULL(sb), r.phase, abort_flag, status);
+                if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t b0 = sbase + static_cast<uint32_t>(sb) * stage_bytes;
+                if (elect_one()) {
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const uint32_t a_tmem = tmem + static_cast<uint32_t>(64 * sa + 8 * t);
-                    const uint64_t bd = sw128_desc(b0 + static_cast<uint32_t>((t >> 2) * Npad * 128 + (t & 3) * 32));
-                    tc_mma(d_tmem, a_tmem, bd, idesc, (kb | t) != 0 ? 1u : 0u);
+                    for (int t = 0; t < 8; ++t) {
+                        const uint32_t a_tmem = tmem + static_cast<uint32_t>(64 * sa + 8 * t);
+                        const uint64_t bd = sw128_desc(b0 + static_cast<uint32_t>((t >> 2) * Npad * 128 + (t & 3) * 32));
+                        tc_mma(d_tmem, a_tmem, bd, idesc, (kb | t) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(A_EMPTY(sa));
+                    tc_commit(B_EMPTY(sb));
                 }
+                __syncwarp();
                 issued = true;
-                tc_commit(A_EMPTY(sa));
-                tc_commit(B_EMPTY(sb));
             }
             if (!ok) break;
-            tc_commit(D_FULL(db));
-            ++d_iter;
+            if (elect_one()) tc_commit(D_FULL(db));
+            __syncwarp();
         }
         if (issued) {
-            // all MMAs issued by this thread have completed before tensor memory is freed
-            tc_commit(DONE);
+            // all MMAs issued by this warp have completed before tensor memory is freed
+            if (elect_one()) tc_commit(DONE);
+            __syncwarp();
             volatile int never = 0;
             mbar_wait(DONE, 0, &never, status);
         }
@@ -581,7 +659,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8) {
+    if (warp == 20) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
@@ -613,6 +691,35 @@ size_t tc_workspace(int count, const nq_weights *w, int M)
         best = std::max(best, sum);
     }
     return best;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map of one nibble plane: uint8 [n][k/2], box 64 bytes x 128 rows.
+bool encode_plane(CUtensorMap *map, const void *plane, int n, int k)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTcTile)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(plane), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename F>
@@ -651,14 +758,20 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
         const int Mc = std::min(kTcMaxN, M - m0);
         const int npad = npad_of(Mc);
         const uint32_t stage_bytes = 256u * npad;
-        const int sb = std::max(2, std::min(8, static_cast<int>((200u * 1024u) / stage_bytes)));
+        const uint32_t wstage = planes * kTcTile * kWPitch + 1024;
+        // shared memory: up to 96 KB of weight stages in flight per SM (at least 3
+        // stages), the rest for activation stages (2 to 8)
+        const uint32_t avail = 222u * 1024u - 2048u;
+        const int wsn = std::max(3, std::min(planes == 2 ? 4 : 8, static_cast<int>((avail - 4 * stage_bytes) / wstage)));
+        const int sb = std::max(2, std::min(8, static_cast<int>((avail - wsn * wstage) / stage_bytes)));
         const int sa = (4 * 64 + 2 * npad <= kTmemCols) ? 4 : 3;
         const int nd = (sa * 64 + 2 * npad <= kTmemCols) ? 2 : 1;
         // 1 CTA per SM: the kernel allocates all 512 tensor-memory columns
-        const int smem = std::max<int>(static_cast<int>(sb * stage_bytes) + 8 * 32 + 64 + 1024, 120 * 1024);
+        const int smem = std::max<int>(static_cast<int>(sb * stage_bytes + wsn * wstage) + 8 * 56 + 64 + 1024,
+                                       120 * 1024);
         for (int i0 = 0; i0 < count; i0 += kTcMaxP) {
             const int cnt = std::min(kTcMaxP, count - i0);
-            long long tiles = 0, cost = 0;
+            long long tiles = 0;
             size_t off = 0;
             int kmax = 0;
             for (int i = 0; i < cnt; ++i) {
@@ -673,16 +786,16 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
                 p.n = L.n_out;
                 p.k = L.k_in;
                 p.tile_begin = static_cast<int>(tiles);
-                p.cost_begin = cost;
                 p.pad = 0;
+                if (!encode_plane(&b.maps[i][0], L.base, L.n_out, L.k_in) ||
+                    (planes == 2 && !encode_plane(&b.maps[i][1], L.resid, L.n_out, L.k_in)))
+                    return NQ_ERR_CUDA;
                 const long long nt = (L.n_out + kTcTile - 1) / kTcTile;
                 tiles += nt;
-                cost += nt * L.k_in;
                 off += stage_region_bytes(L.k_in, npad);
                 kmax = std::max(kmax, L.k_in);
             }
             if (tiles > 0x7fffffffLL) return NQ_ERR_SHAPE;
-            b.total_cost = cost;
             b.count = cnt;
             b.total_tiles = static_cast<int>(tiles);
             b.M = Mc;
@@ -691,6 +804,7 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
             b.sb = sb;
             b.sa = sa;
             b.nd = nd;
+            b.ws = wsn;
             const long long chunks = static_cast<long long>(kmax / 8) * npad;
             const int gx = static_cast<int>(std::min<long long>((chunks + 255) / 256, 4096));
             tc_stage_kernel<<<dim3(gx, cnt), 256, 0, stream>>>(b, status);
