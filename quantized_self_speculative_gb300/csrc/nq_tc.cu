@@ -10,8 +10,7 @@
 //
 //   * warp 22 loads the packed nibble planes of the tile's next k-blocks
 //     into shared-memory stages with TMA (one 128-row x 64-byte box per
-//     plane, 64-byte swizzle) and their group scales with cp.async, several
-//     k-blocks ahead;
+//     plane, 64-byte swizzle), several k-blocks ahead;
 //   * warps 0-15 (one thread per weight row = one tensor-memory lane; two
 //     groups of eight take alternate k-blocks, two warps per row quarter
 //     each taking half of the k-block) decode the
@@ -368,32 +367,15 @@ struct TileSeq {
     }
 };
 
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-// Arrive on `bar` once every cp.async of this thread issued so far has landed
-// (the barrier's count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
 {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(uint32_t a)
 {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
 
@@ -418,7 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const int Npad = B.Npad, SB = B.sb, SA = B.sa, ND = B.nd, WS = B.ws;
     const uint32_t stage_bytes = 256u * static_cast<uint32_t>(Npad);
     constexpr uint32_t kPlaneBytes = kTcTile * kWPitch;
-    constexpr uint32_t kWStage = PLANES * kPlaneBytes + 1024;   // planes, 512 B of scales, pad to 1024
+    constexpr uint32_t kWStage = PLANES * kPlaneBytes;          // 1024-byte multiple (TMA swizzle atoms)
     const uint32_t wbase = sbase + static_cast<uint32_t>(SB) * stage_bytes;
     // barriers: a_full[4] a_empty[4] b_full[8] b_empty[8] d_full[2] d_empty[2] done w_full[12] w_empty[12]
     const uint32_t bars = wbase + static_cast<uint32_t>(WS) * kWStage;
@@ -440,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         for (int i = 0; i < 8; ++i) { mbar_init(B_FULL(i), 1); mbar_init(B_EMPTY(i), 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(D_FULL(i), 1); mbar_init(D_EMPTY(i), 4); }
         mbar_init(DONE, 1);
-        for (int i = 0; i < 12; ++i) { mbar_init(W_FULL(i), 33); mbar_init(W_EMPTY(i), 8); }
+        for (int i = 0; i < 12; ++i) { mbar_init(W_FULL(i), 1); mbar_init(W_EMPTY(i), 8); }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -459,47 +441,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const uint32_t dcol0 = static_cast<uint32_t>(SA) * 64u;
 
     if (warp == 22 && steps > 0) {
-        // ------------------------------------------------ weight loader: TMA boxes and scale words into stages
-        TileSeq q;
-        q.init(B);
-        int last_phase[12];
-        for (int i = 0; i < 12; ++i) last_phase[i] = -1;
-        Ring w(WS);
-        for (int it = 0; it < steps; ++it, w.step()) {
-            const int st = w.slot;
-            bool ok = mbar_wait(W_EMPTY(st), w.phase ^ 1, abort_flag, status);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const TcProb &P = B.p[q.pi];
-            const int r0 = (q.tile - P.tile_begin) * kTcTile;
-            const uint32_t dst = wbase + static_cast<uint32_t>(st) * kWStage;
-            if (lane == 0) {
+        // ------------------------------------------------ weight loader: one elected lane issues
+        // the TMA boxes of each k-block into the next free stage
+        if (elect_one()) {
+            TileSeq q;
+            q.init(B);
+            int last_phase[12];
+            for (int i = 0; i < 12; ++i) last_phase[i] = -1;
+            Ring w(WS);
+            for (int it = 0; it < steps; ++it, w.step()) {
+                const int st = w.slot;
+                if (!mbar_wait(W_EMPTY(st), w.phase ^ 1, abort_flag, status)) break;
+                const TcProb &P = B.p[q.pi];
+                const int r0 = (q.tile - P.tile_begin) * kTcTile;
+                const uint32_t dst = wbase + static_cast<uint32_t>(st) * kWStage;
                 // one arrival with the byte count; rows beyond n are zero-filled by TMA
                 mbar_expect_tx(W_FULL(st), PLANES * kPlaneBytes);
 #pragma unroll
                 for (int p = 0; p < PLANES; ++p)
                     tma_load_2d(dst + static_cast<uint32_t>(p) * kPlaneBytes, &B.maps[q.pi][p], q.kb * 64, r0, W_FULL(st));
+                last_phase[st] = w.phase;
+                q.next(B);
             }
-            // group scales: the 4-byte word holding scale (n, kb * 128 / G) (G = 128: pick the half later)
-            const int ng = P.k / G;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int row = 32 * j + lane;
-                const int n = r0 + row < P.n ? r0 + row : 0;
-                const size_t e = static_cast<size_t>(n) * ng + static_cast<size_t>(q.kb) * (kTcKB / G);
-                cp_async4(dst + PLANES * kPlaneBytes + row * 4, P.scales + (e & ~static_cast<size_t>(1)));
-            }
-            cp_async_arrive(W_FULL(st));
-            last_phase[st] = w.phase;
-            q.next(B);
-        }
-        cp_async_wait_all();
-        // every TMA box issued has landed before the CTA may exit
-        if (lane == 0)
+            // every TMA box issued has landed before the CTA may exit
             for (int i = 0; i < WS && i < 12; ++i)
                 if (last_phase[i] >= 0) {
                     volatile int never = 0;
                     mbar_wait(W_FULL(i), static_cast<uint32_t>(last_phase[i]), &never, status);
                 }
+        }
+        __syncwarp();
     } else if (warp < 16 && steps > 0) {
         // ------------------------------------------------ decode warps: two groups of eight take
         // alternate k-blocks; in a group, warp w decodes rows 32 (w % 4) .. + 31 (its
@@ -510,8 +481,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         TileSeq q;
         q.init(B);
         if (grp == 1) q.next(B);
+        // this row's group scale, loaded from global one k-block of this group ahead
+        auto scale_of = [&](const TileSeq &c) -> unsigned short {
+            const TcProb &P = B.p[c.pi];
+            const int n0 = (c.tile - P.tile_begin) * kTcTile + row;
+            const size_t e = static_cast<size_t>(n0 < P.n ? n0 : 0) * (P.k / G) + static_cast<size_t>(c.kb) * (kTcKB / G) +
+                             (G == 64 ? half : 0);
+            return ld_nc_u16(P.scales + e);
+        };
+        unsigned short s_next = scale_of(q);
         Ring w(WS, grp), a(SA, grp);
         for (int it = grp; it < steps; it += 2, w.step(2), a.step(2)) {
+            const unsigned short sbits = s_next;
+            TileSeq q2 = q;
+            q2.next(B);
+            q2.next(B);
+            if (it + 2 < steps) s_next = scale_of(q2);
             const int st = w.slot, sa = a.slot;
             bool ok = mbar_wait(W_FULL(st), w.phase, abort_flag, status);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -525,20 +510,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 const uint4 r = PLANES == 2 ? lds128(at + kPlaneBytes) : make_uint4(0, 0, 0, 0);
                 rw[4 * j] = r.x; rw[4 * j + 1] = r.y; rw[4 * j + 2] = r.z; rw[4 * j + 3] = r.w;
             }
-            const uint32_t sw = lds32(wbase + static_cast<uint32_t>(st) * kWStage + PLANES * kPlaneBytes + row * 4);
             __syncwarp();
             if (lane == 0) mbar_arrive(W_EMPTY(st));
-            // the scale word holds two consecutive scales: G = 64 -> this half's group is
-            // 2 kb + half; G = 128 -> group kb sits in the half given by its index parity
-            unsigned short sbits;
-            if (G == 64) {
-                sbits = static_cast<unsigned short>(half ? (sw >> 16) : (sw & 0xFFFFu));
-            } else {
-                const TcProb &P = B.p[q.pi];
-                const int n0 = (q.tile - P.tile_begin) * kTcTile + row;
-                const size_t e = static_cast<size_t>(n0 < P.n ? n0 : 0) * (P.k / G) + q.kb;
-                sbits = static_cast<unsigned short>((e & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-            }
             const GroupK g = group_consts<PLANES>(sbits);
             const bool all_fast = __all_sync(0xffffffffu, g.fast);
             uint32_t v[32];
@@ -558,8 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(A_FULL(sa));
-            q.next(B);
-            q.next(B);
+            q = q2;
         }
     } else if (warp < 20 && steps > 0) {
         // ------------------------------------------------ epilogue warps
@@ -758,7 +730,7 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
         const int Mc = std::min(kTcMaxN, M - m0);
         const int npad = npad_of(Mc);
         const uint32_t stage_bytes = 256u * npad;
-        const uint32_t wstage = planes * kTcTile * kWPitch + 1024;
+        const uint32_t wstage = planes * kTcTile * kWPitch;
         // shared memory: up to 96 KB of weight stages in flight per SM (at least 3
         // stages), the rest for activation stages (2 to 8)
         const uint32_t avail = 222u * 1024u - 2048u;
