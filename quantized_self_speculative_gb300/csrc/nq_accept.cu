@@ -211,9 +211,13 @@ __device__ __forceinline__ MaxSum leaf_ms(const float (&l)[kLeaf], float c)
 #pragma unroll
     for (int e = 1; e < kLeaf; ++e) mx = fmaxf(mx, l[e]);
     const float mz = __fmul_rn(mx, c);
+    const unsigned long long c2 = f2_pack(c, c), nmz2 = f2_pack(-mz, -mz);
     float s = 0.0f;
 #pragma unroll
-    for (int e = 0; e < kLeaf; ++e) s = __fadd_rn(s, exp2_canon(__fmaf_rn(l[e], c, -mz)));
+    for (int e = 0; e < kLeaf; e += 2) {
+        const float2 x = exp2_canon_x2(f2_fma(f2_pack(l[e], l[e + 1]), c2, nmz2));
+        s = __fadd_rn(__fadd_rn(s, x.x), x.y);
+    }
     return MaxSum{mz, s};
 }
 
@@ -242,7 +246,7 @@ __device__ __forceinline__ float leaf_factor(float mz_leaf, float M, float inv_s
 }
 
 // ---- pass A: one block of one vector; the last CTA of a row decides.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 6)
 sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
                 unsigned int *__restrict__ counters, float2 *__restrict__ part, SampleRec *__restrict__ rec,
@@ -399,21 +403,25 @@ __device__ __forceinline__ float leaf_weights(const float (&lp)[kLeaf], const fl
         for (int e = 1; e < kLeaf; ++e) mq = fmaxf(mq, lq[e]);
         const float mzq = __fmul_rn(mq, c);
         const float Fq = leaf_factor(mzq, R.Mq, R.invSq);
+        const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp), nmzq = f2_pack(-mzq, -mzq);
 #pragma unroll
-        for (int e = 0; e < kLeaf; ++e) {
-            const float pe = __fmul_rn(exp2_canon(__fmaf_rn(lp[e], c, -mzp)), Fp);
-            const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq[e], c, -mzq)), Fq);
-            const float d = __fsub_rn(pe, qe);
-            const float we = d > 0.0f ? d : 0.0f;
-            s = __fadd_rn(s, we);
-            if (KEEP) w[e] = we;
+        for (int e = 0; e < kLeaf; e += 2) {
+            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[e], lp[e + 1]), c2, nmzp));
+            const float2 eq = exp2_canon_x2(f2_fma(f2_pack(lq[e], lq[e + 1]), c2, nmzq));
+            const float d0 = __fsub_rn(__fmul_rn(ep.x, Fp), __fmul_rn(eq.x, Fq));
+            const float d1 = __fsub_rn(__fmul_rn(ep.y, Fp), __fmul_rn(eq.y, Fq));
+            const float w0 = d0 > 0.0f ? d0 : 0.0f, w1 = d1 > 0.0f ? d1 : 0.0f;
+            s = __fadd_rn(__fadd_rn(s, w0), w1);
+            if (KEEP) { w[e] = w0; w[e + 1] = w1; }
         }
     } else {
+        const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp);
 #pragma unroll
-        for (int e = 0; e < kLeaf; ++e) {
-            const float we = __fmul_rn(exp2_canon(__fmaf_rn(lp[e], c, -mzp)), Fp);
-            s = __fadd_rn(s, we);
-            if (KEEP) w[e] = we;
+        for (int e = 0; e < kLeaf; e += 2) {
+            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[e], lp[e + 1]), c2, nmzp));
+            const float w0 = __fmul_rn(ep.x, Fp), w1 = __fmul_rn(ep.y, Fp);
+            s = __fadd_rn(__fadd_rn(s, w0), w1);
+            if (KEEP) { w[e] = w0; w[e + 1] = w1; }
         }
     }
     return s;
@@ -445,41 +453,33 @@ __device__ float block_sum(float *warp_sum, float *lsum, const float *pv, const 
     return tot;
 }
 
-// Levels of a power-of-two sum tree stacked in one array: level 0 = [0, P),
-// level l starts after the wider levels.  Returns the root.
-__device__ float build_levels(float *tree, int P)
+// Descend the pairwise sum tree over 32 leaves held one per lane (index =
+// lane; pads are zeros).  Level sums are formed as left + right by xor
+// shuffles (fp addition commutes exactly); at each level go left if t < left
+// or the right sum is not positive, else t -= left.  Returns the chosen lane;
+// every lane computes the same result and t.
+__device__ __forceinline__ int warp_descend32(float v, float &t)
 {
-    int in = 0, width = P;
-    while (width > 1) {
-        const int out = in + width;
-        for (int i = threadIdx.x; i < width / 2; i += kThreads)
-            tree[out + i] = __fadd_rn(tree[in + 2 * i], tree[in + 2 * i + 1]);
-        __syncthreads();
-        in = out;
-        width >>= 1;
+    float s[6];
+    s[0] = v;
+#pragma unroll
+    for (int l = 0; l < 5; ++l) s[l + 1] = __fadd_rn(s[l], __shfl_xor_sync(0xffffffffu, s[l], 1 << l));
+    int base = 0;
+#pragma unroll
+    for (int l = 4; l >= 0; --l) {
+        const float left = __shfl_sync(0xffffffffu, s[l], base);
+        const float right = __shfl_sync(0xffffffffu, s[l], base + (1 << l));
+        if (!(t < left || !(right > 0.0f))) {
+            t = __fsub_rn(t, left);
+            base += 1 << l;
+        }
     }
-    return tree[in];
-}
-
-// Descend a stacked power-of-two tree: left if t < left or the right sum is 0.
-__device__ __forceinline__ int descend(const float *tree, int P, float &t)
-{
-    int levels = 0;
-    while ((1 << levels) < P) ++levels;
-    int node = 0;
-    for (int lv = levels; lv >= 1; --lv) {
-        int off = 0;
-        for (int q = 0; q < lv - 1; ++q) off += P >> q;
-        const float left = tree[off + 2 * node], right = tree[off + 2 * node + 1];
-        if (t < left || !(right > 0.0f)) node = 2 * node;
-        else { t = __fsub_rn(t, left); node = 2 * node + 1; }
-    }
-    return node;
+    return base;
 }
 
 // ---- pass B: one block of the chosen position of one row; the last CTA of
 // the row descends the sum tree and writes the row's tokens.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
                 unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ csum,
@@ -487,76 +487,146 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
 {
     __shared__ float warp_sum[kThreads / 32];
     __shared__ __align__(16) float btree[2 * kMaxBlocks];
-    __shared__ __align__(16) float ltree[2 * 4 * kThreads];
     __shared__ bool last;
     __shared__ int pick;
-    const int NBK = gridDim.x, blk = blockIdx.x, b = blockIdx.y;
+    const int NBK = gridDim.x >> 2, blk = blockIdx.x >> 2, q = blockIdx.x & 3, b = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const SampleRec R = rec[b];
     const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + R.js) * V;
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
     bool resid = R.resid != 0;
 
-    float *my_lsum = lsum + (static_cast<size_t>(b) * NBK + blk) * (4 * kThreads);
-    const float tot = block_sum(warp_sum, my_lsum, pv, qv, resid, V, blk, c, R);
+    // one leaf (blk, 4 T + q) per thread: its weight sum goes to lsum
+    float *blk_lsum = lsum + (static_cast<size_t>(b) * NBK + blk) * (4 * kThreads);
+    {
+        float lp[kLeaf], lq[kLeaf], w[kLeaf];
+        load_pq(pv, qv, resid, V, blk, threadIdx.x, q, lp, lq);
+        blk_lsum[4 * threadIdx.x + q] = leaf_weights<false>(lp, lq, resid, V, blk, threadIdx.x, q, c, R, w);
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        csum[static_cast<size_t>(b) * NBK + blk] = tot;
         __threadfence();
         const unsigned int prev = atomicAdd(&counters[b], 1u);
-        last = prev == static_cast<unsigned int>(NBK - 1);
+        last = prev == static_cast<unsigned int>(4 * NBK - 1);
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
 
-    int P = 1;
-    while (P < NBK) P <<= 1;
-    for (int i = threadIdx.x; i < P; i += kThreads) btree[i] = i < NBK ? __ldcg(csum + static_cast<size_t>(b) * NBK + i) : 0.0f;
+    // block totals: the pairwise tree over each block's 1024 leaf sums in index
+    // order (32 consecutive leaves per lane, then the lanes), one warp per block
+    for (int bb = warp; bb < NBK; bb += kThreads / 32) {
+        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads)) + 8 * lane;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 x = __ldcg(src + i);
+            v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+        }
+#pragma unroll
+        for (int w = 1; w < 32; w <<= 1)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2 * w) v[i] = __fadd_rn(v[i], v[i + w]);
+        const float tot = warp_tree_sum(v[0], 5);
+        if (lane == 0) {
+            btree[bb] = tot;
+            csum[static_cast<size_t>(b) * NBK + bb] = tot;
+        }
+    }
     __syncthreads();
-    float root = build_levels(btree, P);
-    if (!(root > 0.0f) && resid) {
-        // all-zero residual (rounding): draw from p_js instead
-        resid = false;
-        for (int bb = 0; bb < NBK; ++bb) {
-            const float s = block_sum(warp_sum, lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads), pv, qv,
-                                      false, V, bb, c, R);
-            if (threadIdx.x == 0) btree[bb] = s;
+    // all-zero residual (rounding): draw from p_js instead (all threads rebuild the leaf sums)
+    if (resid) {
+        float r = warp == 0 ? (lane < NBK ? btree[lane] : 0.0f) : 0.0f;
+        if (warp == 0) r = warp_tree_sum(r, 5);
+        if (threadIdx.x == 0) pick = r > 0.0f ? 1 : 0;
+        __syncthreads();
+        if (pick == 0) {
+            resid = false;
+            for (int bb = 0; bb < NBK; ++bb) {
+                const float sb = block_sum(warp_sum, lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads), pv, qv,
+                                           false, V, bb, c, R);
+                if (threadIdx.x == 0) btree[bb] = sb;
+            }
         }
         __syncthreads();
-        root = build_levels(btree, P);
     }
+    if (warp != 0) return;
+
+    // warp 0: block tree (32 lanes, zero pads), then the chosen block's leaf tree
+    const float bval = lane < NBK ? btree[lane] : 0.0f;
+    const float root = warp_tree_sum(bval, 5);
     float t = __fmul_rn(R.u, root);
-    const int bstar = descend(btree, P, t);
+    const int bstar = warp_descend32(bval, t);
+    float v[32];
     {
-        const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * (4 * kThreads)) + threadIdx.x);
-        *reinterpret_cast<float4 *>(ltree + 4 * threadIdx.x) = v4;
-    }
-    __syncthreads();
-    build_levels(ltree, 4 * kThreads);
-    const int lstar = descend(ltree, 4 * kThreads, t);
-    if (threadIdx.x == 0) {
-        const int Ts = lstar >> 2, qs = lstar & 3;
-        float w[kLeaf], lp[kLeaf], lq[kLeaf];
-        load_pq(pv, qv, resid, V, bstar, Ts, qs, lp, lq);
-        leaf_weights<true>(lp, lq, resid, V, bstar, Ts, qs, c, R, w);
-        int pk = -1;
-        float run = 0.0f;
-        for (int e = 0; e < kLeaf && pk < 0; ++e) {
-            const int x = leaf_entry(bstar, Ts, qs, e);
-            if (x >= V) continue;
-            run = __fadd_rn(run, w[e]);
-            if (t < run) pk = x;
+        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * (4 * kThreads)) + 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 x = __ldcg(src + i);
+            v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
         }
-        for (int e = kLeaf - 1; e >= 0 && pk < 0; --e) {
-            const int x = leaf_entry(bstar, Ts, qs, e);
-            if (x < V && w[e] > 0.0f) pk = x;
-        }
-        pick = pk;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    float lsum32[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) lsum32[i] = v[i];
+#pragma unroll
+    for (int w = 1; w < 32; w <<= 1)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2 * w) v[i] = __fadd_rn(v[i], v[i + w]);
+    const int lane_star = warp_descend32(v[0], t);
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float x = __shfl_sync(0xffffffffu, lsum32[i], lane_star);
+        if (lane == i) mine = x;
+    }
+    const int lstar = 32 * lane_star + warp_descend32(mine, t);
+
+    // the chosen leaf: 16 lanes reload one entry each, the weights are formed
+    // exactly as in the leaf sums, lane 0 scans them in entry order
+    const int Ts = lstar >> 2, qs = lstar & 3;
+    const int e = lane & 15;
+    const int x = leaf_entry(bstar, Ts, qs, e);
+    const bool present = x < V;
+    const float lp = present ? __ldcg(pv + x) : -INFINITY;
+    const float lq = present && resid ? __ldcg(qv + x) : -INFINITY;
+    float mp = lp, mq = lq;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+    }
+    const float mzp = __fmul_rn(mp, c);
+    float we = __fmul_rn(exp2_canon(__fmaf_rn(lp, c, -mzp)), leaf_factor(mzp, R.Mp, R.invSp));
+    if (resid) {
+        const float mzq = __fmul_rn(mq, c);
+        const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq, c, -mzq)), leaf_factor(mzq, R.Mq, R.invSq));
+        const float d = __fsub_rn(we, qe);
+        we = d > 0.0f ? d : 0.0f;
+    }
+    if (!present) we = 0.0f;
+    int pk = -1;
+    float run = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLeaf; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, we, i);
+        const int xi = leaf_entry(bstar, Ts, qs, i);
+        if (xi < V && pk < 0) {
+            run = __fadd_rn(run, wi);
+            if (t < run) pk = xi;
+        }
+    }
+    // fallback: the last entry of the leaf with a positive weight
+#pragma unroll
+    for (int i = kLeaf - 1; i >= 0; --i) {
+        const float wi = __shfl_sync(0xffffffffu, we, i);
+        const int xi = leaf_entry(bstar, Ts, qs, i);
+        if (pk < 0 && xi < V && wi > 0.0f) pk = xi;
+    }
+    if (lane == 0) {
         const int js = R.js;
         for (int jj = 0; jj <= k; ++jj)
-            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? pick : -1);
+            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? pk : -1);
         out_cnt[b] = js + 1;
         counters[b] = 0;
     }
@@ -622,7 +692,7 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     nq::sample_a_kernel<<<grid_a, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
                                                              reinterpret_cast<unsigned int *>(w + L.counters_a),
                                                              reinterpret_cast<float2 *>(w + L.part), rec, status);
-    dim3 grid_b(nq::n_blocks(V), B);
+    dim3 grid_b(4 * nq::n_blocks(V), B);   // one CTA per (block, leaf quarter q)
     nq::sample_b_kernel<<<grid_b, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
                                                              reinterpret_cast<unsigned int *>(w + L.counters_b), rec,
                                                              reinterpret_cast<float *>(w + L.csum),

@@ -114,6 +114,58 @@ __device__ __forceinline__ float exp2_canon(float t)
     return t < -125.0f ? 0.0f : r;
 }
 
+// Two canonical exp2 evaluations at once with the packed fp32 instructions
+// (add/sub/fma .rn.f32x2 perform two independent IEEE operations, so each
+// lane rounds exactly as exp2_canon does).  The clamp at -125 is not needed:
+// t < -125 returns 0 by the final select, and t >= -125 is unchanged.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r)
+{
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float2 exp2_canon_x2(unsigned long long t)
+{
+    const unsigned long long mag = f2_pack(12582912.0f, 12582912.0f);
+    const unsigned long long big = f2_add(t, mag);
+    const unsigned long long f = f2_sub(t, f2_sub(big, mag));
+    unsigned long long p = f2_fma(f2_pack(0.000154035303933816099545f, 0.000154035303933816099545f), f,
+                                  f2_pack(0.00133335581464284434234f, 0.00133335581464284434234f));
+    p = f2_fma(p, f, f2_pack(0.00961812910762847716197f, 0.00961812910762847716197f));
+    p = f2_fma(p, f, f2_pack(0.0555041086648215799531f, 0.0555041086648215799531f));
+    p = f2_fma(p, f, f2_pack(0.240226506959100712333f, 0.240226506959100712333f));
+    p = f2_fma(p, f, f2_pack(0.693147180559945309417f, 0.693147180559945309417f));
+    p = f2_fma(p, f, f2_pack(1.0f, 1.0f));
+    const float2 pv = f2_unpack(p), bv = f2_unpack(big), tv = f2_unpack(t);
+    const float ra = __int_as_float(__float_as_int(pv.x) + (__float_as_int(bv.x) << 23));
+    const float rb = __int_as_float(__float_as_int(pv.y) + (__float_as_int(bv.y) << 23));
+    return make_float2(tv.x < -125.0f ? 0.0f : ra, tv.y < -125.0f ? 0.0f : rb);
+}
+
 struct MaxSum { float m, s; };
 
 // Merge two (max, sum) nodes; the larger max survives, the other sum is

@@ -152,3 +152,40 @@ def test_workspace_and_argument_checks(nq):
     a = [nq.accept_sample(dev(d), dev(dl), dev(tl), 1.0, seeds_dev(synth.seeds_for(9, B)), 3, ws=ws)[0].cpu()
          for _ in range(3)]
     assert torch.equal(a[0], a[1]) and torch.equal(a[1], a[2])
+
+
+def test_sample_zero_residual_falls_back_to_p(nq):
+    """Degenerate residual (Erge, "The same output as the large model alone";
+    the reading for sum max(0, p - q) = 0): when rounding leaves p <= q at every
+    entry of a rejected position, the replacement is drawn from p.  Built from
+    the oracle: canonical p from logits (0, 0, -eps) is elementwise <= the
+    uniform q and one ulp below it at the draft id, and a seed whose accept
+    uniform lands in the one-ulp rejection window is found by search."""
+    V = 3
+    q_logits = np.zeros(V, np.float32)
+    q = O.softmax_canonical(q_logits, 1.0)
+    case = None
+    for e in range(14, 30):
+        p_logits = np.array([0.0, 0.0, -np.float32(2.0) ** -e], np.float32)
+        p = O.softmax_canonical(p_logits, 1.0)
+        if np.all(p <= q) and p[2] < q[2]:
+            ratio = np.float32(p[2]) / np.float32(q[2])
+            if ratio < np.float32(1.0) and (case is None or ratio < case[1]):
+                case = (p_logits, ratio)
+    assert case is not None
+    p_logits, ratio = case
+    seed = None
+    for start in range(0, 1 << 27, 1 << 22):
+        s = np.arange(start, start + (1 << 22), dtype=np.uint64)
+        u = O.uniforms(s, 0, 0, 0)
+        hit = np.nonzero(u >= ratio)[0]
+        if hit.size:
+            seed = int(s[hit[0]])
+            break
+    assert seed is not None
+    d = np.array([[2]], np.int32)
+    dl = q_logits.reshape(1, 1, V)
+    tl = np.stack([p_logits, np.array([1.0, 2.0, 3.0], np.float32)]).reshape(1, 2, V)
+    seeds = np.array([seed], np.uint64)
+    cnt = check_sample(nq, d, dl, tl, 1.0, seeds, 0)
+    assert list(cnt) == [1]
