@@ -73,7 +73,7 @@ def test_workspace_bytes(L):
 def test_linear_workspace_bytes(L):
     """Workspace of the tensor-core linears: fp16 activations of each layer
     (N padded to a multiple of 16, at most 256 rows per launch), 1024-byte
-    regions, the largest launch of 128 layers; 0 where the path is not taken."""
+    regions, the largest launch of 64 layers; 0 where the path is not taken."""
     from quantized_self_speculative_gb300 import nq
     A = 0x10000
     a1k = lambda n: (n + 1023) // 1024 * 1024
@@ -90,7 +90,7 @@ def test_linear_workspace_bytes(L):
     mix = layers([(1024, 4096), (4096, 14336), (333, 384)])
     assert L.nq_linear_workspace_bytes(3, mix, 40, 1) == sum(a1k(2 * 48 * k) for k in (4096, 14336, 384))
     many = layers([(512, 4096)] * 200)
-    assert L.nq_linear_workspace_bytes(200, many, 64, 1) == 128 * a1k(2 * 64 * 4096)
+    assert L.nq_linear_workspace_bytes(200, many, 64, 1) == 64 * a1k(2 * 64 * 4096)
     assert L.nq_linear_workspace_bytes(1, layers([(256, 192)], g=64), 64, 1) == 0   # k % 128 != 0
     assert L.nq_linear_workspace_bytes(1, layers([(256, 512)], fmt=nq.FMT_INT4), 64, 0) == a1k(2 * 64 * 512)
     assert L.nq_linear_workspace_bytes(1, layers([(256, 512)], fmt=nq.FMT_INT4), 64, 1) == 0   # invalid pair
