@@ -48,7 +48,8 @@ namespace {
 constexpr int kTcMinM = 16;            // smallest M routed here
 constexpr int kTcMaxN = 256;           // activation rows per launch (MMA N)
 constexpr int kTcTile = 128;           // weight rows per tile (MMA M)
-constexpr int kTcKB = 128;             // inputs per k-block (8 MMAs of K = 16)
+constexpr int kTcKB = 128;             // inputs per k-block at wide N (8 MMAs of K = 16)
+constexpr int kTcKBWide = 256;         // inputs per k-block when the padded M is at most 64
 constexpr int kTcMaxP = 64;            // linears per launch (two 128-byte tensor maps each)
 constexpr int kTcThreads = 736;        // warps 0-15 decode, 16-19 epilogue, 20 B copy, 21 MMA, 22 weight loads
 constexpr int kTmemCols = 512;
@@ -348,13 +349,14 @@ struct Ring {
 // Tiles are dealt round-robin (CTA c takes tiles c, c + grid, ...), so the
 // CTAs running at any moment work on neighbouring tiles of one or two linears
 // and share their staged activations in L2.
+template <int KB>
 struct TileSeq {
     int tile, pi, kb, nkb;
     __device__ void init(const TcBatch &B)
     {
         tile = blockIdx.x;
         kb = 0;
-        if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / kTcKB; }
+        if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / KB; }
         else { pi = 0; nkb = 1; }
     }
     __device__ void next(const TcBatch &B)
@@ -362,7 +364,7 @@ struct TileSeq {
         if (++kb == nkb) {
             kb = 0;
             tile += gridDim.x;
-            if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / kTcKB; }
+            if (tile < B.total_tiles) { pi = tile_problem(B, tile); nkb = B.p[pi].k / KB; }
         }
     }
 };
@@ -379,18 +381,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t a)
     return v;
 }
 
-// Weight stage: per plane 128 rows of 64 bytes as TMA writes them with the
-// 64-byte swizzle (address bits 4-5 XOR bits 7-8 of a 1024-byte aligned
-// stage): the 16-byte piece p of row r sits at piece position p ^ ((r >> 1) & 3),
+// Weight stage: per plane 128 rows of KB/2 bytes as TMA writes them with the
+// 64-byte (KB = 128) or 128-byte (KB = 256) swizzle of a 1024-byte aligned
+// stage: the 16-byte piece p of row r sits at p ^ ((r >> 1) & 3) or p ^ (r & 7),
 // so the 8 rows read by a quarter warp (same logical piece) fall in 8
 // different bank groups.
-constexpr int kWPitch = 64;
+template <int KB>
 __host__ __device__ constexpr uint32_t wpos(int row, int piece)
 {
-    return static_cast<uint32_t>(row * kWPitch + ((piece ^ ((row >> 1) & 3)) << 4));
+    return KB == 128 ? static_cast<uint32_t>(row * 64 + ((piece ^ ((row >> 1) & 3)) << 4))
+                     : static_cast<uint32_t>(row * 128 + ((piece ^ (row & 7)) << 4));
 }
 
-template <int PLANES, int G>
+template <int PLANES, int G, int KB>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ TcBatch B, unsigned int *status)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -398,8 +401,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (sbase - raw);
     const int Npad = B.Npad, SB = B.sb, SA = B.sa, ND = B.nd, WS = B.ws;
-    const uint32_t stage_bytes = 256u * static_cast<uint32_t>(Npad);
-    constexpr uint32_t kPlaneBytes = kTcTile * kWPitch;
+    const uint32_t stage_bytes = 2u * KB * static_cast<uint32_t>(Npad);   // KB/64 swizzle atoms of Npad x 128 B
+    constexpr uint32_t kPlaneBytes = kTcTile * (KB / 2);
+    constexpr int kACols = KB / 2;                                         // tensor-memory columns per A stage
     constexpr uint32_t kWStage = PLANES * kPlaneBytes;          // 1024-byte multiple (TMA swizzle atoms)
     const uint32_t wbase = sbase + static_cast<uint32_t>(SB) * stage_bytes;
     // barriers: a_full[4] a_empty[4] b_full[8] b_empty[8] d_full[2] d_empty[2] done w_full[12] w_empty[12]
@@ -437,14 +441,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     int steps = 0;
-    for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) steps += B.p[tile_problem(B, t)].k / kTcKB;
-    const uint32_t dcol0 = static_cast<uint32_t>(SA) * 64u;
+    for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) steps += B.p[tile_problem(B, t)].k / KB;
+    const uint32_t dcol0 = static_cast<uint32_t>(SA) * kACols;
 
     if (warp == 22 && steps > 0) {
         // ------------------------------------------------ weight loader: one elected lane issues
         // the TMA boxes of each k-block into the next free stage
         if (elect_one()) {
-            TileSeq q;
+            TileSeq<KB> q;
             q.init(B);
             int last_phase[12];
             for (int i = 0; i < 12; ++i) last_phase[i] = -1;
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 mbar_expect_tx(W_FULL(st), PLANES * kPlaneBytes);
 #pragma unroll
                 for (int p = 0; p < PLANES; ++p)
-                    tma_load_2d(dst + static_cast<uint32_t>(p) * kPlaneBytes, &B.maps[q.pi][p], q.kb * 64, r0, W_FULL(st));
+                    tma_load_2d(dst + static_cast<uint32_t>(p) * kPlaneBytes, &B.maps[q.pi][p], q.kb * (KB / 2), r0, W_FULL(st));
                 last_phase[st] = w.phase;
                 q.next(B);
             }
@@ -474,37 +478,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     } else if (warp < 16 && steps > 0) {
         // ------------------------------------------------ decode warps: two groups of eight take
         // alternate k-blocks; in a group, warp w decodes rows 32 (w % 4) .. + 31 (its
-        // tensor-memory lane quarter) and inputs 64 h .. + 63 (h = (w / 4) % 2) of the
-        // k-block, i.e. A-stage columns 32 h .. + 31
+        // tensor-memory lane quarter) and half h = (w / 4) % 2 of the k-block (inputs
+        // h KB/2 .. + KB/2 - 1, A-stage columns h KB/4 .. + KB/4 - 1), in chunks of 64
+        // inputs (8 words per plane, 32 columns)
+        constexpr int kChunks = KB / 128;   // 64-input chunks per half k-block
         const int grp = warp >> 3, half = (warp >> 2) & 1, row = 32 * (warp & 3) + lane;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 32u * half;
-        TileSeq q;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(half * (KB / 4));
+        TileSeq<KB> q;
         q.init(B);
         if (grp == 1) q.next(B);
-        // this row's group scale, loaded from global one k-block of this group ahead
-        auto scale_of = [&](const TileSeq &c) -> unsigned short {
+        // this row's group scales for the chunks of its half, loaded from global one
+        // k-block of this group ahead
+        auto scales_of = [&](const TileSeq<KB> &c, unsigned short (&out)[kChunks]) {
             const TcProb &P = B.p[c.pi];
             const int n0 = (c.tile - P.tile_begin) * kTcTile + row;
-            const size_t e = static_cast<size_t>(n0 < P.n ? n0 : 0) * (P.k / G) + static_cast<size_t>(c.kb) * (kTcKB / G) +
-                             (G == 64 ? half : 0);
-            return ld_nc_u16(P.scales + e);
+            const size_t base = static_cast<size_t>(n0 < P.n ? n0 : 0) * (P.k / G);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+                out[ch] = ld_nc_u16(P.scales + base + (static_cast<size_t>(c.kb) * KB + half * (KB / 2) + 64 * ch) / G);
         };
-        unsigned short s_next = scale_of(q);
+        unsigned short s_next[kChunks];
+        scales_of(q, s_next);
         Ring w(WS, grp), a(SA, grp);
         for (int it = grp; it < steps; it += 2, w.step(2), a.step(2)) {
-            const unsigned short sbits = s_next;
-            TileSeq q2 = q;
+            unsigned short sbits[kChunks];
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) sbits[ch] = s_next[ch];
+            TileSeq<KB> q2 = q;
             q2.next(B);
             q2.next(B);
-            if (it + 2 < steps) s_next = scale_of(q2);
+            if (it + 2 < steps) scales_of(q2, s_next);
             const int st = w.slot, sa = a.slot;
             bool ok = mbar_wait(W_FULL(st), w.phase, abort_flag, status);
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t src = wbase + static_cast<uint32_t>(st) * kWStage;
-            uint32_t bw[8], rw[8];
+            uint32_t bw[8 * kChunks], rw[8 * kChunks];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint32_t at = src + wpos(row, 2 * half + j);
+            for (int j = 0; j < 2 * kChunks; ++j) {
+                const uint32_t at = src + wpos<KB>(row, 2 * kChunks * half + j);
                 const uint4 v = lds128(at);
                 bw[4 * j] = v.x; bw[4 * j + 1] = v.y; bw[4 * j + 2] = v.z; bw[4 * j + 3] = v.w;
                 const uint4 r = PLANES == 2 ? lds128(at + kPlaneBytes) : make_uint4(0, 0, 0, 0);
@@ -512,21 +523,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(W_EMPTY(st));
-            const GroupK g = group_consts<PLANES>(sbits);
-            const bool all_fast = __all_sync(0xffffffffu, g.fast);
-            uint32_t v[32];
-            if (all_fast) {
+            GroupK g[kChunks];
+            bool all_fast = true;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) decode_word<PLANES, true>(bw[w], rw[w], g, &v[4 * w]);
-            } else {
-#pragma unroll
-                for (int w = 0; w < 8; ++w) decode_word<PLANES, false>(bw[w], rw[w], g, &v[4 * w]);
+            for (int ch = 0; ch < kChunks; ++ch) {
+                g[ch] = group_consts<PLANES>(sbits[ch]);
+                all_fast = all_fast && g[ch].fast;
             }
+            all_fast = __all_sync(0xffffffffu, all_fast);
             ok = mbar_wait(A_EMPTY(sa), a.phase ^ 1, abort_flag, status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            tc_st16(lane_addr + static_cast<uint32_t>(64 * sa), *reinterpret_cast<const uint32_t(*)[16]>(&v[0]));
-            tc_st16(lane_addr + static_cast<uint32_t>(64 * sa + 16), *reinterpret_cast<const uint32_t(*)[16]>(&v[16]));
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) {
+                uint32_t v[32];
+                if (all_fast) {
+#pragma unroll
+                    for (int w8 = 0; w8 < 8; ++w8)
+                        decode_word<PLANES, true>(bw[8 * ch + w8], rw[8 * ch + w8], g[ch], &v[4 * w8]);
+                } else {
+#pragma unroll
+                    for (int w8 = 0; w8 < 8; ++w8)
+                        decode_word<PLANES, false>(bw[8 * ch + w8], rw[8 * ch + w8], g[ch], &v[4 * w8]);
+                }
+                const uint32_t col = lane_addr + static_cast<uint32_t>(kACols * sa + 32 * ch);
+                tc_st16(col, *reinterpret_cast<const uint32_t(*)[16]>(&v[0]));
+                tc_st16(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&v[16]));
+            }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -562,7 +585,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         }
     } else if (warp == 20 && lane == 0 && steps > 0) {
         // ------------------------------------------------ activation copies
-        TileSeq q;
+        TileSeq<KB> q;
         q.init(B);
         int last_phase[8];
         for (int i = 0; i < 8; ++i) last_phase[i] = -1;
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         Ring a(SA), r(SB), d(ND);
         bool ok = true, issued = false;
         for (int tile = blockIdx.x; ok && tile < B.total_tiles; tile += gridDim.x, d.step()) {
-            const int nkb = B.p[tile_problem(B, tile)].k / kTcKB;
+            const int nkb = B.p[tile_problem(B, tile)].k / KB;
             const int db = d.slot;
             if (!__all_sync(0xffffffffu, mbar_wait(D_EMPTY(db), d.phase ^ 1, abort_flag, status))) break;
             tc_fence_after();
@@ -604,8 +627,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 const uint32_t b0 = sbase + static_cast<uint32_t>(sb) * stage_bytes;
                 if (elect_one()) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const uint32_t a_tmem = tmem + static_cast<uint32_t>(64 * sa + 8 * t);
+                    for (int t = 0; t < KB / 16; ++t) {
+                        const uint32_t a_tmem = tmem + static_cast<uint32_t>(kACols * sa + 8 * t);
                         const uint64_t bd = sw128_desc(b0 + static_cast<uint32_t>((t >> 2) * Npad * 128 + (t & 3) * 32));
                         tc_mma(d_tmem, a_tmem, bd, idesc, (kb | t) != 0 ? 1u : 0u);
                     }
@@ -680,17 +703,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// 2-D map of one nibble plane: uint8 [n][k/2], box 64 bytes x 128 rows.
-bool encode_plane(CUtensorMap *map, const void *plane, int n, int k)
+// 2-D map of one nibble plane: uint8 [n][k/2], box kb/2 bytes x 128 rows with
+// the swizzle of the same width (64 or 128 bytes).
+bool encode_plane(CUtensorMap *map, const void *plane, int n, int k, int kb)
 {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(n)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTcTile)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kb / 2), static_cast<cuuint32_t>(kTcTile)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(plane), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, kb == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -703,10 +728,10 @@ cudaError_t set_smem(F kernel, int bytes, std::atomic<int> &done)
     return e;
 }
 
-template <int PLANES, int G>
+template <int PLANES, int G, int KB>
 cudaError_t launch_tc(TcBatch &b, int smem, cudaStream_t s, unsigned int *status)
 {
-    auto k = tc_kernel<PLANES, G>;
+    auto k = tc_kernel<PLANES, G, KB>;
     static std::atomic<int> attr{0};
     const cudaError_t e = set_smem(k, smem, attr);
     if (e != cudaSuccess) return e;
@@ -725,19 +750,26 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
     unsigned int *status = device_status_ptr();
     if (!status) return NQ_ERR_CUDA;
     const int planes = verify ? 2 : 1, group = w[0].group;
+    bool k256 = true;   // every layer splits into 256-input k-blocks
+    for (int i = 0; i < count; ++i) k256 = k256 && (w[i].k_in % kTcKBWide == 0);
     TcBatch b{};
     for (int m0 = 0; m0 < M; m0 += kTcMaxN) {
         const int Mc = std::min(kTcMaxN, M - m0);
         const int npad = npad_of(Mc);
-        const uint32_t stage_bytes = 256u * npad;
-        const uint32_t wstage = planes * kTcTile * kWPitch;
+        // 256-input k-blocks halve the per-k-block hand-offs per weight byte; they
+        // fit tensor memory (3 x 128 A columns + 2 x Npad accumulator columns)
+        // when Npad <= 64
+        const int KB = (k256 && npad <= 64) ? kTcKBWide : kTcKB;
+        const int acols = KB / 2;
+        const uint32_t stage_bytes = 2u * KB * npad;
+        const uint32_t wstage = planes * kTcTile * (KB / 2);
         // shared memory: up to 96 KB of weight stages in flight per SM (at least 3
         // stages), the rest for activation stages (2 to 8)
         const uint32_t avail = 222u * 1024u - 2048u;
         const int wsn = std::max(3, std::min(planes == 2 ? 4 : 8, static_cast<int>((avail - 4 * stage_bytes) / wstage)));
         const int sb = std::max(2, std::min(8, static_cast<int>((avail - wsn * wstage) / stage_bytes)));
-        const int sa = (4 * 64 + 2 * npad <= kTmemCols) ? 4 : 3;
-        const int nd = (sa * 64 + 2 * npad <= kTmemCols) ? 2 : 1;
+        const int sa = (4 * acols + 2 * npad <= kTmemCols) ? 4 : 3;
+        const int nd = (sa * acols + 2 * npad <= kTmemCols) ? 2 : 1;
         // 1 CTA per SM: the kernel allocates all 512 tensor-memory columns
         const int smem = std::max<int>(static_cast<int>(sb * stage_bytes + wsn * wstage) + 8 * 56 + 64 + 1024,
                                        120 * 1024);
@@ -759,8 +791,8 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
                 p.k = L.k_in;
                 p.tile_begin = static_cast<int>(tiles);
                 p.pad = 0;
-                if (!encode_plane(&b.maps[i][0], L.base, L.n_out, L.k_in) ||
-                    (planes == 2 && !encode_plane(&b.maps[i][1], L.resid, L.n_out, L.k_in)))
+                if (!encode_plane(&b.maps[i][0], L.base, L.n_out, L.k_in, KB) ||
+                    (planes == 2 && !encode_plane(&b.maps[i][1], L.resid, L.n_out, L.k_in, KB)))
                     return NQ_ERR_CUDA;
                 const long long nt = (L.n_out + kTcTile - 1) / kTcTile;
                 tiles += nt;
@@ -782,8 +814,13 @@ nq_status tc_run(int count, const nq_weights *w, const uint16_t *const *x, int M
             tc_stage_kernel<<<dim3(gx, cnt), 256, 0, stream>>>(b, status);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return NQ_ERR_CUDA;
-            if (planes == 2) e = group == 128 ? launch_tc<2, 128>(b, smem, stream, status) : launch_tc<2, 64>(b, smem, stream, status);
-            else e = group == 128 ? launch_tc<1, 128>(b, smem, stream, status) : launch_tc<1, 64>(b, smem, stream, status);
+            if (KB == kTcKB) {
+                if (planes == 2) e = group == 128 ? launch_tc<2, 128, 128>(b, smem, stream, status) : launch_tc<2, 64, 128>(b, smem, stream, status);
+                else e = group == 128 ? launch_tc<1, 128, 128>(b, smem, stream, status) : launch_tc<1, 64, 128>(b, smem, stream, status);
+            } else {
+                if (planes == 2) e = group == 128 ? launch_tc<2, 128, 256>(b, smem, stream, status) : launch_tc<2, 64, 256>(b, smem, stream, status);
+                else e = group == 128 ? launch_tc<1, 128, 256>(b, smem, stream, status) : launch_tc<1, 64, 256>(b, smem, stream, status);
+            }
             if (e != cudaSuccess) return NQ_ERR_CUDA;
         }
     }

@@ -63,6 +63,12 @@ CASES = [  # (fmt, verify, n, k, group, M)
     ("NESTED44", False, 200, 384, 128, 16),    # draft: base plane only
     ("NESTED44", False, 333, 640, 64, 33),
     ("INT4", False, 140, 512, 128, 144),
+    # 256-input k-blocks (padded M <= 64 and k % 256 == 0)
+    ("NESTED44", True, 1000, 1024, 128, 16),
+    ("NESTED44", False, 1000, 1024, 128, 16),
+    ("NESTED44", True, 130, 768, 64, 64),
+    ("NESTED44", False, 257, 512, 64, 20),
+    ("INT4", False, 300, 1536, 128, 48),
 ]
 
 
