@@ -267,8 +267,8 @@ __device__ __forceinline__ void decode_word(uint32_t b, uint32_t r, const GroupK
         const uint32_t H = ((bx & 0xF0F0F0F0u) | ((rx >> 4) & 0x0F0F0F0Fu)) - 0x08080808u;
         c[0] = L & 0x00FF00FFu;
         c[1] = H & 0x00FF00FFu;
-        c[2] = (L >> 8) & 0x00FF00FFu;
-        c[3] = (H >> 8) & 0x00FF00FFu;
+        c[2] = __byte_perm(L, 0u, 0x4341);   // bytes 1 and 3 of L into the low byte of each half
+        c[3] = __byte_perm(H, 0u, 0x4341);
     } else {
         (void)r;
         c[0] = (bx << 4) & 0x00F000F0u;
