@@ -176,6 +176,11 @@ class Round:
                 else:
                     ys.append(torch.empty((M, n), dtype=torch.float32, device=device))
             self.batches.append(nq.LinearBatch(p == K_DRAFT, self.layers, xs, ys))
+        # target-only decoding step for Eq. (2)'s baseline: the 8-bit target (both
+        # planes) over one token per pass (M = 1), same weights and activations
+        self.target_only = nq.LinearBatch(True, self.layers, self.batches[0]._keep[1],
+                                          [torch.empty((1, n), dtype=torch.float32, device=device)
+                                           for _, n, _ in self.shapes])
         g = np.random.default_rng(seed + 2)
         self.draft = torch.from_numpy(g.integers(0, V_LM, size=(1, K_DRAFT), dtype=np.int32)).to(device)
         self.seeds = torch.from_numpy(np.array([seed + 3], dtype=np.int64)).to(device)
@@ -224,6 +229,43 @@ class Round:
     @property
     def d2h_bytes(self):
         return 2 * (K_DRAFT + 2) * 4
+
+    def time_target_only(self, iters=20):
+        torch = self.torch
+        for _ in range(3):
+            self.target_only()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            self.target_only()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / iters
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one draft-pass
+# launch of the streaming kernel at this workload, from an ncu capture of the
+# full-size round (1.01x the algorithmic 3,414,627,328 B: no re-reads).  Set to
+# None whenever that kernel changes until it is captured again.
+DRAFT_PASS_DRAM_BYTES = 3_452_500_000
+
+
+def eq2_report(t_draft_us, t_verify_us, t_accept_us, t_target_us, k=K_DRAFT):
+    """Erge, "Tokens per pass and time per token": Eq. (1) gives the expected
+    tokens per target pass E = (1 - a^(k+1)) / (1 - a) at acceptance rate a,
+    Eq. (2) the time per token t = (t_pass + k t_draft) / E, from the measured
+    pass times (t_pass = verify pass + acceptance).  The baseline is the
+    target alone, one token per pass (verify linears at M = 1)."""
+    t_pass = t_verify_us + t_accept_us
+    out = {"k": k, "t_draft_us": round(t_draft_us, 1), "t_pass_us": round(t_pass, 1),
+           "t_target_only_us": round(t_target_us, 1), "by_alpha": {}}
+    for a in (0.46, 0.6, 0.88, 0.95):
+        E = (1 - a ** (k + 1)) / (1 - a)
+        t = (t_pass + k * t_draft_us) / E
+        out["by_alpha"][str(a)] = {"tokens_per_pass": round(E, 3), "t_token_us": round(t, 1),
+                                   "speedup_vs_target_only": round(t_target_us / t, 3)}
+    return out
 
 
 # ------------------------------------------------------------------ acceptance at the sweep shape
@@ -581,12 +623,14 @@ def run_ours(args):
         "accept_round_us": round(statistics.mean(accept_ms) * 1e3, 2),
         "roofline": {"bound": "hbm", "kernel": "draft GEMV (one persistent launch per model pass, M=1)",
                      "achieved": round(draft_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(draft_gbs / hbm, 4), "peak_kind": peak_kind, "traffic": None,
+                     "frac": round(draft_gbs / hbm, 4), "peak_kind": peak_kind, "traffic": DRAFT_PASS_DRAM_BYTES,
                      "verify_achieved": round(verify_gbs, 1), "verify_frac": round(verify_gbs / hbm, 4)},
         "clocks": clk.summary(),
         "e2e": {"value": round(R.bytes_round * args.steps * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": R.h2d_bytes, "d2h_bytes_per_step": R.d2h_bytes},
         "gpu_launches": R.launches_per_round * args.steps,
+        "eq2_time_per_token": eq2_report(d_avg * 1e3, v_avg * 1e3, statistics.mean(accept_ms) * 1e3,
+                                         R.time_target_only()),
     }
     if not args.no_extras:
         line["accept_sweep_B64_V152064"] = accept_sweep(device)
