@@ -252,6 +252,9 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                 unsigned int *__restrict__ counters, float2 *__restrict__ part, SampleRec *__restrict__ rec,
                 unsigned int *status)
 {
+    // the resample pass may be scheduled now; it waits (griddepcontrol.wait) for
+    // this grid to complete before reading anything this grid writes
+    asm volatile("griddepcontrol.launch_dependents;");
     __shared__ MaxSum red[kThreads / 32];
     __shared__ RowRoots roots[2 * kMaxK + 1];
     __shared__ bool last;
@@ -485,6 +488,9 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                 unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ csum,
                 float *__restrict__ lsum)
 {
+    // launched as a programmatic dependent of the decision pass: wait for that
+    // grid to complete (its records and partials visible) before anything else
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float warp_sum[kThreads / 32];
     __shared__ __align__(16) float btree[2 * kMaxBlocks];
     __shared__ bool last;
@@ -692,12 +698,24 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     nq::sample_a_kernel<<<grid_a, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
                                                              reinterpret_cast<unsigned int *>(w + L.counters_a),
                                                              reinterpret_cast<float2 *>(w + L.part), rec, status);
-    dim3 grid_b(4 * nq::n_blocks(V), B);   // one CTA per (block, leaf quarter q)
-    nq::sample_b_kernel<<<grid_b, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
-                                                             reinterpret_cast<unsigned int *>(w + L.counters_b), rec,
-                                                             reinterpret_cast<float *>(w + L.csum),
-                                                             reinterpret_cast<float *>(w + L.lsum));
-    return nq::cuda_status(cudaGetLastError());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return NQ_ERR_CUDA;
+    // pass B as a programmatic dependent launch: its CTAs are scheduled while
+    // pass A drains and block in griddepcontrol.wait until pass A completes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4 * nq::n_blocks(V), B);   // one CTA per (block, leaf quarter q)
+    cfg.blockDim = dim3(nq::kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
+                           reinterpret_cast<unsigned int *>(w + L.counters_b), static_cast<const nq::SampleRec *>(rec),
+                           reinterpret_cast<float *>(w + L.csum), reinterpret_cast<float *>(w + L.lsum));
+    return nq::cuda_status(e);
 }
 
 // ------------------------------------------------------------------ allocation-free greedy acceptance
