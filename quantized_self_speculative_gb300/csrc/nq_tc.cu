@@ -26,9 +26,10 @@
 //   * warps 16-19 read the finished accumulators (tcgen05.ld) and store y.
 //
 // Decoding: offset-binary codes land in fp16 subnormals (code * 2^-24) with
-// integer masks only; one fma per pair, fma(code * 2^-24, s * 2^20, -8 s),
-// yields fp16(q8 * s / 16) (verify) or fp16(q4 * s) (draft) with one
-// rounding.  Groups with s * 2^20 beyond the fp16 range (s > 0.0625) take an
+// integer masks only; one fma per pair, fma(code * 2^-24, s * 2^20, -8 s) with
+// code = q8 + 128 (verify; the byte holds q8 + 136 and an exact subnormal
+// subtract removes the 8) or 16 (q4 + 8) (draft), yields fp16(q8 * s / 16) or
+// fp16(q4 * s) with one rounding.  Groups with s * 2^20 beyond the fp16 range (s > 0.0625) take an
 // equivalent exact path (1024-biased fp16 integer, subtract, multiply) with
 // the same result.  Every wait on an mbarrier is bounded by a timer; on a
 // timeout the CTA sets NQ_DEV_TIMEOUT, drains its copies and MMAs, frees its
@@ -258,13 +259,16 @@ __device__ __forceinline__ GroupK group_consts(unsigned short s_bits)
 template <int PLANES, bool FAST>
 __device__ __forceinline__ void decode_word(uint32_t b, uint32_t r, const GroupK &g, uint32_t *o)
 {
-    uint32_t c[4];   // codes as fp16 subnormals: (q8 + 128) or 16 (q4 + 8), times 2^-24
+    uint32_t c[4];   // codes as fp16 subnormals: (q8 + 136) or 16 (q4 + 8), times 2^-24
     const uint32_t bx = b ^ 0x88888888u;
     if constexpr (PLANES == 2) {
         const uint32_t rx = r ^ 0x88888888u;
-        // byte c of L: inputs 2c (base nibble high, refinement nibble low); H: inputs 2c+1
-        const uint32_t L = (((bx << 4) & 0xF0F0F0F0u) | (rx & 0x0F0F0F0Fu)) - 0x08080808u;
-        const uint32_t H = ((bx & 0xF0F0F0F0u) | ((rx >> 4) & 0x0F0F0F0Fu)) - 0x08080808u;
+        // byte c of L: inputs 2c (base nibble high, refinement nibble low); H: inputs
+        // 2c+1.  Each byte is 16 (q4 + 8) + (r + 8) = q8 + 136 in [0, 255]: q8 spans
+        // [-136, 119], so no byte-wide offset of 128 exists and the remaining -8 is
+        // taken per half below, where the sign fits.
+        const uint32_t L = ((bx << 4) & 0xF0F0F0F0u) | (rx & 0x0F0F0F0Fu);
+        const uint32_t H = (bx & 0xF0F0F0F0u) | ((rx >> 4) & 0x0F0F0F0Fu);
         c[0] = L & 0x00FF00FFu;
         c[1] = H & 0x00FF00FFu;
         c[2] = __byte_perm(L, 0u, 0x4341);   // bytes 1 and 3 of L into the low byte of each half
@@ -278,12 +282,15 @@ __device__ __forceinline__ void decode_word(uint32_t b, uint32_t r, const GroupK
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+        // verify: (q8 + 136) 2^-24 - 8 2^-24 is exact on the subnormal grid (sign
+        // included), leaving (q8 + 128) 2^-24 for the fma
+        const uint32_t cf = PLANES == 2 ? hsub2_u(c[i], 0x00080008u) : c[i];
         if constexpr (FAST) {
-            o[i] = hfma2_u(c[i], g.F, g.C);
+            o[i] = hfma2_u(cf, g.F, g.C);
         } else {
-            const uint32_t slow = PLANES == 2 ? hmul2_u(hsub2_u(c[i] | 0x64006400u, 0x64806480u), g.S)    // 1152
+            const uint32_t slow = PLANES == 2 ? hmul2_u(hsub2_u(c[i] | 0x64006400u, 0x64886488u), g.S)    // 1160
                                               : hmul2_u(hsub2_u((c[i] >> 4) | 0x64006400u, 0x64086408u), g.S);  // 1032
-            o[i] = g.fast ? hfma2_u(c[i], g.F, g.C) : slow;
+            o[i] = g.fast ? hfma2_u(cf, g.F, g.C) : slow;
         }
     }
 }

@@ -31,6 +31,27 @@ def weights(seed: int, n_out: int, k_in: int, std: float = 0.02) -> np.ndarray:
     return (rng(seed).standard_normal((n_out, k_in), dtype=np.float32) * np.float32(std)).astype(np.float32)
 
 
+def random_planes(seed: int, n_out: int, k_in: int, group: int):
+    """Packed nibble planes drawn byte-uniform (every 4-bit code pair, including
+    base -8 with a negative refinement, which quantising tiny weights also
+    produces) and fp16 group-scale bits from a mix of classes: zero, subnormal,
+    normal up to 0.0625, normal above it (up to 8), and negatives of the normal
+    classes.  Returns (base uint8 [n][k/2], resid uint8 [n][k/2],
+    scales uint16 [n][k/group])."""
+    g = rng(seed)
+    base = g.integers(0, 256, size=(n_out, k_in // 2), dtype=np.uint8)
+    resid = g.integers(0, 256, size=(n_out, k_in // 2), dtype=np.uint8)
+    shape = (n_out, k_in // group)
+    cls = g.integers(0, 6, size=shape)
+    bits = np.where(cls == 0, 0,
+           np.where(cls == 1, g.integers(1, 0x0400, size=shape),
+           np.where(cls == 2, g.integers(0x0400, 0x2C00, size=shape),
+           np.where(cls == 3, g.integers(0x2C00, 0x4800, size=shape),
+           np.where(cls == 4, 0x8000 | g.integers(0x0400, 0x2C00, size=shape),
+                    0x8000 | g.integers(0x2C00, 0x4800, size=shape))))))
+    return base, resid, bits.astype(np.uint16)
+
+
 def activations_bf16(seed: int, m: int, k_in: int, std: float = 1.0) -> np.ndarray:
     """x bf16 bits [m][k_in], values ~ N(0, std^2) rounded to bfloat16."""
     return f32_to_bf16_bits(rng(seed).standard_normal((m, k_in), dtype=np.float32) * np.float32(std))

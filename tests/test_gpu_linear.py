@@ -108,3 +108,23 @@ def test_rejected_arguments(nq):
     with pytest.raises(nq.NQError) as e:
         nq.draft_gemv(pl, x, y)
     assert e.value.status == nq.NQ_ERR_ALIGN
+
+
+@pytest.mark.parametrize("g", [64, 128])
+def test_every_code_pair_and_scale_class_exact(nq, g):
+    """Byte-uniform planes (every (q4, r) pair, q8 down to -136) under zero,
+    subnormal, small, large and negative group scales: identity activations
+    return each dequantised weight q8 s / 16 (verify) or q4 s (draft) exactly."""
+    from gpu_helpers import to_dev_u8
+    n, k = 160, 384
+    base, resid, scales = synth.random_planes(4400 + g, n, k, g)
+    pl = nq.PackedLinear(n, k, g, nq.FMT_NESTED44, to_dev_u8(base), to_dev_u8(resid), to_dev_u8(scales))
+    one = synth.f32_to_bf16_bits(np.float32([1.0]))[0]
+    x = np.zeros((k, k), np.uint16)
+    x[np.arange(k), np.arange(k)] = one
+    for verify in (False, True):
+        for m0 in range(0, k, 16):
+            xs = x[m0:m0 + 16]
+            y = (nq.verify_gemm if verify else nq.draft_gemv)(pl, bf16_dev(xs))
+            ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, xs, verify)
+            assert np.array_equal(y.cpu().numpy().astype(np.float64), ref), (verify, m0)

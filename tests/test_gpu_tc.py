@@ -155,3 +155,30 @@ def test_tc_small_m_falls_back(nq):
     y_plain = nq.verify_gemm(pl, x)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(ys[0].cpu().numpy(), y_plain.cpu().numpy())
+
+
+def _upload_planes(nq, base, resid, scales, n, k, g):
+    from gpu_helpers import to_dev_u8
+    return nq.PackedLinear(n, k, g, nq.FMT_NESTED44, to_dev_u8(base), to_dev_u8(resid), to_dev_u8(scales))
+
+
+@pytest.mark.parametrize("g", [64, 128])
+@pytest.mark.parametrize("rows_per_call", [256, 64])   # 128-input k-blocks; 256-input k-blocks (padded M <= 64)
+def test_tc_every_code_pair_and_scale_class(nq, g, rows_per_call):
+    """Byte-uniform planes (all 256 (q4, r) pairs, q4 = -8 with r < 0 included:
+    q8 = 16 q4 + r reaches -136) under zero, subnormal, fast, slow and negative
+    group scales; identity activations read back every decoded weight, which
+    must be fp16(q8 s / 16) (verify) or fp16(q4 s) (draft), rounded once."""
+    n, k = 192, 512
+    base, resid, scales = synth.random_planes(7600 + g, n, k, g)
+    pl = _upload_planes(nq, base, resid, scales, n, k, g)
+    one = synth.f32_to_bf16_bits(np.float32([1.0]))[0]
+    for verify in (False, True):
+        w16 = fp16_weights(base, resid, scales, n, k, g, verify).astype(np.float32)
+        for c0 in range(0, k, rows_per_call):
+            x = np.zeros((rows_per_call, k), np.uint16)
+            x[np.arange(rows_per_call), c0 + np.arange(rows_per_call)] = one
+            (y,) = run_tc(nq, [pl], [x], rows_per_call, verify)
+            np.testing.assert_array_equal(y, w16[:, c0:c0 + rows_per_call].T)
+            ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, x, verify)
+            assert normwise_err(y, ref) <= 2.0 ** -11
