@@ -72,16 +72,18 @@ def test_one_hot_columns_are_exact(nq):
         assert np.array_equal(y.cpu().numpy().astype(np.float64), ref)
 
 
-def test_batch_invariance_and_batched_call(nq):
+@pytest.mark.parametrize("fmt", ["NESTED44", "FP8E4M3_ROW", "FP16"])
+def test_batch_invariance_and_batched_call(nq, fmt):
     """Each output row is bit-identical whatever M is and whether the layer
     runs alone or inside a batched launch."""
+    f = getattr(nq, "FMT_" + fmt)
     shapes = [(256, 1024), (96, 2048), (1000, 512)]
     layers, xs = [], []
     for i, (n, k) in enumerate(shapes):
-        pl, _ = oracle_packed(nq, synth.weights(4400 + i, n, k), nq.FMT_NESTED44, 128)
+        pl, _ = oracle_packed(nq, synth.weights(4400 + i, n, k), f, 128 if fmt == "NESTED44" else 0)
         layers.append(pl)
         xs.append(bf16_dev(synth.activations_bf16(4410 + i, 9, k)))
-    for verify in (False, True):
+    for verify in ((False, True) if fmt == "NESTED44" else (True,)):
         fn = nq.verify_gemm if verify else nq.draft_gemv
         for pl, x in zip(layers, xs):
             full = fn(pl, x).cpu()
@@ -128,3 +130,37 @@ def test_every_code_pair_and_scale_class_exact(nq, g):
             y = (nq.verify_gemm if verify else nq.draft_gemv)(pl, bf16_dev(xs))
             ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, xs, verify)
             assert np.array_equal(y.cpu().numpy().astype(np.float64), ref), (verify, m0)
+
+
+@pytest.mark.parametrize("fmt", ["NESTED44", "FP8E4M3_ROW", "FP16"])
+def test_wide_batch_matches_oracle_and_single_calls(nq, fmt):
+    """A batch with enough rows for the widest (256-row) units: every output
+    equals the oracle and, bit for bit, the layer's own single-layer call
+    (4-warp units), at M = 5 and M = 9."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    f = getattr(nq, "FMT_" + fmt)
+    g = 128 if fmt == "NESTED44" else 0
+    shapes = []
+    while sum(n for n, _ in shapes) < 2 * sms * 256 + 4096:
+        i = len(shapes)
+        shapes.append((4096 - 40 * (i % 3), (256, 384, 512)[i % 3]))
+    layers, packs = [], []
+    for i, (n, k) in enumerate(shapes):
+        pl, planes = oracle_packed(nq, synth.weights(4600 + i, n, k), f, g)
+        layers.append(pl)
+        packs.append(planes)
+    passes = (False, True) if fmt == "NESTED44" else (True,)
+    for M in (5, 9):
+        xs_h = [synth.activations_bf16(4700 + i + M, M, k) for i, (_, k) in enumerate(shapes)]
+        xs = [bf16_dev(x) for x in xs_h]
+        for verify in passes:
+            ys = [torch.empty((M, n), dtype=torch.float32, device="cuda") for n, _ in shapes]
+            nq.LinearBatch(verify, layers, xs, ys)()
+            fn = nq.verify_gemm if verify else nq.draft_gemv
+            for i in (0, 1, 2, len(shapes) - 1):
+                n, k = shapes[i]
+                base, resid, scales = packs[i]
+                ref = O.linear(oracle_fmt(nq, f), n, k, g, base, resid, scales, xs_h[i], verify)
+                assert normwise_err(ys[i].cpu().numpy(), ref) <= TOL, (fmt, M, verify, i)
+            for i in range(len(shapes)):
+                assert torch.equal(ys[i].cpu(), fn(layers[i], xs[i]).cpu()), (fmt, M, verify, i)
