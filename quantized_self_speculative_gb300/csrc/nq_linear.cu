@@ -48,11 +48,15 @@ namespace {
 constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
 constexpr int kMaxM = 16;             // activation rows per launch (two 8-column MMA tiles)
 constexpr int kXsMax = 112 * 1024;    // dynamic shared memory cap per CTA (two CTAs fit one SM)
-// Activation staging cap: the whole activation matrix at M = 1 (K <= 11008),
-// segments beyond.  Measured on GB300: a larger buffer shrinks L1 and slows
-// the verify pass (4.5 TB/s at 48 KB, 2.5 TB/s at 112 KB vs 4.9 TB/s at
-// 40 KB), a smaller one forces restaging at M = 1.
-constexpr int kXsStage = 40 * 1024;
+// Activation staging cap: whole activation rows up to K = 4096 at M <= 6
+// (and K = 11008 at M <= 2) with 16-warp units, segments beyond.  Shared
+// memory is carved out of L1, so the cap trades restaging against L1: with
+// one 16-warp CTA per SM, 56 KB measured best on whole-model passes
+// (LLaMA-2-7B verify at M = 5 and Qwen2.5-7B FP8 verify at M = 7 1.2% and 5%
+// faster than at 40 KB); with two 8-warp CTAs per SM anything above 40 KB
+// was slower.
+constexpr int kXsStageWide = 56 * 1024;   // 16-warp units (one CTA per SM)
+constexpr int kXsStage = 40 * 1024;       // 8- and 4-warp units
 
 enum Kind { kNib = 0, kFp8 = 1, kFp16 = 2 };
 
@@ -601,15 +605,15 @@ nq_status check_layer(const nq_weights &w, bool verify, int &kind, int &planes)
 }
 
 // Dynamic shared memory for a launch: all activation rows of the widest layer
-// (in fp16, padded rows, plus offset corrections), capped at kXsMax.
-int xs_bytes_for(int kind, int M, int kmax, int group)
+// (in fp16, padded rows, plus offset corrections), capped by the unit width.
+int xs_bytes_for(int kind, int M, int kmax, int group, int warps)
 {
     const int ch = kind == kNib ? group : (kind == kFp8 ? 64 : 32);
     const int chunks = kmax / ch;
     const int mt = M > 8 ? 16 : 8;
     const long long need = static_cast<long long>(M) * (chunks * 2 * ch + kRowPad) +
                            (kind == kNib ? static_cast<long long>(chunks) * mt * 4 : 0);
-    return static_cast<int>(std::min<long long>(need, kXsStage));
+    return static_cast<int>(std::min<long long>(need, warps == 16 ? kXsStageWide : kXsStage));
 }
 
 template <int MAXP>
@@ -660,7 +664,7 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
             b.count = cnt;
             b.total_units = static_cast<int>(units);
             b.M = Mc;
-            b.xs_bytes = xs_bytes_for(kind, Mc, kmax, group);
+            b.xs_bytes = xs_bytes_for(kind, Mc, kmax, group, warps);
             const cudaError_t e = launch_kind<MAXP>(kind, planes, group, nt, warps, b, stream, status);
             if (e != cudaSuccess) return NQ_ERR_CUDA;
         }

@@ -182,3 +182,28 @@ def test_tc_every_code_pair_and_scale_class(nq, g, rows_per_call):
             np.testing.assert_array_equal(y, w16[:, c0:c0 + rows_per_call].T)
             ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, x, verify)
             assert normwise_err(y, ref) <= 2.0 ** -11
+
+
+def test_tc_repeated_launches_are_bit_identical(nq):
+    """Warp-specialised stages hand data over through mbarriers; a missed
+    hand-off would show up as run-to-run differences.  Twelve launches of a
+    multi-layer batch at the batched-verify width give one result."""
+    shapes = [(1024, 1024), (300, 2048), (640, 512)]
+    M, g = 144, 128
+    layers = [oracle_packed(nq, synth.weights(7700 + i, n, k), nq.FMT_NESTED44, g)[0]
+              for i, (n, k) in enumerate(shapes)]
+    xs = [bf16_dev(synth.activations_bf16(7710 + i, M, k)) for i, (_, k) in enumerate(shapes)]
+    for verify in (False, True):
+        ys = [torch.empty((M, n), dtype=torch.float32, device="cuda") for n, _ in shapes]
+        b = nq.LinearBatch(verify, layers, xs, ys, tensor_cores=True)
+        first = None
+        for _ in range(12):
+            for y in ys:
+                y.fill_(float("nan"))
+            b()
+            got = [y.cpu() for y in ys]
+            if first is None:
+                first = got
+            else:
+                for a, c in zip(first, got):
+                    assert torch.equal(a, c)
