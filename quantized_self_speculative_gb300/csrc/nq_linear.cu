@@ -191,7 +191,11 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     constexpr int MT = 8 * NT;
     constexpr int CORR = KIND == kNib ? MT * 4 : 0;   // offset-correction bytes per chunk
     constexpr int LANE_BYTES = 2 * PLANES * VB;
-    constexpr int R = LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8);   // ring slots (R-1 chunks in flight)
+    // ring slots (R - 1 chunks in flight), measured per kind on whole-model
+    // passes: nibbles 3 (both planes) / 5 (one plane, 128-input groups); E4M3
+    // and fp16 rows 7 with one 8-column tile and 6 with two (4% faster than 5
+    // for E4M3 at M = 3..7)
+    constexpr int R = KIND == kNib ? (LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8)) : (NT == 1 ? 7 : 6);
     constexpr int ROWS = 16 * WARPS;
     constexpr float kNeg8Ulp = -4.76837158203125e-07f;   // -8 * 2^-24
 
