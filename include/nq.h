@@ -60,7 +60,7 @@ typedef enum {
     NQ_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned */
     NQ_ERR_CUDA = 4,       /* a CUDA runtime call failed (launch error, bad device) */
     NQ_ERR_NONFINITE = 5,  /* reported by nq_get_device_status(): non-finite logits */
-    NQ_ERR_TIMEOUT = 6,    /* reserved: a bounded device wait gave up */
+    NQ_ERR_TIMEOUT = 6,    /* reserved (a bounded device wait that gives up sets NQ_DEV_TIMEOUT) */
     NQ_ERR_WORKSPACE = 7,  /* workspace NULL or smaller than the *_workspace_bytes() size */
     NQ_ERR_TOKEN = 8       /* reported by nq_get_device_status(): draft id outside [0, V) */
 } nq_status;
@@ -244,6 +244,19 @@ NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_log
  */
 NQ_API nq_status spec_accept_greedy_noalloc(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
                                             int32_t *out_tok, int32_t *out_cnt, cudaStream_t stream);
+
+/*
+ * Diagnostic for the failure path of the library's bounded device waits (the
+ * tensor-core linears hand stages between warp roles through mbarriers, each
+ * wait limited to 2 s).  Launches one warp that waits, through the same
+ * bounded wait, on an mbarrier that nothing ever completes; after limit_us
+ * microseconds (1 .. 1,000,000) the wait gives up, sets NQ_DEV_TIMEOUT in the
+ * sticky status word and the kernel returns.  Nothing else is in flight, so
+ * the CUDA context stays usable: read the bit with nq_get_device_status().
+ * Returns NQ_ERR_ARG for a limit outside that range, NQ_ERR_CUDA if the launch
+ * fails, else NQ_OK (asynchronous on `stream`).
+ */
+NQ_API nq_status nq_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 NQ_API const char *nq_status_string(int status);

@@ -112,22 +112,27 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-// Wait for the phase of `bar` with the given parity.  Gives up after kWaitNs
-// (sets the CTA's abort flag and NQ_DEV_TIMEOUT) or when another role of the
-// CTA has given up; returns false then.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                            unsigned int *status)
+// Wait for the phase of `bar` with the given parity.  Gives up after
+// limit_ns (sets the CTA's abort flag and NQ_DEV_TIMEOUT) or when another
+// role of the CTA has given up; returns false then.
+__device__ __noinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned int *status, unsigned long long limit_ns)
 {
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             set_status(status, NQ_DEV_TIMEOUT);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                               unsigned int *status)
+{
+    return mbar_wait_until(bar, parity, abort_flag, status, kWaitNs);
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *status)
@@ -667,6 +672,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     }
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One warp waits, through the library's bounded wait, on an mbarrier that no
+// thread or copy ever completes: the wait gives up after limit_ns, sets
+// NQ_DEV_TIMEOUT and the kernel returns.  Nothing is in flight, so the
+// context stays usable.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(unsigned long long limit_ns, unsigned int *status)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const bool ok = mbar_test(b, 0) || mbar_wait_until(b, 0, &abort_flag, status, limit_ns);
+    (void)__all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- host side
 int npad_of(int M) { return (std::min(M, kTcMaxN) + 15) / 16 * 16; }
 
@@ -838,3 +863,12 @@ bool tc_route(int count, const nq_weights *w, int M, bool verify) { return tc_ro
 size_t tc_workspace_bytes(int count, const nq_weights *w, int M) { return tc_workspace(count, w, M); }
 
 }  // namespace nq
+
+extern "C" nq_status nq_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return NQ_ERR_ARG;
+    unsigned int *status = nq::device_status_ptr();
+    if (!status) return NQ_ERR_CUDA;
+    nq::wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(limit_us) * 1000ull, status);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}

@@ -67,6 +67,8 @@ def lib():
             L.nq_status_string.argtypes = [i32]
             L.nq_status_string.restype = C.c_char_p
             L.nq_get_device_status.argtypes = [vp, C.POINTER(C.c_uint32)]
+            L.nq_selftest_bounded_wait.argtypes = [C.c_uint32, vp]
+            L.nq_selftest_bounded_wait.restype = i32
             for name in ("nq_packed_bytes", "nq_pack_weights", "nq_draft_gemv", "nq_verify_gemm",
                          "nq_draft_gemv_batch", "nq_verify_gemm_batch", "spec_accept_greedy",
                          "spec_accept_sample", "nq_get_device_status"):
@@ -259,6 +261,12 @@ def accept_sample(draft: torch.Tensor, draft_logits: torch.Tensor, tgt_logits: t
                                     _dev(out_cnt, torch.int32, "out_cnt"), _dev(ws, torch.uint8, "ws"), ws.numel(),
                                     _stream(stream)), "spec_accept_sample")
     return out_tok, out_cnt
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Run the bounded-wait diagnostic (a wait that nothing completes gives up
+    after limit_us and sets NQ_DEV_TIMEOUT); read the bit with device_status()."""
+    _check(lib().nq_selftest_bounded_wait(int(limit_us), _stream(stream)), "nq_selftest_bounded_wait")
 
 
 def device_status(stream=None) -> int:

@@ -145,6 +145,9 @@ def test_host_validation_rejects_before_launch(L):
     assert L.nq_pack_weights(None, C.byref(W), None) == nq.NQ_ERR_ARG
     assert L.nq_pack_weights(A + 4, C.byref(W), None) == nq.NQ_ERR_ALIGN
     assert L.nq_get_device_status(None, None) == nq.NQ_ERR_ARG
+    L.nq_selftest_bounded_wait.argtypes = [C.c_uint32, C.c_void_p]
+    assert L.nq_selftest_bounded_wait(0, None) == nq.NQ_ERR_ARG
+    assert L.nq_selftest_bounded_wait(1000001, None) == nq.NQ_ERR_ARG
 
 
 def test_product_and_oracle_share_nothing():

@@ -207,3 +207,25 @@ def test_tc_repeated_launches_are_bit_identical(nq):
             else:
                 for a, c in zip(first, got):
                     assert torch.equal(a, c)
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(nq):
+    """Failure path of the bounded mbarrier waits, without a GPU fault: a wait
+    that nothing completes gives up after its limit and reports
+    NQ_DEV_TIMEOUT; later launches run clean."""
+    import time
+    torch.cuda.synchronize()
+    nq.device_status()
+    t0 = time.perf_counter()
+    nq.selftest_bounded_wait(20000)          # 20 ms
+    st = nq.device_status()
+    dt = time.perf_counter() - t0
+    assert st & nq.NQ_DEV_TIMEOUT, st
+    assert 0.02 <= dt < 10.0, dt
+    # the context is usable: a tensor-core pass afterwards is correct and clean
+    n, k, g, M = 200, 512, 128, 32
+    pl, (base, resid, scales) = oracle_packed(nq, synth.weights(7800, n, k), nq.FMT_NESTED44, g)
+    x = synth.activations_bf16(7801, M, k)
+    (y,) = run_tc(nq, [pl], [x], M, True)
+    ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, x, True)
+    assert normwise_err(y, ref) <= TOL
