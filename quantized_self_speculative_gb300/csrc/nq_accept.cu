@@ -25,7 +25,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLeaf = 16;
-constexpr int kChunk = kThreads * kLeaf;     // vocabulary entries per greedy CTA
+constexpr int kChunk = kThreads * kLeaf;     // vocabulary entries per workspace partial slot
+constexpr int kGreedyChunk = 4 * kChunk;     // vocabulary entries per greedy CTA
 constexpr int kMaxChunks = 128;              // V <= 524288
 constexpr int kBlock = 4 * kChunk;           // vocabulary entries per sampling CTA (1024 leaves)
 constexpr int kMaxBlocks = kMaxChunks / 4;   // 32
@@ -33,6 +34,7 @@ constexpr int kMaxK = 16;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 inline int n_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+inline int n_greedy_chunks(int V) { return (V + kGreedyChunk - 1) / kGreedyChunk; }
 inline int n_blocks(int V) { return (V + kBlock - 1) / kBlock; }
 inline size_t counters_bytes(int B) { return (static_cast<size_t>(B) * 4 + 255) / 256 * 256; }
 
@@ -70,23 +72,32 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 
     ValIdx best{-INFINITY, 0x7fffffff};
     float finite = 0.0f;   // becomes NaN if any entry is not finite
-    const int x0 = c * kChunk;
+    const int x0 = c * kGreedyChunk;
     if ((V & 3) == 0) {
+        // two batches of eight 16-byte loads per thread (eight in flight)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int x = x0 + r * (kThreads * 4) + threadIdx.x * 4;
-            if (x < V) {
-                const float4 v = __ldcs(reinterpret_cast<const float4 *>(vec + x));
-                finite = __fmaf_rn(0.0f, v.x, finite); finite = __fmaf_rn(0.0f, v.y, finite);
-                finite = __fmaf_rn(0.0f, v.z, finite); finite = __fmaf_rn(0.0f, v.w, finite);
-                best = better(best, ValIdx{v.x, x});
-                best = better(best, ValIdx{v.y, x + 1});
-                best = better(best, ValIdx{v.z, x + 2});
-                best = better(best, ValIdx{v.w, x + 3});
+        for (int h = 0; h < 2; ++h) {
+            float4 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int x = x0 + (8 * h + r) * (kThreads * 4) + threadIdx.x * 4;
+                v[r] = x < V ? __ldcs(reinterpret_cast<const float4 *>(vec + x)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int x = x0 + (8 * h + r) * (kThreads * 4) + threadIdx.x * 4;
+                if (x < V) {
+                    finite = __fmaf_rn(0.0f, v[r].x, finite); finite = __fmaf_rn(0.0f, v[r].y, finite);
+                    finite = __fmaf_rn(0.0f, v[r].z, finite); finite = __fmaf_rn(0.0f, v[r].w, finite);
+                    best = better(best, ValIdx{v[r].x, x});
+                    best = better(best, ValIdx{v[r].y, x + 1});
+                    best = better(best, ValIdx{v[r].z, x + 2});
+                    best = better(best, ValIdx{v[r].w, x + 3});
+                }
             }
         }
     } else {
-        for (int e = threadIdx.x; e < kChunk; e += kThreads) {
+        for (int e = threadIdx.x; e < kGreedyChunk; e += kThreads) {
             const int x = x0 + e;
             if (x < V) {
                 const float v = vec[x];
@@ -669,7 +680,7 @@ extern "C" nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_l
     if (!status) return NQ_ERR_CUDA;
     const nq::WsLayout L = nq::ws_layout(B, k, V);
     char *w = static_cast<char *>(ws);
-    dim3 grid(nq::n_chunks(V), k + 1, B);
+    dim3 grid(nq::n_greedy_chunks(V), k + 1, B);
     nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
                                                          reinterpret_cast<unsigned int *>(w + L.counters_a),
                                                          reinterpret_cast<float2 *>(w + L.part), status);
@@ -774,7 +785,7 @@ extern "C" nq_status spec_accept_greedy_noalloc(const int32_t *draft, const floa
     if (!scratch || !status) return NQ_ERR_CUDA;
     // the per-row tickets must start at zero; the partials are overwritten
     if (cudaMemsetAsync(scratch, 0, counters, stream) != cudaSuccess) return NQ_ERR_CUDA;
-    dim3 grid(nq::n_chunks(V), k + 1, B);
+    dim3 grid(nq::n_greedy_chunks(V), k + 1, B);
     nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
                                                          reinterpret_cast<unsigned int *>(scratch),
                                                          reinterpret_cast<float2 *>(scratch + counters), status);
