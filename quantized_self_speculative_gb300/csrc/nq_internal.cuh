@@ -51,15 +51,7 @@ __device__ __forceinline__ unsigned short ld_nc_u16(const void *p)
     return v;
 }
 
-// D += A(16x16) * B(16x8), bf16 inputs, fp32 accumulators (legacy warp MMA).
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+// D += A(16x16) * B(16x8), fp16 inputs, fp32 accumulators (warp MMA).
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1)
 {
@@ -67,16 +59,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
                  "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two 4-bit two's-complement codes -> bf16x2 holding (136 + code) each.
-// Nibble i of w goes to the low half, nibble i+4 to the high half.  The
-// constant 0x4300 is bf16 128.0 (unit spacing); XOR 8 maps the signed nibble
-// to offset binary, so the value is 128 + (nib ^ 8) = 136 + code, exactly.
-template <int I>
-__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w)
-{
-    return ((w >> (4 * I)) & 0x000F000Fu) ^ 0x43084308u;
 }
 
 // Four E4M3 codes (bytes 0..3 of w) -> two f16x2 (bytes 0,1 and 2,3), exact.
