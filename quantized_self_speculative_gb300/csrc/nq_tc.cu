@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     constexpr uint32_t kWStage = PLANES * kPlaneBytes;          // 1024-byte multiple (TMA swizzle atoms)
     const uint32_t wbase = sbase + static_cast<uint32_t>(SB) * stage_bytes;
     // barriers: a_full[4] a_empty[4] b_full[8] b_empty[8] d_full[2] d_empty[2] done w_full[12] w_empty[12]
+    // done_all
     const uint32_t bars = wbase + static_cast<uint32_t>(WS) * kWStage;
     auto A_FULL = [&](int i) { return bars + 8u * i; };
     auto A_EMPTY = [&](int i) { return bars + 8u * (4 + i); };
@@ -427,6 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     auto D_FULL = [&](int i) { return bars + 8u * (24 + i); };
     auto D_EMPTY = [&](int i) { return bars + 8u * (26 + i); };
     const uint32_t DONE = bars + 8u * 28;
+    const uint32_t DONE_ALL = bars + 8u * 53;   // 32 arrivals: the MMA warp's commits after an abort
     auto W_FULL = [&](int i) { return bars + 8u * (29 + i); };
     auto W_EMPTY = [&](int i) { return bars + 8u * (41 + i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bars - sbase) + 8 * 56);
@@ -438,6 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         for (int i = 0; i < 8; ++i) { mbar_init(B_FULL(i), 1); mbar_init(B_EMPTY(i), 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(D_FULL(i), 1); mbar_init(D_EMPTY(i), 4); }
         mbar_init(DONE, 1);
+        mbar_init(DONE_ALL, 32);
         for (int i = 0; i < 12; ++i) { mbar_init(W_FULL(i), 1); mbar_init(W_EMPTY(i), 8); }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -533,6 +536,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 const uint4 r = PLANES == 2 ? lds128(at + kPlaneBytes) : make_uint4(0, 0, 0, 0);
                 rw[4 * j] = r.x; rw[4 * j + 1] = r.y; rw[4 * j + 2] = r.z; rw[4 * j + 3] = r.w;
             }
+            // the stage is refilled by TMA (async proxy) once every decode warp has
+            // arrived: order this thread's shared-memory reads (generic proxy)
+            // before that write.  Without the fence a refill could land before a
+            // lane's read and feed that row the next k-block's codes (seen as rare
+            // run-to-run differences in single rows at M = 144).
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(W_EMPTY(st));
             GroupK g[kChunks];
@@ -630,6 +639,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
             if (!__all_sync(0xffffffffu, mbar_wait(D_EMPTY(db), d.phase ^ 1, abort_flag, status))) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + dcol0 + static_cast<uint32_t>(db * Npad);
+            const bool last_tile = tile + static_cast<int>(gridDim.x) >= B.total_tiles;
             for (int kb = 0; kb < nkb; ++kb, a.step(), r.step()) {
                 const int sa = a.slot, sb = r.slot;
                 bool w_ok = mbar_wait(A_FULL(sa), a.phase, abort_flag, status) &&
@@ -637,6 +647,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t b0 = sbase + static_cast<uint32_t>(sb) * stage_bytes;
+                // every commit comes from the thread that issued the MMAs it must
+                // track (a commit covers the issuing thread's own prior MMAs)
                 if (elect_one()) {
 #pragma unroll
                     for (int t = 0; t < KB / 16; ++t) {
@@ -646,20 +658,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                     }
                     tc_commit(A_EMPTY(sa));
                     tc_commit(B_EMPTY(sb));
+                    if (kb == nkb - 1) {
+                        tc_commit(D_FULL(db));
+                        // all MMAs of this CTA have completed before tensor memory is freed
+                        if (last_tile) tc_commit(DONE);
+                    }
                 }
                 __syncwarp();
                 issued = true;
             }
             if (!ok) break;
-            if (elect_one()) tc_commit(D_FULL(db));
-            __syncwarp();
         }
         if (issued) {
-            // all MMAs issued by this warp have completed before tensor memory is freed
-            if (elect_one()) tc_commit(DONE);
-            __syncwarp();
             volatile int never = 0;
-            mbar_wait(DONE, 0, &never, status);
+            if (ok) {
+                mbar_wait(DONE, 0, &never, status);
+            } else {
+                // a wait gave up mid-tile: every lane commits (each commit covers that
+                // lane's own MMAs; the barrier completes after all 32), then wait
+                tc_commit(DONE_ALL);
+                __syncwarp();
+                mbar_wait(DONE_ALL, 0, &never, status);
+            }
         }
     }
 

@@ -229,3 +229,32 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable(nq):
     (y,) = run_tc(nq, [pl], [x], M, True)
     ref = O.linear(O.FMT_NESTED44, n, k, g, base, resid, scales, x, True)
     assert normwise_err(y, ref) <= TOL
+
+
+def test_tc_full_width_batch_is_repeatable(nq):
+    """The batched-verify workload itself (8 LLaMA-3-8B-shaped layers, M = 144,
+    2688 tiles): 30 launches give one bit pattern.  A missing proxy fence
+    between the decoders' shared-memory reads and the TMA refill of a weight
+    stage showed up here as a differing tile in about one pass in ten."""
+    layer, _, _ = synth.llama3_8b_linears()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    layers = []
+    for _ in range(8):
+        for _, n, k in layer:
+            w = torch.randn((n, k), generator=gen, device="cuda").mul_(0.02)
+            layers.append(nq.pack_weights(w, nq.FMT_NESTED44, 128))
+            del w
+    M = 144
+    xs = [torch.randn((M, L.k_in), generator=gen, device="cuda").to(torch.bfloat16) for L in layers]
+    ys = [torch.empty((M, L.n_out), dtype=torch.float32, device="cuda") for L in layers]
+    b = nq.LinearBatch(True, layers, xs, ys, tensor_cores=True)
+    b()
+    torch.cuda.synchronize()
+    first = [y.clone() for y in ys]
+    for _ in range(30):
+        b()
+        torch.cuda.synchronize()
+        for y, y0 in zip(ys, first):
+            assert torch.equal(y, y0)
+    assert nq.device_status() == 0
