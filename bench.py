@@ -46,6 +46,18 @@ def peaks():
         return 6800.0, "fallback"
 
 
+NOMINAL_HBM_GBS = 8000.0   # HBM3e nominal, reported beside the measured-peak fraction
+
+
+def bf16_peak_tflops():
+    """Measured dense bf16 (= fp16) tensor throughput, burst; fallback 1900."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi samples during the timed region (read-only queries)."""
@@ -354,9 +366,11 @@ def _time_pass(device, layers, M, verify, iters=10, tensor_cores=False):
         sb = (2 * L.n_out * L.k_in // L.group) if L.fmt in (nq.FMT_NESTED44, nq.FMT_INT4) else (4 * L.n_out if L.fmt == nq.FMT_FP8E4M3_ROW else 0)
         byts += wb + sb + 2 * M * L.k_in + 4 * M * L.n_out
     hbm, _ = peaks()
+    tflops = 2.0 * M * sum(L.n_out * L.k_in for L in layers) / (us * 1e-6) / 1e12
     return {"M": M, "us": round(us, 1), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
-            "frac": round(byts / (us * 1e-6) / 1e9 / hbm, 4), "bytes": int(byts),
-            "tflops": round(2.0 * M * sum(L.n_out * L.k_in for L in layers) / (us * 1e-6) / 1e12, 2)}
+            "frac": round(byts / (us * 1e-6) / 1e9 / hbm, 4),
+            "frac_nominal": round(byts / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4), "bytes": int(byts),
+            "tflops": round(tflops, 2), "frac_tensor": round(tflops / bf16_peak_tflops(), 4)}
 
 
 def _shapes(spec):
@@ -656,7 +670,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "draft GEMV (one persistent launch per model pass, M=1)",
                      "achieved": round(draft_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(draft_gbs / hbm, 4), "peak_kind": peak_kind, "traffic": DRAFT_PASS_DRAM_BYTES,
-                     "verify_achieved": round(verify_gbs, 1), "verify_frac": round(verify_gbs / hbm, 4)},
+                     "verify_achieved": round(verify_gbs, 1), "verify_frac": round(verify_gbs / hbm, 4),
+                     "frac_nominal": round(draft_gbs / NOMINAL_HBM_GBS, 4),
+                     "verify_frac_nominal": round(verify_gbs / NOMINAL_HBM_GBS, 4)},
         "clocks": clk.summary(),
         "e2e": {"value": round(R.bytes_round * args.steps * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": R.h2d_bytes, "d2h_bytes_per_step": R.d2h_bytes},
