@@ -31,7 +31,7 @@
  *   [Philox]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *              as 1, 2, 3", SC'11 -- the Philox4x32-10 bijection.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   R1  per (row, group of G consecutive inputs) symmetric scale
  *       s = fp16(fp32(absmax / 7)); base q4 = clamp(rint(w/s), -8, 7);
  *       refinement r = clamp(rint(16 (w/s - q4)), -8, 7); residual scale s/16;

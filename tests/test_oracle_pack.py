@@ -2,8 +2,9 @@
 
 BitNest, Fig. 2: a b-bit base plus an r-bit refinement of the remaining error;
 Fig. 3: two independent 4-bit planes of N/2 bytes each, the target recovers
-the full 8-bit representation.  The reading fixed here (scale, rounding,
-residual step s/16) is listed in the design doc.
+the full 8-bit representation.  The pages fix neither the scale nor the
+rounding; the reading pinned here: s = fp16(absmax / 7) per group, rint
+(half to even), refinement step s/16.
 """
 import numpy as np
 import pytest
