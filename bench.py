@@ -568,6 +568,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Largest value over the ranks (the job takes as long as its slowest
+    replica); a no-op for one process."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: float, steps: int, world: int, t_max_ms: float) -> float:
+    """Whole-job throughput: every rank streams bytes_per_step per step (weak
+    scaling), the job lasts t_max_ms."""
+    return bytes_per_step * steps * world / (t_max_ms * 1e-3) / 1e9
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -627,11 +644,7 @@ def run_ours(args):
     draft_ms = [ev[s][p].elapsed_time(ev[s][p + 1]) for s in range(args.steps) for p in range(K_DRAFT)]
     verify_ms = [ev[s][K_DRAFT].elapsed_time(ev[s][K_DRAFT + 1]) for s in range(args.steps)]
     accept_ms = [ev[s][K_DRAFT + 1].elapsed_time(ev[s][K_DRAFT + 2]) for s in range(args.steps)]
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = reduce_max(ms, world, device)
     # ---- end to end: host activations in, emitted tokens out
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -640,15 +653,11 @@ def run_ours(args):
         R.run_e2e()
     e1.record()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device)
     if rank != 0:
         return
     hbm, peak_kind = peaks()
-    value = R.bytes_round * args.steps * world / (t_max * 1e-3) / 1e9
+    value = whole_job_gbs(R.bytes_round, args.steps, world, t_max)
     d_avg = statistics.mean(draft_ms)
     v_avg = statistics.mean(verify_ms)
     draft_gbs = R.bytes_draft_pass / (d_avg * 1e-3) / 1e9
@@ -674,7 +683,7 @@ def run_ours(args):
                      "frac_nominal": round(draft_gbs / NOMINAL_HBM_GBS, 4),
                      "verify_frac_nominal": round(verify_gbs / NOMINAL_HBM_GBS, 4)},
         "clocks": clk.summary(),
-        "e2e": {"value": round(R.bytes_round * args.steps * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(R.bytes_round, args.steps, world, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": R.h2d_bytes, "d2h_bytes_per_step": R.d2h_bytes},
         "gpu_launches": R.launches_per_round * args.steps,
         "eq2_time_per_token": eq2_report(d_avg * 1e3, v_avg * 1e3, statistics.mean(accept_ms) * 1e3,
