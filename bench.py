@@ -611,11 +611,11 @@ def run_reference(args):
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
+    torch.cuda.set_device(local)          # before the process group: NCCL binds the current device
+    device = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
     from quantized_self_speculative_gb300 import build
     build.build()
     R = Round(device, seed=17 + rank)
