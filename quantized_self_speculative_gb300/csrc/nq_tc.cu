@@ -31,9 +31,12 @@
 // subtract removes the 8) or 16 (q4 + 8) (draft), yields fp16(q8 * s / 16) or
 // fp16(q4 * s) with one rounding.  Groups with s * 2^20 beyond the fp16 range (s > 0.0625) take an
 // equivalent exact path (1024-biased fp16 integer, subtract, multiply) with
-// the same result.  Every wait on an mbarrier is bounded by a timer; on a
-// timeout the CTA sets NQ_DEV_TIMEOUT, drains its copies and MMAs, frees its
-// tensor memory and returns.
+// the same result.  Stage hand-offs: a weight stage is read through the
+// generic proxy and refilled by TMA through the async proxy, so the readers
+// fence (fence.proxy.async) before releasing it; every tcgen05.commit is
+// issued by the thread whose MMAs it must track.  Every wait on an mbarrier
+// is bounded by a timer; on a timeout the CTA sets NQ_DEV_TIMEOUT, drains its
+// copies and MMAs, frees its tensor memory and returns.
 #include "nq_internal.cuh"
 
 #include <cuda.h>           // CUtensorMap (types only; the encoder is fetched through the runtime)
