@@ -313,8 +313,9 @@ def accept_sweep(device, iters=20):
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / iters
             byts = accept_bytes(B, k, V, kind == "sample")
+            gbs = byts / (us * 1e-6) / 1e9
             res[kind] = {"us": round(us, 2), "rounds_per_s": round(B / (us * 1e-6), 1),
-                         "gbs": round(byts / (us * 1e-6) / 1e9, 1)}
+                         "gbs": round(gbs, 1), "frac": round(gbs / peaks()[0], 4)}
         out[f"k{k}"] = res
         del tl, dl
     return out
