@@ -167,7 +167,7 @@ struct SampleRec {      // per-row decision, written by pass A, read by pass B
 
 // Workspace layout shared by the greedy and sampled calls.
 struct WsLayout {
-    size_t counters_a, counters_b, part, rec, csum, lsum, total;
+    size_t counters_a, counters_b, part, rec, qsum, lsum, total;
 };
 
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
@@ -183,8 +183,8 @@ inline WsLayout ws_layout(int B, int k, int V)
     L.counters_b = align256(static_cast<size_t>(B) * 4);
     L.part = L.counters_b + align256(static_cast<size_t>(B) * 4);
     L.rec = L.part + align256(static_cast<size_t>(B) * (2 * k + 1) * C * sizeof(float2));
-    L.csum = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));
-    L.lsum = L.csum + align256(static_cast<size_t>(B) * NB * sizeof(float));
+    L.qsum = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));   // 4 quarter nodes per block
+    L.lsum = L.qsum + align256(static_cast<size_t>(B) * NB * 4 * sizeof(float));
     L.total = L.lsum + static_cast<size_t>(B) * NB * 4 * kThreads * sizeof(float);
     return L;
 }
@@ -496,7 +496,7 @@ __device__ __forceinline__ int warp_descend32(float v, float &t)
 __global__ void __launch_bounds__(kThreads, 4)
 sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
-                unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ csum,
+                unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ qsum,
                 float *__restrict__ lsum)
 {
     // launched as a programmatic dependent of the decision pass: wait for that
@@ -513,42 +513,39 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
     bool resid = R.resid != 0;
 
-    // one leaf (blk, 4 T + q) per thread: its weight sum goes to lsum
+    // one leaf per thread: leaf 256 q + T of block blk, so the CTA holds 256
+    // consecutive leaves and forms their node of the block's pairwise sum tree
+    // (lanes, then warps); its leaf sum goes to lsum, the node to qsum
     float *blk_lsum = lsum + (static_cast<size_t>(b) * NBK + blk) * (4 * kThreads);
+    const int leaf = kThreads * q + threadIdx.x, Tl = leaf >> 2, ql = leaf & 3;   // leaf = 4 Tl + ql
+    float ls;
     {
         float lp[kLeaf], lq[kLeaf], w[kLeaf];
-        load_pq(pv, qv, resid, V, blk, threadIdx.x, q, lp, lq);
-        blk_lsum[4 * threadIdx.x + q] = leaf_weights<false>(lp, lq, resid, V, blk, threadIdx.x, q, c, R, w);
+        load_pq(pv, qv, resid, V, blk, Tl, ql, lp, lq);
+        ls = leaf_weights<false>(lp, lq, resid, V, blk, Tl, ql, c, R, w);
+        blk_lsum[leaf] = ls;
     }
+    ls = warp_tree_sum(ls, 5);
+    if (lane == 0) warp_sum[warp] = ls;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned int prev = atomicAdd(&counters[b], 1u);
-        last = prev == static_cast<unsigned int>(4 * NBK - 1);
+    if (warp == 0) {
+        const float node = warp_tree_sum(lane < kThreads / 32 ? warp_sum[lane] : 0.0f, 3);
+        if (lane == 0) {
+            qsum[(static_cast<size_t>(b) * NBK + blk) * 4 + q] = node;
+            __threadfence();
+            const unsigned int prev = atomicAdd(&counters[b], 1u);
+            last = prev == static_cast<unsigned int>(4 * NBK - 1);
+        }
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
 
-    // block totals: the pairwise tree over each block's 1024 leaf sums in index
-    // order (32 consecutive leaves per lane, then the lanes), one warp per block
-    for (int bb = warp; bb < NBK; bb += kThreads / 32) {
-        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads)) + 8 * lane;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 x = __ldcg(src + i);
-            v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-        }
-#pragma unroll
-        for (int w = 1; w < 32; w <<= 1)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2 * w) v[i] = __fadd_rn(v[i], v[i + w]);
-        const float tot = warp_tree_sum(v[0], 5);
-        if (lane == 0) {
-            btree[bb] = tot;
-            csum[static_cast<size_t>(b) * NBK + bb] = tot;
-        }
+    // block totals: the top two levels of each block's tree over its four
+    // quarter nodes, (q0 + q1) + (q2 + q3)
+    for (int bb = threadIdx.x; bb < NBK; bb += kThreads) {
+        const float4 n4 = __ldcg(reinterpret_cast<const float4 *>(qsum + (static_cast<size_t>(b) * NBK + bb) * 4));
+        btree[bb] = __fadd_rn(__fadd_rn(n4.x, n4.y), __fadd_rn(n4.z, n4.w));
     }
     __syncthreads();
     // all-zero residual (rounding): draw from p_js instead (all threads rebuild the leaf sums)
@@ -729,7 +726,7 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     cfg.numAttrs = dependent ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
                            reinterpret_cast<unsigned int *>(w + L.counters_b), static_cast<const nq::SampleRec *>(rec),
-                           reinterpret_cast<float *>(w + L.csum), reinterpret_cast<float *>(w + L.lsum));
+                           reinterpret_cast<float *>(w + L.qsum), reinterpret_cast<float *>(w + L.lsum));
     return nq::cuda_status(e);
 }
 

@@ -56,14 +56,15 @@ def test_workspace_bytes(L):
     from quantized_self_speculative_gb300 import nq
     # sections, each starting on a 256-byte boundary: two ticket arrays, (2k+1)
     # partials per 4096-entry chunk per row, a 32-B decision record per row,
-    # one sum per 16384-entry block per row, 1024 leaf sums per block per row
+    # four quarter-block sums per 16384-entry block per row, 1024 leaf sums per
+    # block per row
     a = lambda n: (n + 255) // 256 * 256
 
     def expect(B, k, V):
         C, NB = -(-V // 4096), -(-V // 16384)
-        return a(4 * B) * 2 + a(B * (2 * k + 1) * C * 8) + a(32 * B) + a(4 * B * NB) + 4096 * B * NB
+        return a(4 * B) * 2 + a(B * (2 * k + 1) * C * 8) + a(32 * B) + a(16 * B * NB) + 4096 * B * NB
 
-    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 2957312
+    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 2964992
     assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 5376
     assert nq.workspace_bytes(3, 16, 4099) == expect(3, 16, 4099)
     for bad in [(0, 4, 10), (1, 0, 10), (1, 17, 10), (1, 4, 0), (1, 4, 524289), (65536, 1, 1)]:
