@@ -667,6 +667,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "arithmetic": "4-bit / 8-bit codes decoded to fp16, bf16 activations rounded to fp16, fp32 accumulation",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
         "config": {"workload": WORKLOAD, "layers": 32, "group": GROUP, "batch": 1, "k": K_DRAFT,
                    "draft_M": 1, "verify_M": K_DRAFT + 1, "vocab": V_LM,
