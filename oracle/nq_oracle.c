@@ -378,18 +378,17 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  * on the same fp32 values, computed by this fixed recipe:
  *
  *   c      = fp32(log2(e)) / T                       (IEEE division)
- *   leaf   = the vocabulary is cut into blocks of 16384 entries of 1024
- *            leaves; leaf 4T + q (T = 0..255, q = 0..3) of block b holds the
- *            16 entries b*16384 + 4096*q + 1024*r + 4*T + j (r, j = 0..3) in
- *            that (r, j) order -- thread T of a 256-thread block reads its four
- *            consecutive leaves with sixteen coalesced 16-byte loads -- and has
- *            global index 1024*b + 4T + q; entries >= V are absent, a leaf with
+ *   leaf   = 16 consecutive vocabulary entries in index order: leaf i holds
+ *            entries 16 i .. 16 i + 15; entries >= V are absent, a leaf with
  *            none is a pad; mx = max raw logit of the leaf
+ *   lsum   = the sum of 16 values w_0..w_15 of a leaf: four serial quarter
+ *            sums Q_q = ((w_4q + w_4q+1) + w_4q+2) + w_4q+3, then
+ *            (Q_0 + Q_1) + (Q_2 + Q_3); absent entries count as 0
  *   mz     = RN(mx * c);  t(x) = fma(l(x), c, -mz)    (base-2 exponent, <= ~0)
  *   e2(t)  = 0 if t < -125, else P(f) * 2^n with n = rint(t), f = t - n and
  *            P the degree-6 Taylor polynomial of 2^f (coefficients
  *            RN(ln2^i / i!)), evaluated by Horner with fma
- *   leaf s = serial fp32 sum, in leaf order, of e2(t(x))
+ *   leaf s = lsum of e2(t(x)) over the leaf
  *   merge  (m1,s1),(m2,s2): the larger m survives; s = fma(s_small,
  *            e2(m_small - m_large), s_large); a (-inf, 0) pad is the identity
  *   valid  = every logit finite and every leaf's mz finite (a logit whose
@@ -399,7 +398,7 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  *   p(x)   = RN(e2(t(x)) * F_leaf), F_leaf = RN(e2(mz_leaf - M) * RN(1/S))
  *   accept position j  <=>  u_j < RN(p_j(d_j) / q_j(d_j))
  *   residual r(x) = max(0, RN(p(x) - q(x))); sampling from a non-negative w:
- *            leaf sums serial, pairwise power-of-two tree (pads 0), root R,
+ *            leaf sums lsum, pairwise power-of-two tree (pads 0), root R,
  *            t = RN(u R), descend (left if t < L or the right sum is 0, else
  *            t -= L and go right), then scan the leaf for the first x whose
  *            running sum exceeds t (fallback: last x of the leaf with w > 0).
@@ -450,16 +449,21 @@ static ms_t ms_merge(ms_t a, ms_t b)
     return r;
 }
 
-#define ORC_BLOCK 16384
-
-/* Number of leaf slots (1024 per 16384-entry block) and the entry held at
- * position e (0..15) of leaf i; -1 if that entry lies at or beyond V. */
-static int n_leaves(int V) { return 1024 * ((V + ORC_BLOCK - 1) / ORC_BLOCK); }
+/* Number of 16-entry leaves and the entry held at position e (0..15) of
+ * leaf i; -1 if that entry lies at or beyond V. */
+static int n_leaves(int V) { return (V + ORC_LEAF - 1) / ORC_LEAF; }
 static int leaf_entry(int V, int i, int e)
 {
-    int blk = i / 1024, T = (i % 1024) / 4, q = i % 4;
-    int x = blk * ORC_BLOCK + 4096 * q + 1024 * (e / 4) + 4 * T + (e % 4);
+    int x = ORC_LEAF * i + e;
     return x < V ? x : -1;
+}
+
+/* lsum of R5: serial sums of the four quarters, then (Q0 + Q1) + (Q2 + Q3). */
+static float leaf_sum(const float w[ORC_LEAF])
+{
+    float Q[4];
+    for (int q = 0; q < 4; q++) Q[q] = ((w[4 * q] + w[4 * q + 1]) + w[4 * q + 2]) + w[4 * q + 3];
+    return (Q[0] + Q[1]) + (Q[2] + Q[3]);
 }
 static int pow2_at_least(int n) { int p = 1; while (p < n) p *= 2; return p; }
 
@@ -475,12 +479,12 @@ static int leaf_stats(const float *l, int V, float c, ms_t *leaf)
             if (x >= 0 && (!any || l[x] > mx)) { mx = l[x]; any = 1; }
         }
         if (!any) { leaf[i].m = -INFINITY; leaf[i].s = 0.0f; continue; }
-        float mz = mx * c, s = 0.0f;
+        float mz = mx * c, w[ORC_LEAF];
         for (int e = 0; e < ORC_LEAF; e++) {
             int x = leaf_entry(V, i, e);
-            if (x >= 0) s = s + orc_exp2c(fmaf(l[x], c, -mz));
+            w[e] = x >= 0 ? orc_exp2c(fmaf(l[x], c, -mz)) : 0.0f;
         }
-        leaf[i].m = mz; leaf[i].s = s;
+        leaf[i].m = mz; leaf[i].s = leaf_sum(w);
     }
     return L;
 }
@@ -535,12 +539,12 @@ int orc_tree_sample(const float *w, int V, float u)
     float **level = malloc(sizeof(float *) * (levels + 1));
     for (int l = 0; l <= levels; l++) level[l] = calloc((size_t)(P >> l), sizeof(float));
     for (int i = 0; i < L; i++) {
-        float s = 0.0f;
+        float wl[ORC_LEAF];
         for (int e = 0; e < ORC_LEAF; e++) {
             int x = leaf_entry(V, i, e);
-            if (x >= 0) s = s + w[x];
+            wl[e] = x >= 0 ? w[x] : 0.0f;
         }
-        level[0][i] = s;
+        level[0][i] = leaf_sum(wl);
     }
     for (int l = 1; l <= levels; l++)
         for (int i = 0; i < (P >> l); i++) level[l][i] = level[l - 1][2 * i] + level[l - 1][2 * i + 1];
@@ -617,8 +621,10 @@ int orc_accept_sample(const int32_t *draft, const float *draft_logits, const flo
 }
 
 /*
- * The same round in plain fp64 (libm exp, serial sums, inverse CDF), for
- * checking the canonical fp32 recipe against textbook arithmetic.  Also
+ * The same round in plain fp64 (libm exp, serial sums, the textbook inverse
+ * CDF over the vocabulary in index order), for checking the canonical fp32
+ * recipe against textbook arithmetic: the recipe's sum tree over index-order
+ * leaves, descended by u * R, is that inverse CDF up to rounding.  Also
  * reports per row the smallest distance between a uniform and the boundary
  * it was compared with (|u - ratio| and, for the drawn token, the distance
  * of u*R to the nearest cumulative boundary) so that callers can separate
@@ -632,27 +638,25 @@ static void softmax_f64(const float *l, int V, double T, double *p)
     for (int x = 0; x < V; x++) p[x] /= s;
 }
 
-/* Inverse CDF in fp64, walking the entries in the recipe's leaf order. */
+/* Textbook inverse CDF in fp64 over the vocabulary in index order: the first
+ * x whose cumulative weight exceeds u * total (the last x with positive
+ * weight if rounding leaves none).  *margin receives the distance of u * total
+ * to the nearer boundary of the chosen entry, relative to the total. */
 static int cdf_sample_f64(const double *w, int V, double u, double *margin)
 {
-    int L = n_leaves(V);
     double tot = 0.0;
     for (int x = 0; x < V; x++) tot += w[x];
     if (!(tot > 0.0)) return -1;
     double t = u * tot, run = 0.0;
     int pick = -1, last = -1;
-    for (int i = 0; i < L; i++) {
-        for (int e = 0; e < ORC_LEAF; e++) {
-            int x = leaf_entry(V, i, e);
-            if (x < 0) continue;
-            double prev = run;
-            run += w[x];
-            if (w[x] > 0.0) last = x;
-            if (w[x] > 0.0 && pick < 0 && t < run) {
-                pick = x;
-                double d0 = (t - prev) / tot, d1 = (run - t) / tot;
-                *margin = d0 < d1 ? d0 : d1;
-            }
+    for (int x = 0; x < V; x++) {
+        double prev = run;
+        run += w[x];
+        if (w[x] > 0.0) last = x;
+        if (w[x] > 0.0 && pick < 0 && t < run) {
+            pick = x;
+            double d0 = (t - prev) / tot, d1 = (run - t) / tot;
+            *margin = d0 < d1 ? d0 : d1;
         }
     }
     if (pick < 0) { pick = last; *margin = 0.0; }

@@ -149,13 +149,17 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 
 // ------------------------------------------------------------------ sampled
 //
-// Leaves of the recipe: the vocabulary is cut into blocks of 16384 entries of
-// 1024 leaves; leaf 4T + q (T = 0..255, q = 0..3) of block b holds the entries
-// b*16384 + 4096*q + 1024*r + 4*T + j (r, j = 0..3), in (r, j) order, and has
-// global index 1024*b + 4T + q.  Thread T of a 256-thread CTA owns the four
-// consecutive leaves 4T..4T+3 of a block and reads them with sixteen coalesced
-// 16-byte loads.  Absent entries (>= V) are read as -inf: they cannot raise a
-// maximum and contribute an exact zero to every sum.
+// Leaves of the recipe: 16 consecutive vocabulary entries in index order
+// (leaf i holds entries 16 i .. 16 i + 15); a block of 1024 leaves (16384
+// entries) is the unit of one pass-A CTA.  Four lanes share a leaf: lane
+// 4 g + qq of a warp holds entries 4 qq .. 4 qq + 3 of its group's leaf (one
+// 16-byte load, so a warp's load instruction reads eight 64-byte leaves in
+// full sectors).  The leaf's maximum and sum are formed across the four lanes
+// with xor shuffles: the maximum, and (Q0 + Q1) + (Q2 + Q3) of the serial
+// quarter sums Q -- the same bits on all four lanes, since fp32 max and
+// addition commute.  Absent entries (>= V) are read as -inf: they cannot
+// raise a maximum and contribute an exact zero to every sum; a leaf with no
+// present entry is a pad, (-inf, 0) or 0.
 
 struct SampleRec {      // per-row decision, written by pass A, read by pass B
     int js;             // first rejected position, or k if all accepted
@@ -189,47 +193,39 @@ inline WsLayout ws_layout(int B, int k, int V)
     return L;
 }
 
-__device__ __forceinline__ int leaf_entry(int blk, int T, int q, int e)
+// The four entries x .. x + 3 (x a multiple of 4) of one vector; `full` means
+// they are all present and 16-byte aligned.
+__device__ __forceinline__ float4 load_quarter(const float *vec, int V, bool full, int x)
 {
-    return blk * kBlock + 4096 * q + 1024 * (e >> 2) + 4 * T + (e & 3);
-}
-
-// Leaf (blk, 4T + q); `full` means the whole block lies inside [0, V).
-__device__ __forceinline__ void load_leaf(const float *vec, int V, bool full, int blk, int T, int q, float (&l)[kLeaf])
-{
-    const int base = leaf_entry(blk, T, q, 0);
-    if (full) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(vec + base + 1024 * r));
-            l[4 * r] = v.x; l[4 * r + 1] = v.y; l[4 * r + 2] = v.z; l[4 * r + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kLeaf; ++e) {
-            const int x = base + 1024 * (e >> 2) + (e & 3);
-            l[e] = x < V ? __ldcg(vec + x) : -INFINITY;
-        }
-    }
+    if (full) return __ldcg(reinterpret_cast<const float4 *>(vec + x));
+    if ((V & 3) == 0)
+        return x < V ? __ldcg(reinterpret_cast<const float4 *>(vec + x))
+                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    return make_float4(x < V ? __ldcg(vec + x) : -INFINITY, x + 1 < V ? __ldcg(vec + x + 1) : -INFINITY,
+                       x + 2 < V ? __ldcg(vec + x + 2) : -INFINITY, x + 3 < V ? __ldcg(vec + x + 3) : -INFINITY);
 }
 
 __device__ __forceinline__ bool block_full(int V, int blk) { return (V & 3) == 0 && (blk + 1) * kBlock <= V; }
 
-// (mz, s) of a leaf with at least one present entry.
-__device__ __forceinline__ MaxSum leaf_ms(const float (&l)[kLeaf], float c)
+// Leaf maximum and leaf sum across the four lanes sharing a leaf.
+__device__ __forceinline__ float leaf_max4(float m)
 {
-    float mx = l[0];
-#pragma unroll
-    for (int e = 1; e < kLeaf; ++e) mx = fmaxf(mx, l[e]);
-    const float mz = __fmul_rn(mx, c);
-    const unsigned long long c2 = f2_pack(c, c), nmz2 = f2_pack(-mz, -mz);
-    float s = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kLeaf; e += 2) {
-        const float2 x = exp2_canon_x2(f2_fma(f2_pack(l[e], l[e + 1]), c2, nmz2));
-        s = __fadd_rn(__fadd_rn(s, x.x), x.y);
-    }
-    return MaxSum{mz, s};
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+}
+__device__ __forceinline__ float leaf_sum4(float s)
+{
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));   // Q0 + Q1 | Q2 + Q3
+    return __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2)); // (Q0 + Q1) + (Q2 + Q3)
+}
+__device__ __forceinline__ float quad_max(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+
+// Canonical base-2 exponents t(x) = fma(l(x), c, -mz) of a quarter, exponentiated.
+__device__ __forceinline__ void quad_exp2(float4 v, float c, float mz, float2 &e01, float2 &e23)
+{
+    const unsigned long long c2 = f2_pack(c, c), nmz = f2_pack(-mz, -mz);
+    e01 = exp2_canon_x2(f2_fma(f2_pack(v.x, v.y), c2, nmz));
+    e23 = exp2_canon_x2(f2_fma(f2_pack(v.z, v.w), c2, nmz));
 }
 
 // Pairwise tree over 32 lanes (lane i holds node i of the level below).
@@ -256,7 +252,29 @@ __device__ __forceinline__ float leaf_factor(float mz_leaf, float M, float inv_s
     return __fmul_rn(exp2_canon(__fsub_rn(mz_leaf, M)), inv_s);
 }
 
+// p(x) of entry x of one vector (recipe: RN(e2(t(x)) F_leaf), with the
+// maximum of the 16-entry leaf that holds x).
+__device__ __forceinline__ float prob_at(const float *vec, int V, int x, float c, RowRoots root)
+{
+    const int leaf = x >> 4, r_x = (x & 15) >> 2, j_x = x & 3;
+    float mx = -INFINITY, lx = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float4 v = load_quarter(vec, V, false, kLeaf * leaf + 4 * r);
+        mx = fmaxf(mx, quad_max(v));
+        if (r == r_x) lx = j_x == 0 ? v.x : (j_x == 1 ? v.y : (j_x == 2 ? v.z : v.w));
+    }
+    const float mz = __fmul_rn(mx, c);
+    return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz)), leaf_factor(mz, root.M, root.inv_s));
+}
+
 // ---- pass A: one block of one vector; the last CTA of a row decides.
+// Warp w covers leaves 128 w .. 128 w + 127 of the block; lane group g (four
+// lanes) covers 16 of them, 16 g + n, in four batches b (n = 4 i + b,
+// i = 0..3, one load each).  After batch b, lane qq keeps leaf 4 qq + b, so
+// each lane ends with four consecutive leaves, 4 qq .. 4 qq + 3 of its group:
+// lane index = position of its 4-leaf node, and the warp tree over lanes is
+// the pairwise tree over the warp's 128 leaves.
 __global__ void __launch_bounds__(kThreads, 6)
 sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
@@ -271,34 +289,46 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     __shared__ bool last;
     const int NBK = gridDim.x, blk = blockIdx.x, v = blockIdx.y, b = blockIdx.z;
     const int NV = 2 * k + 1;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, T = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, qq = lane & 3;
     // vectors 0..k: target positions 0..k; k+1..2k: draft positions 0..k-1
     const float *vec = v <= k ? tlog + (static_cast<size_t>(b) * (k + 1) + v) * V
                               : dlog + (static_cast<size_t>(b) * k + (v - k - 1)) * V;
     {
         const bool full = block_full(V, blk);
-        float finite = 0.0f;   // becomes NaN if a present entry is not finite
-        MaxSum ms[4];
+        const int gleaf = blk * (kBlock / kLeaf) + 128 * warp + 16 * (lane >> 2);   // the group's first leaf
+        float finite = 0.0f;   // becomes NaN if a present entry or leaf maximum is not finite
+        MaxSum mine[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float l[kLeaf];
-            load_leaf(vec, V, full, blk, T, q, l);
-            if (full) {
+        for (int bt = 0; bt < 4; ++bt) {
+            float4 x4[4];
 #pragma unroll
-                for (int e = 0; e < kLeaf; ++e) finite = __fmaf_rn(0.0f, l[e], finite);
-                ms[q] = leaf_ms(l, c);
-            } else if (leaf_entry(blk, T, q, 0) < V) {
+            for (int i = 0; i < 4; ++i) x4[i] = load_quarter(vec, V, full, kLeaf * (gleaf + 4 * i + bt) + 4 * qq);
+            MaxSum keep{-INFINITY, 0.0f};
 #pragma unroll
-                for (int e = 0; e < kLeaf; ++e)
-                    if (leaf_entry(blk, T, q, e) < V) finite = __fmaf_rn(0.0f, l[e], finite);
-                ms[q] = leaf_ms(l, c);
-            } else {
-                ms[q] = MaxSum{-INFINITY, 0.0f};
+            for (int i = 0; i < 4; ++i) {
+                const int leaf = gleaf + 4 * i + bt, x = kLeaf * leaf + 4 * qq;
+                const bool present = full || kLeaf * leaf < V;
+                const float4 q = x4[i];
+                if (full) {
+                    finite = __fmaf_rn(0.0f, q.x, finite); finite = __fmaf_rn(0.0f, q.y, finite);
+                    finite = __fmaf_rn(0.0f, q.z, finite); finite = __fmaf_rn(0.0f, q.w, finite);
+                } else {
+                    if (x < V) finite = __fmaf_rn(0.0f, q.x, finite);
+                    if (x + 1 < V) finite = __fmaf_rn(0.0f, q.y, finite);
+                    if (x + 2 < V) finite = __fmaf_rn(0.0f, q.z, finite);
+                    if (x + 3 < V) finite = __fmaf_rn(0.0f, q.w, finite);
+                }
+                const float mz = __fmul_rn(leaf_max4(quad_max(q)), c);
+                float2 e01, e23;
+                quad_exp2(q, c, mz, e01, e23);
+                const float s = leaf_sum4(__fadd_rn(__fadd_rn(__fadd_rn(e01.x, e01.y), e23.x), e23.y));
+                if (present) finite = __fmaf_rn(0.0f, mz, finite);
+                if (i == qq) keep = present ? MaxSum{mz, s} : MaxSum{-INFINITY, 0.0f};
             }
-            finite = __fmaf_rn(0.0f, ms[q].m == -INFINITY ? 0.0f : ms[q].m, finite);
+            mine[bt] = keep;
         }
         if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
-        MaxSum a = ms_merge(ms_merge(ms[0], ms[1]), ms_merge(ms[2], ms[3]));
+        MaxSum a = ms_merge(ms_merge(mine[0], mine[1]), ms_merge(mine[2], mine[3]));
         a = warp_tree_ms(a, lane, 5);
         if (lane == 0) red[warp] = a;
         __syncthreads();
@@ -340,25 +370,8 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                 set_status(status, NQ_DEV_BAD_TOKEN);
                 reject = true;
             } else {
-                const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + j) * V;
-                const float *qv = dlog + (static_cast<size_t>(b) * k + j) * V;
-                const int bd = d / kBlock, o = d - bd * kBlock;
-                const int qd = o >> 12, o2 = o & 4095;
-                const int Td = (o2 & 1023) >> 2, ed = 4 * (o2 >> 10) + (o2 & 3);
-                const bool fd = block_full(V, bd);
-                float lp[kLeaf], lq[kLeaf];
-                load_leaf(pv, V, fd, bd, Td, qd, lp);
-                load_leaf(qv, V, fd, bd, Td, qd, lq);
-                float mp = lp[0], mq = lq[0];
-#pragma unroll
-                for (int e = 1; e < kLeaf; ++e) { mp = fmaxf(mp, lp[e]); mq = fmaxf(mq, lq[e]); }
-                const float mzp = __fmul_rn(mp, c), mzq = __fmul_rn(mq, c);
-                float ld_p = lp[0], ld_q = lq[0];
-#pragma unroll
-                for (int e = 1; e < kLeaf; ++e) if (e == ed) { ld_p = lp[e]; ld_q = lq[e]; }
-                const float p = __fmul_rn(exp2_canon(__fmaf_rn(ld_p, c, -mzp)), leaf_factor(mzp, roots[j].M, roots[j].inv_s));
-                const float q = __fmul_rn(exp2_canon(__fmaf_rn(ld_q, c, -mzq)),
-                                          leaf_factor(mzq, roots[k + 1 + j].M, roots[k + 1 + j].inv_s));
+                const float p = prob_at(tlog + (static_cast<size_t>(b) * (k + 1) + j) * V, V, d, c, roots[j]);
+                const float q = prob_at(dlog + (static_cast<size_t>(b) * k + j) * V, V, d, c, roots[k + 1 + j]);
                 const float ratio = __fdiv_rn(p, q);
                 const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
                 reject = !(u < ratio);
@@ -382,84 +395,60 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     }
 }
 
-// Sampling weights of leaf (blk, 4T + q) of row b's chosen position and their
-// serial sum: max(0, p - q) (resid) or p.  The logits are loaded separately
-// (load_pq) so that the next leaf's loads can overlap this leaf's arithmetic.
-__device__ __forceinline__ void load_pq(const float *pv, const float *qv, bool resid, int V, int blk, int T, int q,
-                                        float (&lp)[kLeaf], float (&lq)[kLeaf])
+// Sampling weights of one quarter of a leaf of row b's chosen position and
+// their serial sum: max(0, RN(p - q)) (resid) or p, with p = RN(e2(t_p) Fp).
+// Called by all four lanes of the leaf (the leaf maxima are shuffled).
+__device__ __forceinline__ float quarter_weights(float4 lp, float4 lq, bool resid, float c, const SampleRec &R,
+                                                 float (&w)[4])
 {
-    if (leaf_entry(blk, T, q, 0) >= V) return;
-    const bool full = block_full(V, blk);
-    load_leaf(pv, V, full, blk, T, q, lp);
-    if (resid) load_leaf(qv, V, full, blk, T, q, lq);
-}
-
-template <bool KEEP>
-__device__ __forceinline__ float leaf_weights(const float (&lp)[kLeaf], const float (&lq)[kLeaf], bool resid, int V,
-                                              int blk, int T, int q, float c, const SampleRec &R, float (&w)[kLeaf])
-{
-    if (leaf_entry(blk, T, q, 0) >= V) {
-        if (KEEP) {
-#pragma unroll
-            for (int e = 0; e < kLeaf; ++e) w[e] = 0.0f;
-        }
-        return 0.0f;
-    }
-    float mp = lp[0];
-#pragma unroll
-    for (int e = 1; e < kLeaf; ++e) mp = fmaxf(mp, lp[e]);
-    const float mzp = __fmul_rn(mp, c);
+    const float mzp = __fmul_rn(leaf_max4(quad_max(lp)), c);
     const float Fp = leaf_factor(mzp, R.Mp, R.invSp);
-    float s = 0.0f;
+    float2 p01, p23;
+    quad_exp2(lp, c, mzp, p01, p23);
+    w[0] = __fmul_rn(p01.x, Fp); w[1] = __fmul_rn(p01.y, Fp);
+    w[2] = __fmul_rn(p23.x, Fp); w[3] = __fmul_rn(p23.y, Fp);
     if (resid) {
-        float mq = lq[0];
-#pragma unroll
-        for (int e = 1; e < kLeaf; ++e) mq = fmaxf(mq, lq[e]);
-        const float mzq = __fmul_rn(mq, c);
+        const float mzq = __fmul_rn(leaf_max4(quad_max(lq)), c);
         const float Fq = leaf_factor(mzq, R.Mq, R.invSq);
-        const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp), nmzq = f2_pack(-mzq, -mzq);
-#pragma unroll
-        for (int e = 0; e < kLeaf; e += 2) {
-            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[e], lp[e + 1]), c2, nmzp));
-            const float2 eq = exp2_canon_x2(f2_fma(f2_pack(lq[e], lq[e + 1]), c2, nmzq));
-            const float d0 = __fsub_rn(__fmul_rn(ep.x, Fp), __fmul_rn(eq.x, Fq));
-            const float d1 = __fsub_rn(__fmul_rn(ep.y, Fp), __fmul_rn(eq.y, Fq));
-            const float w0 = d0 > 0.0f ? d0 : 0.0f, w1 = d1 > 0.0f ? d1 : 0.0f;
-            s = __fadd_rn(__fadd_rn(s, w0), w1);
-            if (KEEP) { w[e] = w0; w[e + 1] = w1; }
-        }
-    } else {
-        const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp);
-#pragma unroll
-        for (int e = 0; e < kLeaf; e += 2) {
-            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[e], lp[e + 1]), c2, nmzp));
-            const float w0 = __fmul_rn(ep.x, Fp), w1 = __fmul_rn(ep.y, Fp);
-            s = __fadd_rn(__fadd_rn(s, w0), w1);
-            if (KEEP) { w[e] = w0; w[e + 1] = w1; }
-        }
+        float2 q01, q23;
+        quad_exp2(lq, c, mzq, q01, q23);
+        const float d0 = __fsub_rn(w[0], __fmul_rn(q01.x, Fq)), d1 = __fsub_rn(w[1], __fmul_rn(q01.y, Fq));
+        const float d2 = __fsub_rn(w[2], __fmul_rn(q23.x, Fq)), d3 = __fsub_rn(w[3], __fmul_rn(q23.y, Fq));
+        w[0] = d0 > 0.0f ? d0 : 0.0f; w[1] = d1 > 0.0f ? d1 : 0.0f;
+        w[2] = d2 > 0.0f ? d2 : 0.0f; w[3] = d3 > 0.0f ? d3 : 0.0f;
     }
-    return s;
+    return __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), w[2]), w[3]);
 }
 
-// Sum over the 1024 leaves of block blk by the fixed pairwise tree (valid in
-// thread 0); optionally stores the 1024 leaf sums (index 4T + q) at lsum.
-__device__ float block_sum(float *warp_sum, float *lsum, const float *pv, const float *qv, bool resid, int V,
-                           int blk, float c, const SampleRec &R)
+// Leaf sums of the 256 consecutive leaves leaf0 .. leaf0 + 255 of row b's
+// chosen position (all threads of the CTA take part): they are stored at
+// out[0..255] and the node of the pairwise sum tree over them is returned
+// (valid in warp 0).  Warp w covers leaves 32 w .. 32 w + 31; its lane group
+// g the four leaves 4 g + i (one load per lane each), of which lane qq keeps
+// leaf 4 g + qq, so lane index = leaf index within the warp.
+__device__ float quarter_block(float *warp_sum, float *out, const float *pv, const float *qv, bool resid, int V,
+                               int leaf0, float c, const SampleRec &R)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, T = threadIdx.x;
-    float w[kLeaf];
-    float lp[2][kLeaf], lq[2][kLeaf];
-    float ls[4];
-    load_pq(pv, qv, resid, V, blk, T, 0, lp[0], lq[0]);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, qq = lane & 3;
+    const int gl = leaf0 + 32 * warp + 4 * (lane >> 2);
+    const bool full = (V & 3) == 0 && kLeaf * (leaf0 + kThreads) <= V;
+    float4 lp[4], lq[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (q + 1 < 4) load_pq(pv, qv, resid, V, blk, T, q + 1, lp[(q + 1) & 1], lq[(q + 1) & 1]);
-        ls[q] = leaf_weights<false>(lp[q & 1], lq[q & 1], resid, V, blk, T, q, c, R, w);
+    for (int i = 0; i < 4; ++i) {
+        lp[i] = load_quarter(pv, V, full, kLeaf * (gl + i) + 4 * qq);
+        lq[i] = resid ? load_quarter(qv, V, full, kLeaf * (gl + i) + 4 * qq) : lp[i];
     }
-    if (lsum) *reinterpret_cast<float4 *>(lsum + 4 * T) = make_float4(ls[0], ls[1], ls[2], ls[3]);
-    float s = __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3]));
-    s = warp_tree_sum(s, 5);
-    if (lane == 0) warp_sum[warp] = s;
+    float keep = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float w[4];
+        const float s = leaf_sum4(quarter_weights(lp[i], lq[i], resid, c, R, w));
+        const bool present = full || kLeaf * (gl + i) < V;
+        if (i == qq) keep = present ? s : 0.0f;
+    }
+    out[32 * warp + lane] = keep;
+    const float node = warp_tree_sum(keep, 5);
+    if (lane == 0) warp_sum[warp] = node;
     __syncthreads();
     float tot = 0.0f;
     if (warp == 0) tot = warp_tree_sum(lane < kThreads / 32 ? warp_sum[lane] : 0.0f, 3);
@@ -491,8 +480,9 @@ __device__ __forceinline__ int warp_descend32(float v, float &t)
     return base;
 }
 
-// ---- pass B: one block of the chosen position of one row; the last CTA of
-// the row descends the sum tree and writes the row's tokens.
+// ---- pass B: one quarter (256 leaves) of one block of the chosen position
+// of one row; the last CTA of the row descends the sum tree and writes the
+// row's tokens.
 __global__ void __launch_bounds__(kThreads, 4)
 sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
@@ -506,6 +496,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     __shared__ __align__(16) float btree[2 * kMaxBlocks];
     __shared__ bool last;
     __shared__ int pick;
+    constexpr int kBlockLeaves = kBlock / kLeaf;   // 1024
     const int NBK = gridDim.x >> 2, blk = blockIdx.x >> 2, q = blockIdx.x & 3, b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const SampleRec R = rec[b];
@@ -513,24 +504,12 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
     bool resid = R.resid != 0;
 
-    // one leaf per thread: leaf 256 q + T of block blk, so the CTA holds 256
-    // consecutive leaves and forms their node of the block's pairwise sum tree
-    // (lanes, then warps); its leaf sum goes to lsum, the node to qsum
-    float *blk_lsum = lsum + (static_cast<size_t>(b) * NBK + blk) * (4 * kThreads);
-    const int leaf = kThreads * q + threadIdx.x, Tl = leaf >> 2, ql = leaf & 3;   // leaf = 4 Tl + ql
-    float ls;
+    // this CTA's node of the block's pairwise sum tree (leaf sums go to lsum,
+    // the node to qsum)
     {
-        float lp[kLeaf], lq[kLeaf], w[kLeaf];
-        load_pq(pv, qv, resid, V, blk, Tl, ql, lp, lq);
-        ls = leaf_weights<false>(lp, lq, resid, V, blk, Tl, ql, c, R, w);
-        blk_lsum[leaf] = ls;
-    }
-    ls = warp_tree_sum(ls, 5);
-    if (lane == 0) warp_sum[warp] = ls;
-    __syncthreads();
-    if (warp == 0) {
-        const float node = warp_tree_sum(lane < kThreads / 32 ? warp_sum[lane] : 0.0f, 3);
-        if (lane == 0) {
+        const float node = quarter_block(warp_sum, lsum + (static_cast<size_t>(b) * NBK + blk) * kBlockLeaves + kThreads * q,
+                                         pv, qv, resid, V, blk * kBlockLeaves + kThreads * q, c, R);
+        if (threadIdx.x == 0) {
             qsum[(static_cast<size_t>(b) * NBK + blk) * 4 + q] = node;
             __threadfence();
             const unsigned int prev = atomicAdd(&counters[b], 1u);
@@ -557,9 +536,12 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         if (pick == 0) {
             resid = false;
             for (int bb = 0; bb < NBK; ++bb) {
-                const float sb = block_sum(warp_sum, lsum + (static_cast<size_t>(b) * NBK + bb) * (4 * kThreads), pv, qv,
-                                           false, V, bb, c, R);
-                if (threadIdx.x == 0) btree[bb] = sb;
+                float n4[4];
+                for (int qb = 0; qb < 4; ++qb)
+                    n4[qb] = quarter_block(warp_sum,
+                                           lsum + (static_cast<size_t>(b) * NBK + bb) * kBlockLeaves + kThreads * qb,
+                                           pv, qv, false, V, bb * kBlockLeaves + kThreads * qb, c, R);
+                if (threadIdx.x == 0) btree[bb] = __fadd_rn(__fadd_rn(n4[0], n4[1]), __fadd_rn(n4[2], n4[3]));
             }
         }
         __syncthreads();
@@ -573,7 +555,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const int bstar = warp_descend32(bval, t);
     float v[32];
     {
-        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * (4 * kThreads)) + 8 * lane;
+        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * kBlockLeaves) + 8 * lane;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float4 x = __ldcg(src + i);
@@ -594,13 +576,12 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         const float x = __shfl_sync(0xffffffffu, lsum32[i], lane_star);
         if (lane == i) mine = x;
     }
-    const int lstar = 32 * lane_star + warp_descend32(mine, t);
+    const int lstar = bstar * kBlockLeaves + 32 * lane_star + warp_descend32(mine, t);   // global leaf index
 
-    // the chosen leaf: 16 lanes reload one entry each, the weights are formed
-    // exactly as in the leaf sums, lane 0 scans them in entry order
-    const int Ts = lstar >> 2, qs = lstar & 3;
+    // the chosen leaf: lanes e and e + 16 reload entry e, the weights are
+    // formed exactly as in the leaf sums, lane 0 scans them in entry order
     const int e = lane & 15;
-    const int x = leaf_entry(bstar, Ts, qs, e);
+    const int x = kLeaf * lstar + e;
     const bool present = x < V;
     const float lp = present ? __ldcg(pv + x) : -INFINITY;
     const float lq = present && resid ? __ldcg(qv + x) : -INFINITY;
@@ -624,7 +605,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
 #pragma unroll
     for (int i = 0; i < kLeaf; ++i) {
         const float wi = __shfl_sync(0xffffffffu, we, i);
-        const int xi = leaf_entry(bstar, Ts, qs, i);
+        const int xi = kLeaf * lstar + i;
         if (xi < V && pk < 0) {
             run = __fadd_rn(run, wi);
             if (t < run) pk = xi;
@@ -634,7 +615,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
 #pragma unroll
     for (int i = kLeaf - 1; i >= 0; --i) {
         const float wi = __shfl_sync(0xffffffffu, we, i);
-        const int xi = leaf_entry(bstar, Ts, qs, i);
+        const int xi = kLeaf * lstar + i;
         if (pk < 0 && xi < V && wi > 0.0f) pk = xi;
     }
     if (lane == 0) {

@@ -36,7 +36,8 @@
 // fence (fence.proxy.async) before releasing it; every tcgen05.commit is
 // issued by the thread whose MMAs it must track.  Every wait on an mbarrier
 // is bounded by a timer; on a timeout the CTA sets NQ_DEV_TIMEOUT, drains its
-// copies and MMAs, frees its tensor memory and returns.
+// copies and MMAs, frees its tensor memory (kept if the MMA drain itself gave
+// up, since MMAs might still write it) and returns.
 #include "nq_internal.cuh"
 
 #include <cuda.h>           // CUtensorMap (types only; the encoder is fetched through the runtime)
@@ -153,6 +154,14 @@ __device__ __forceinline__ bool elect_one()
 {
     uint32_t e;
     asm volatile("{ .reg .b32 r; .reg .pred p; elect.sync r|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(e));
+    return e != 0;
+}
+// The same, also returning the elected lane's id (the same value on every lane).
+__device__ __forceinline__ bool elect_one(uint32_t &leader)
+{
+    uint32_t e, l;
+    asm volatile("{ .reg .pred p; elect.sync %1|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(e), "=r"(l));
+    leader = l;
     return e != 0;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -430,22 +439,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     auto B_EMPTY = [&](int i) { return bars + 8u * (16 + i); };
     auto D_FULL = [&](int i) { return bars + 8u * (24 + i); };
     auto D_EMPTY = [&](int i) { return bars + 8u * (26 + i); };
-    const uint32_t DONE = bars + 8u * 28;
-    const uint32_t DONE_ALL = bars + 8u * 53;   // 32 arrivals: the MMA warp's commits after an abort
+    // 32 arrivals: the MMA warp's final commits (lanes that issued MMAs) and
+    // plain arrivals (lanes that issued none)
+    const uint32_t DONE_ALL = bars + 8u * 53;
     auto W_FULL = [&](int i) { return bars + 8u * (29 + i); };
     auto W_EMPTY = [&](int i) { return bars + 8u * (41 + i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bars - sbase) + 8 * 56);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *keep_tmem = reinterpret_cast<volatile int *>(tmem_slot + 2);   // set if the MMA drain gave up
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < 4; ++i) { mbar_init(A_FULL(i), 8); mbar_init(A_EMPTY(i), 1); }
         for (int i = 0; i < 8; ++i) { mbar_init(B_FULL(i), 1); mbar_init(B_EMPTY(i), 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(D_FULL(i), 1); mbar_init(D_EMPTY(i), 4); }
-        mbar_init(DONE, 1);
         mbar_init(DONE_ALL, 32);
         for (int i = 0; i < 12; ++i) { mbar_init(W_FULL(i), 1); mbar_init(W_EMPTY(i), 8); }
         *abort_flag = 0;
+        *keep_tmem = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 20) {
@@ -635,7 +646,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         // loop and waits; one elected lane issues the MMAs and commits)
         const uint32_t idesc = f16_idesc(kTcTile, Npad);
         Ring a(SA), r(SB), d(ND);
-        bool ok = true, issued = false;
+        bool ok = true;
+        uint32_t issued_by = 0;   // lanes that have issued MMAs (the same mask on every lane)
         for (int tile = blockIdx.x; ok && tile < B.total_tiles; tile += gridDim.x, d.step()) {
             const int nkb = B.p[tile_problem(B, tile)].k / KB;
             const int db = d.slot;
@@ -652,7 +664,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                 const uint32_t b0 = sbase + static_cast<uint32_t>(sb) * stage_bytes;
                 // every commit comes from the thread that issued the MMAs it must
                 // track (a commit covers the issuing thread's own prior MMAs)
-                if (elect_one()) {
+                uint32_t leader;
+                if (elect_one(leader)) {
 #pragma unroll
                     for (int t = 0; t < KB / 16; ++t) {
                         const uint32_t a_tmem = tmem + static_cast<uint32_t>(kACols * sa + 8 * t);
@@ -661,35 +674,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                     }
                     tc_commit(A_EMPTY(sa));
                     tc_commit(B_EMPTY(sb));
-                    if (kb == nkb - 1) {
-                        tc_commit(D_FULL(db));
-                        // all MMAs of this CTA have completed before tensor memory is freed
-                        if (last_tile) tc_commit(DONE);
-                    }
+                    if (kb == nkb - 1) tc_commit(D_FULL(db));
                 }
                 __syncwarp();
-                issued = true;
+                issued_by |= 1u << leader;
             }
             if (!ok) break;
         }
-        if (issued) {
+        // every MMA of this CTA has completed before tensor memory is freed, on
+        // the normal path and after a wait gave up mid-tile alike: a lane that
+        // issued MMAs commits to DONE_ALL (the commit tracks that lane's own
+        // earlier MMAs), every other lane arrives on it without a commit, so no
+        // commit is ever issued by a thread with no MMA behind it
+        if (issued_by) {
+            if ((issued_by >> lane) & 1u) tc_commit(DONE_ALL);
+            else mbar_arrive(DONE_ALL);
+            __syncwarp();
             volatile int never = 0;
-            if (ok) {
-                mbar_wait(DONE, 0, &never, status);
-            } else {
-                // a wait gave up mid-tile: every lane commits (each commit covers that
-                // lane's own MMAs; the barrier completes after all 32), then wait
-                tc_commit(DONE_ALL);
-                __syncwarp();
-                mbar_wait(DONE_ALL, 0, &never, status);
-            }
+            const bool drained = mbar_wait(DONE_ALL, 0, &never, status);
+            // the drain itself gave up (sets NQ_DEV_TIMEOUT): MMAs may still
+            // write tensor memory, so it is not freed
+            if (!__all_sync(0xffffffffu, drained) && lane == 0) *keep_tmem = 1;
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 20) {
+    if (warp == 20 && *keep_tmem == 0) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }

@@ -99,23 +99,6 @@ def test_canonical_softmax_underflow_is_exact_zero():
     assert p[1] == 0 and p[3] == 0 and p[0] > 0 and p[2] > p[0]
 
 
-def sampling_order(V):
-    """The recipe's leaf order: blocks of 16384 entries; within a block, leaf
-    4T + q (T = 0..255, q = 0..3) holds entries 4096 q + 1024 r + 4 T + j for
-    r, j = 0..3 in that order."""
-    order = []
-    for b in range((V + 16383) // 16384):
-        for T in range(256):
-            for q in range(4):
-                for r in range(4):
-                    for j in range(4):
-                        x = 16384 * b + 4096 * q + 1024 * r + 4 * T + j
-                        if x < V:
-                            order.append(x)
-    assert sorted(order) == list(range(V))
-    return np.array(order)
-
-
 def test_tree_sample_is_inverse_cdf_away_from_boundaries():
     g = synth.rng(91)
     for V in (1, 7, 16, 33, 1000, 4096, 5000, 20000):
@@ -123,15 +106,14 @@ def test_tree_sample_is_inverse_cdf_away_from_boundaries():
         if w.sum() == 0:
             w[0] = 1
         us = g.random(150).astype(np.float32)
-        order = sampling_order(V)
-        cdf = np.cumsum(w[order].astype(np.float64))
+        cdf = np.cumsum(w.astype(np.float64))       # textbook inverse CDF, index order
         tot = cdf[-1]
         for u in us:
             got = O.tree_sample(w, float(u))
             t = float(u) * tot
             if np.min(np.abs(cdf - t)) < 1e-5 * tot:
                 continue
-            want = int(order[np.searchsorted(cdf, t, side="right")])
+            want = int(np.searchsorted(cdf, t, side="right"))
             assert got == want, (V, u)
             assert w[got] > 0
 
@@ -155,7 +137,7 @@ def test_tree_sample_zero_total_and_extreme_u():
     assert O.tree_sample(np.zeros(20, np.float32), 0.5) == -1
     w = np.zeros(40, np.float32)
     w[[3, 37]] = [1.0, 2.0]
-    # entry 3 sits in leaf 0, entry 37 in leaf 36 of block 0: index order here
+    # entry 3 sits in leaf 0, entry 37 in leaf 2: the first and the last positive weight
     assert O.tree_sample(w, 0.0) == 3
     assert O.tree_sample(w, float(np.float32(1 - 2**-24))) == 37
 
@@ -265,3 +247,22 @@ def test_invalid_inputs_rejected():
     tl[0, 2, 3] = np.nan
     with pytest.raises(ValueError):
         O.accept_sample(d, dl, tl, 1.0, seeds, 0)
+
+
+@pytest.mark.parametrize("k,noise", [(4, 1.05), (8, 0.132)])
+def test_canonical_round_agrees_with_fp64_round_sweep_shape(k, noise):
+    """Acceptance-sweep shape (V = 152064, target ~ N(0, 3), draft noise at the
+    two calibrated levels): the canonical recipe and the textbook fp64 round
+    (index-order inverse CDF) emit the same ids and counts on every row whose
+    decisions are not near-ties."""
+    B, V = 12, 152064
+    tl = synth.target_logits(430 + k, B, k, V, 3.0)
+    dl = synth.draft_logits_from(tl, 431 + k, noise)
+    d = synth.draft_tokens_sampled(dl, 432 + k)
+    seeds = synth.seeds_for(2, B)
+    for rnd in (0, 7):
+        out, cnt = O.accept_sample(d, dl, tl, 1.0, seeds, rnd)
+        out64, cnt64, margin = O.accept_sample_f64(d, dl, tl, 1.0, seeds, rnd)
+        differ = np.any(out != out64, axis=1) | (cnt != cnt64)
+        assert np.all(margin[differ] < 1e-5)
+        assert differ.sum() == 0
