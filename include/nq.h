@@ -236,7 +236,8 @@ NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_log
  * have no counterpart; this is a deployment variant.
  * Scratch: a fixed 1 MiB array inside the library, held on every GPU that
  * loads the library until the process exits.  Sizes needing more than that,
- * 256 + B*(k+1)*ceil(V/4096)*8 bytes > 1 MiB, return NQ_ERR_WORKSPACE.
+ * 256*ceil(4B/256) + B*(k+1)*ceil(V/16384)*8 bytes > 1 MiB, return
+ * NQ_ERR_WORKSPACE (e.g. B = 64, k = 8, V = 152064 needs 46,336 bytes).
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  Every
  * call clears the part of the array that must start at zero.  All calls share

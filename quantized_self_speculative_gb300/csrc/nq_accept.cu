@@ -756,7 +756,8 @@ extern "C" nq_status spec_accept_greedy_noalloc(const int32_t *draft, const floa
     if (!nq::aligned16(draft) || !nq::aligned16(tgt_logits) || !nq::aligned16(out_tok) || !nq::aligned16(out_cnt))
         return NQ_ERR_ALIGN;
     const size_t counters = nq::counters_bytes(B);
-    const size_t need = counters + static_cast<size_t>(B) * (k + 1) * nq::n_chunks(V) * sizeof(float2);
+    // one (value, index) partial per (row, position, greedy CTA of 16384 entries)
+    const size_t need = counters + static_cast<size_t>(B) * (k + 1) * nq::n_greedy_chunks(V) * sizeof(float2);
     if (need > nq::kNoAllocScratchBytes) return NQ_ERR_WORKSPACE;
     unsigned char *scratch = static_cast<unsigned char *>(nq::noalloc_scratch());
     unsigned int *status = nq::device_status_ptr();
