@@ -280,16 +280,61 @@ def eq2_report(t_draft_us, t_verify_us, t_accept_us, t_target_us, k=K_DRAFT):
     return out
 
 
+# ------------------------------------------------------------------ per-linear times (LLaMA-2-7B shapes)
+def per_linear_table(R, reps=3):
+    """Device time of one linear per launch, for each linear shape of the
+    round: the 32 layer copies of the shape (their weights exceed L2 together)
+    run back to back as single-linear calls inside a CUDA graph; time per
+    launch = graph time / 32.  Draft (M = 1, base plane) and verify (M = 5,
+    both planes).  The whole-pass figures come from one persistent launch over
+    all 225 linears, which hides the per-launch gaps these numbers include."""
+    import torch
+    nq = R.nq
+    groups = {"q/k/v/o 4096x4096": (".q", ".k", ".v", ".o"), "gate/up 4096->11008": (".gate", ".up"),
+              "down 11008->4096": (".down",), "lm_head 4096->32000": ("lm_head",)}
+    out = {}
+    for name, suffixes in groups.items():
+        idx = [i for i, (nm, _, _) in enumerate(R.shapes) if nm.endswith(suffixes)][:32]
+        n, k = R.shapes[idx[0]][1], R.shapes[idx[0]][2]
+        row = {"n_out": n, "k_in": k, "launches": len(idx)}
+        for kind, M in (("draft_M1", 1), ("verify_M5", 5)):
+            verify = kind.startswith("verify")
+            x = torch.randn((M, k), device=R.dev).to(torch.bfloat16)
+            y = torch.empty((M, n), dtype=torch.float32, device=R.dev)
+            fn = nq.verify_gemm if verify else nq.draft_gemv
+            for i in idx:                                   # warm-up outside capture
+                fn(R.layers[i], x, y)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in idx:
+                    fn(R.layers[i], x, y)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * len(idx))
+            byts = (verify_bytes if verify else draft_bytes)(n, k, M)
+            row[kind] = {"us": round(us, 2), "gbs": round(byts / (us * 1e-6) / 1e9, 1), "bytes": byts}
+        out[name] = row
+    return out
+
+
 # ------------------------------------------------------------------ acceptance at the sweep shape
-def accept_sweep(device, iters=20):
-    """Acceptance kernels alone at B = 64, V = 152064 (fp32 logits ~ N(0, 3))."""
+def accept_sweep(device, iters=20, ks=(2, 4, 6, 8)):
+    """Acceptance kernels alone at B = 64, V = 152064 (fp32 logits ~ N(0, 3),
+    draft = target + N(0, 0.3)), k in {2, 4, 6, 8}."""
     import torch
     from quantized_self_speculative_gb300 import nq
     out = {}
     B, V = 64, 152064
     gen = torch.Generator(device=device)
     gen.manual_seed(5)
-    for k in (4, 8):
+    for k in ks:
         tl = torch.randn((B, k + 1, V), generator=gen, device=device).mul_(3.0)
         dl = (tl[:, :k] + 0.3 * torch.randn((B, k, V), generator=gen, device=device)).contiguous()
         d = dl.argmax(-1).to(torch.int32)
@@ -692,8 +737,9 @@ def run_ours(args):
                                          R.time_target_only()),
     }
     if not args.no_extras:
+        line["per_linear_llama2_7b"] = per_linear_table(R)
         line["accept_sweep_B64_V152064"] = accept_sweep(device)
-    if args.extras == "full":
+    if args.extras == "full" and not args.no_extras:
         del R
         torch.cuda.empty_cache()
         line["config3_llama3_8b_b16_k8"] = config3_sweep(device)
@@ -713,8 +759,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--extras", choices=["quick", "full"], default="quick",
-                    help="full: also the LLaMA-3-8B (M=16/144), Qwen2.5-7B tier and acceptance-sweep passes")
+    ap.add_argument("--extras", choices=["quick", "full"], default="full",
+                    help="full (default): also the LLaMA-3-8B (M=16/144), Qwen2.5-7B tier and acceptance-sweep "
+                         "passes; quick: the LLaMA-2-7B round, per-linear times and acceptance timing only")
     ap.add_argument("--case", default=None,
                     help="profiling workload: draft|verify|draft16|verify144|int4|fp8|fp16|greedy|sample")
     ap.add_argument("--layers", type=int, default=8)

@@ -218,9 +218,13 @@ NQ_API nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_logit
  * seeds: uint64 [B] (device); round: caller's round counter.  Uniforms come
  * from Philox4x32-10 with key = seeds[b], counter = (j, purpose, round) --
  * purpose 0 accept test, 1 resample, 2 bonus -- so a (seed, round) pair
- * replays exactly.  The fp32 arithmetic follows a fixed recipe (own base-2
- * exponential, power-of-two max/sum trees over 16-entry leaves, sum-tree
- * sampling) so that every decision is reproducible bit for bit.
+ * replays exactly.  The fp32 arithmetic follows a fixed recipe so that every
+ * decision is reproducible bit for bit: an own base-2 exponential; exponents
+ * taken against the maximum of each 1024-entry segment of the vocabulary;
+ * sums of 16-entry leaves as two serial chains (even and odd entries); a
+ * pairwise tree over each segment's leaves and a pairwise (max, sum) tree
+ * over the segments; sampling by descending the pairwise sum tree over the
+ * leaves, all in vocabulary index order.
  */
 NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
                              int B, int k, int V, float temperature, const uint64_t *seeds,

@@ -74,6 +74,7 @@ def lib():
             L.orc_exp2c_n.argtypes = [vp, vp, i32]
             L.orc_softmax_canonical.argtypes = [vp, i32, f32, vp]
             L.orc_tree_sample.argtypes = [vp, i32, f32]
+            L.orc_softmax_stats.argtypes = [vp, i32, f32, vp, vp, vp, vp]
             L.orc_f32_to_f16_n.argtypes = [vp, vp, i32]
             L.orc_f16_to_f32_n.argtypes = [vp, vp, i32]
             L.orc_f32_to_e4m3_n.argtypes = [vp, vp, i32]
@@ -278,3 +279,17 @@ def softmax_canonical(logits, temperature: float = 1.0) -> np.ndarray:
 def tree_sample(w, u: float) -> int:
     w = np.ascontiguousarray(w, dtype=np.float32).ravel()
     return lib().orc_tree_sample(_p(w), w.size, float(u))
+
+
+def softmax_stats(logits, temperature: float = 1.0):
+    """Intermediate values of the canonical recipe for one logits vector:
+    per 1024-entry segment (mz, s) and the root (M, S) of the (max, sum) tree."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    V = l.shape[0]
+    ns = -(-V // 1024)
+    mz, s = np.empty(ns, np.float32), np.empty(ns, np.float32)
+    M, S = C.c_float(), C.c_float()
+    if lib().orc_softmax_stats(l.ctypes.data, V, float(temperature), mz.ctypes.data, s.ctypes.data,
+                               C.byref(M), C.byref(S)) < 0:
+        raise ValueError("non-finite logits")
+    return mz, s, np.float32(M.value), np.float32(S.value)

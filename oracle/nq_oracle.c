@@ -379,23 +379,25 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  *
  *   c      = fp32(log2(e)) / T                       (IEEE division)
  *   leaf   = 16 consecutive vocabulary entries in index order: leaf i holds
- *            entries 16 i .. 16 i + 15; entries >= V are absent, a leaf with
- *            none is a pad; mx = max raw logit of the leaf
- *   lsum   = the sum of 16 values w_0..w_15 of a leaf: four serial quarter
- *            sums Q_q = ((w_4q + w_4q+1) + w_4q+2) + w_4q+3, then
- *            (Q_0 + Q_1) + (Q_2 + Q_3); absent entries count as 0
- *   mz     = RN(mx * c);  t(x) = fma(l(x), c, -mz)    (base-2 exponent, <= ~0)
+ *            entries 16 i .. 16 i + 15; entries >= V are absent
+ *   lsum   = the sum of the 16 values w_0..w_15 of a leaf as two serial
+ *            chains, E = (..((w_0 + w_2) + w_4) ..) + w_14 and
+ *            O = (..((w_1 + w_3) + w_5) ..) + w_15, then E + O; absent
+ *            entries count as 0
+ *   segment = 1024 consecutive entries (64 leaves): segment s holds entries
+ *            1024 s .. 1024 s + 1023; mx = its maximum raw logit
+ *   mz     = RN(mx * c);  t(x) = fma(l(x), c, -mz of x's segment)  (<= ~0)
  *   e2(t)  = 0 if t < -125, else P(f) * 2^n with n = rint(t), f = t - n and
  *            P the degree-6 Taylor polynomial of 2^f (coefficients
  *            RN(ln2^i / i!)), evaluated by Horner with fma
- *   leaf s = lsum of e2(t(x)) over the leaf
+ *   segment s = pairwise sum tree over its 64 leaves' lsum of e2(t(x))
  *   merge  (m1,s1),(m2,s2): the larger m survives; s = fma(s_small,
  *            e2(m_small - m_large), s_large); a (-inf, 0) pad is the identity
- *   valid  = every logit finite and every leaf's mz finite (a logit whose
+ *   valid  = every logit finite and every segment's mz finite (a logit whose
  *            scaled value underflows gets probability 0)
- *   tree   = leaves padded to a power of two with (-inf, 0), merged pairwise,
- *            left operand first, level by level -> (M, S)
- *   p(x)   = RN(e2(t(x)) * F_leaf), F_leaf = RN(e2(mz_leaf - M) * RN(1/S))
+ *   tree   = segments padded to a power of two with (-inf, 0), merged
+ *            pairwise, left operand first, level by level -> (M, S)
+ *   p(x)   = RN(e2(t(x)) * F_seg), F_seg = RN(e2(mz_seg - M) * RN(1/S))
  *   accept position j  <=>  u_j < RN(p_j(d_j) / q_j(d_j))
  *   residual r(x) = max(0, RN(p(x) - q(x))); sampling from a non-negative w:
  *            leaf sums lsum, pairwise power-of-two tree (pads 0), root R,
@@ -458,38 +460,52 @@ static int leaf_entry(int V, int i, int e)
     return x < V ? x : -1;
 }
 
-/* lsum of R5: serial sums of the four quarters, then (Q0 + Q1) + (Q2 + Q3). */
+/* lsum of R5: two serial chains over the even and the odd entries, then E + O. */
 static float leaf_sum(const float w[ORC_LEAF])
 {
-    float Q[4];
-    for (int q = 0; q < 4; q++) Q[q] = ((w[4 * q] + w[4 * q + 1]) + w[4 * q + 2]) + w[4 * q + 3];
-    return (Q[0] + Q[1]) + (Q[2] + Q[3]);
+    float E = w[0], O = w[1];
+    for (int e = 2; e < ORC_LEAF; e += 2) { E = E + w[e]; O = O + w[e + 1]; }
+    return E + O;
 }
 static int pow2_at_least(int n) { int p = 1; while (p < n) p *= 2; return p; }
 
-/* Per-leaf (mz, s) for one logits vector; returns the number of leaf slots. */
-static int leaf_stats(const float *l, int V, float c, ms_t *leaf)
+/* Number of 1024-entry segments of a vector. */
+static int n_segments(int V) { return (V + ORC_SEG - 1) / ORC_SEG; }
+
+/* Plain pairwise sum of n (a power of two) values, left operand first. */
+static float pairwise_sum(float *v, int n)
 {
-    int L = n_leaves(V);
-    for (int i = 0; i < L; i++) {
-        float mx = -INFINITY;
-        int any = 0;
-        for (int e = 0; e < ORC_LEAF; e++) {
-            int x = leaf_entry(V, i, e);
-            if (x >= 0 && (!any || l[x] > mx)) { mx = l[x]; any = 1; }
-        }
-        if (!any) { leaf[i].m = -INFINITY; leaf[i].s = 0.0f; continue; }
-        float mz = mx * c, w[ORC_LEAF];
-        for (int e = 0; e < ORC_LEAF; e++) {
-            int x = leaf_entry(V, i, e);
-            w[e] = x >= 0 ? orc_exp2c(fmaf(l[x], c, -mz)) : 0.0f;
-        }
-        leaf[i].m = mz; leaf[i].s = leaf_sum(w);
-    }
-    return L;
+    for (int width = n; width > 1; width /= 2)
+        for (int i = 0; i < width / 2; i++) v[i] = v[2 * i] + v[2 * i + 1];
+    return v[0];
 }
 
-/* Root (M, S) of the power-of-two (max, sum) tree over the leaves. */
+/* Per-segment (mz, s) for one logits vector; returns the number of segments.
+ * Every segment holds at least one present entry. */
+static int seg_stats(const float *l, int V, float c, ms_t *seg)
+{
+    const int NS = n_segments(V), LPS = ORC_SEG / ORC_LEAF;
+    for (int sg = 0; sg < NS; sg++) {
+        float mx = -INFINITY;
+        int any = 0;
+        for (int x = ORC_SEG * sg; x < ORC_SEG * (sg + 1) && x < V; x++)
+            if (!any || l[x] > mx) { mx = l[x]; any = 1; }
+        float mz = mx * c, ls[ORC_SEG / ORC_LEAF];
+        for (int i = 0; i < LPS; i++) {
+            float w[ORC_LEAF];
+            for (int e = 0; e < ORC_LEAF; e++) {
+                int x = leaf_entry(V, LPS * sg + i, e);
+                w[e] = x >= 0 ? orc_exp2c(fmaf(l[x], c, -mz)) : 0.0f;
+            }
+            ls[i] = leaf_sum(w);
+        }
+        seg[sg].m = mz;
+        seg[sg].s = pairwise_sum(ls, LPS);
+    }
+    return NS;
+}
+
+/* Root (M, S) of the power-of-two (max, sum) tree over the segments. */
 static ms_t ms_tree(const ms_t *leaf, int L)
 {
     int P = pow2_at_least(L);
@@ -510,22 +526,36 @@ int orc_softmax_canonical(const float *l, int V, float T, float *p)
 {
     float c = orc_temper_coef(T);
     for (int x = 0; x < V; x++) if (!isfinite(l[x])) return -1;
-    ms_t *leaf = malloc(sizeof(ms_t) * n_leaves(V));
-    int L = leaf_stats(l, V, c, leaf);
-    for (int i = 0; i < L; i++)
-        if (leaf_entry(V, i, 0) >= 0 && !isfinite(leaf[i].m)) { free(leaf); return -1; }
-    ms_t root = ms_tree(leaf, L);
+    ms_t *seg = malloc(sizeof(ms_t) * n_segments(V));
+    int NS = seg_stats(l, V, c, seg);
+    for (int i = 0; i < NS; i++)
+        if (!isfinite(seg[i].m)) { free(seg); return -1; }
+    ms_t root = ms_tree(seg, NS);
     float inv_s = 1.0f / root.s;
-    for (int i = 0; i < L; i++) {
-        if (leaf_entry(V, i, 0) < 0) continue;
-        float F = orc_exp2c(leaf[i].m - root.m) * inv_s;
-        for (int e = 0; e < ORC_LEAF; e++) {
-            int x = leaf_entry(V, i, e);
-            if (x >= 0) p[x] = orc_exp2c(fmaf(l[x], c, -leaf[i].m)) * F;
-        }
+    for (int i = 0; i < NS; i++) {
+        float F = orc_exp2c(seg[i].m - root.m) * inv_s;
+        for (int x = ORC_SEG * i; x < ORC_SEG * (i + 1) && x < V; x++)
+            p[x] = orc_exp2c(fmaf(l[x], c, -seg[i].m)) * F;
     }
-    free(leaf);
+    free(seg);
     return 0;
+}
+
+/* The intermediate values of the recipe for one logits vector (for tests):
+ * per segment (mz, s), and the root (M, S).  Returns the number of segments,
+ * or -1 if the vector is not valid. */
+int orc_softmax_stats(const float *l, int V, float T, float *seg_mz, float *seg_s, float *M, float *S)
+{
+    float c = orc_temper_coef(T);
+    for (int x = 0; x < V; x++) if (!isfinite(l[x])) return -1;
+    ms_t *seg = malloc(sizeof(ms_t) * n_segments(V));
+    int NS = seg_stats(l, V, c, seg);
+    for (int i = 0; i < NS; i++) { seg_mz[i] = seg[i].m; seg_s[i] = seg[i].s; }
+    ms_t root = ms_tree(seg, NS);
+    *M = root.m;
+    *S = root.s;
+    free(seg);
+    return NS;
 }
 
 /* Draw an index from the non-negative weights w (not necessarily normalised)

@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #define ORC_LEAF 16
+#define ORC_SEG 1024
 
 enum { ORC_FMT_NESTED44 = 0, ORC_FMT_INT4 = 1, ORC_FMT_FP8 = 2, ORC_FMT_FP16 = 3 };
 
@@ -44,6 +45,7 @@ float orc_exp2_coef(int i);
 float orc_temper_coef(float T);
 int orc_softmax_canonical(const float *l, int V, float T, float *p);
 int orc_tree_sample(const float *w, int V, float u);
+int orc_softmax_stats(const float *l, int V, float T, float *seg_mz, float *seg_s, float *M, float *S);
 int orc_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
                       int B, int k, int V, float T, const uint64_t *seeds, uint64_t round,
                       int32_t *out_tok, int32_t *out_cnt);

@@ -29,7 +29,6 @@ constexpr int kChunk = kThreads * kLeaf;     // vocabulary entries per workspace
 constexpr int kGreedyChunk = 4 * kChunk;     // vocabulary entries per greedy CTA
 constexpr int kMaxChunks = 128;              // V <= 524288
 constexpr int kBlock = 4 * kChunk;           // vocabulary entries per sampling CTA (1024 leaves)
-constexpr int kMaxBlocks = kMaxChunks / 4;   // 32
 constexpr int kMaxK = 16;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -149,17 +148,39 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 
 // ------------------------------------------------------------------ sampled
 //
-// Leaves of the recipe: 16 consecutive vocabulary entries in index order
-// (leaf i holds entries 16 i .. 16 i + 15); a block of 1024 leaves (16384
-// entries) is the unit of one pass-A CTA.  Four lanes share a leaf: lane
-// 4 g + qq of a warp holds entries 4 qq .. 4 qq + 3 of its group's leaf (one
-// 16-byte load, so a warp's load instruction reads eight 64-byte leaves in
-// full sectors).  The leaf's maximum and sum are formed across the four lanes
-// with xor shuffles: the maximum, and (Q0 + Q1) + (Q2 + Q3) of the serial
-// quarter sums Q -- the same bits on all four lanes, since fp32 max and
-// addition commute.  Absent entries (>= V) are read as -inf: they cannot
-// raise a maximum and contribute an exact zero to every sum; a leaf with no
-// present entry is a pad, (-inf, 0) or 0.
+// Arithmetic of the recipe (spec_accept_sample in nq.h): segments of 1024
+// consecutive vocabulary entries carry the maximum every base-2 exponent is
+// taken against; a leaf of 16 consecutive entries is summed as two serial
+// chains, over its even and over its odd entries, E + O; a segment's sum is
+// the pairwise tree over its 64 leaves; segments merge pairwise as (max, sum)
+// nodes.
+//
+// Work unit: one warp, one segment at a time.  Lane l computes entries
+// 32 l .. 32 l + 31 (leaves 2 l and 2 l + 1).  The warp stages its segments in
+// its own slice of shared memory with cp.async: copy instruction t of lane l
+// reads the 16 bytes at entry 128 t + 4 l (512 contiguous bytes per
+// instruction) and stores them as chunk c = l % 8 of row r = 4 t + l / 8,
+// at position c ^ (r % 8) of that 128-byte row, so that the lane that owns
+// row r later reads its eight chunks with no bank conflict.  Loads in flight
+// cost no registers, and the warps are independent: each writes its own
+// partial and takes its own ticket, and the last warp of a row finishes the
+// row (no CTA-wide barrier).
+//
+// The chains of a leaf run on the packed fp32 adds, the even and the odd
+// chain in the two halves of one register pair; products that feed an add
+// are formed with scalar __fmul_rn, since a packed multiply followed by a
+// packed add may be fused into one fma by the code generator.  Absent
+// entries (>= V) are read as -inf: they cannot raise a maximum and contribute
+// an exact zero to every sum.
+
+constexpr int kSeg = 1024;                       // entries per segment
+constexpr int kSegPerBlock = kBlock / kSeg;      // 16 per pass-A CTA (two per warp)
+constexpr int kLeavesPerSeg = kSeg / kLeaf;      // 64
+constexpr int kWarpsS = kThreads / 32;           // 8 warps per sampling CTA
+constexpr int kSmemS = kWarpsS * 2 * kSeg * 4;   // 64 KB: two segment buffers per warp
+constexpr int kSampleCtas = 3;                   // resident CTAs per SM (shared memory bound)
+
+inline int n_segments_padded(int V) { return n_blocks(V) * kSegPerBlock; }
 
 struct SampleRec {      // per-row decision, written by pass A, read by pass B
     int js;             // first rejected position, or k if all accepted
@@ -171,61 +192,95 @@ struct SampleRec {      // per-row decision, written by pass A, read by pass B
 
 // Workspace layout shared by the greedy and sampled calls.
 struct WsLayout {
-    size_t counters_a, counters_b, part, rec, qsum, lsum, total;
+    size_t counters_a, counters_b, part, rec, segmax, ssum, lsum, vcount, roots, total;
 };
 
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Every section starts on a 256-byte boundary (the kernels use 16-byte
+// Every section starts on a 256-byte boundary (the kernels use 8- and 16-byte
 // vector accesses on some of them).
 inline WsLayout ws_layout(int B, int k, int V)
 {
-    const size_t C = static_cast<size_t>(n_chunks(V));   // greedy partials per vector (>= blocks)
-    const size_t NB = static_cast<size_t>(n_blocks(V));
+    const size_t C = static_cast<size_t>(n_chunks(V));   // greedy partials per vector
+    const size_t NSP = static_cast<size_t>(n_segments_padded(V));
+    const size_t NV = static_cast<size_t>(2 * k + 1);
     WsLayout L;
     L.counters_a = 0;
     L.counters_b = align256(static_cast<size_t>(B) * 4);
     L.part = L.counters_b + align256(static_cast<size_t>(B) * 4);
-    L.rec = L.part + align256(static_cast<size_t>(B) * (2 * k + 1) * C * sizeof(float2));
-    L.qsum = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));   // 4 quarter nodes per block
-    L.lsum = L.qsum + align256(static_cast<size_t>(B) * NB * 4 * sizeof(float));
-    L.total = L.lsum + static_cast<size_t>(B) * NB * 4 * kThreads * sizeof(float);
+    // greedy: one (value, index) per 4096-entry chunk; sampled: one (max, sum)
+    // per segment pair (warp of pass A), NSP / 2 of them
+    const size_t P = C > NSP / 2 ? C : NSP / 2;
+    L.rec = L.part + align256(static_cast<size_t>(B) * NV * P * sizeof(float2));
+    L.segmax = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));        // per (row, vector, segment)
+    L.ssum = L.segmax + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));
+    L.lsum = L.ssum + align256(static_cast<size_t>(B) * NSP * sizeof(float));         // per (row, segment)
+    L.vcount = L.lsum + align256(static_cast<size_t>(B) * NSP * kLeavesPerSeg * sizeof(float));
+    L.roots = L.vcount + align256(static_cast<size_t>(B) * NV * sizeof(unsigned int));  // per (row, vector)
+    L.total = L.roots + static_cast<size_t>(B) * NV * sizeof(float2);
     return L;
 }
 
-// The four entries x .. x + 3 (x a multiple of 4) of one vector; `full` means
-// they are all present and 16-byte aligned.
-__device__ __forceinline__ float4 load_quarter(const float *vec, int V, bool full, int x)
+// Stage the 1024 entries x0 .. x0 + 1023 of one vector in `buf` (4 KB of the
+// warp's shared memory) in the swizzled row layout; absent entries are zero.
+// al >= 1 (V % 4 == 0, 16-byte aligned vectors): cp.async, completed by the
+// caller's wait; al == 0: synchronous loads.
+__device__ __forceinline__ void stage_segment(float *buf, const float *vec, int V, int x0, int al)
 {
-    if (full) return __ldcg(reinterpret_cast<const float4 *>(vec + x));
-    if ((V & 3) == 0)
-        return x < V ? __ldcg(reinterpret_cast<const float4 *>(vec + x))
-                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    return make_float4(x < V ? __ldcg(vec + x) : -INFINITY, x + 1 < V ? __ldcg(vec + x + 1) : -INFINITY,
-                       x + 2 < V ? __ldcg(vec + x + 2) : -INFINITY, x + 3 < V ? __ldcg(vec + x + 3) : -INFINITY);
+    const int lane = threadIdx.x & 31;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const int x = x0 + 128 * t + 4 * lane;
+        const int r = 4 * t + (lane >> 3), cch = lane & 7;
+        const uint32_t dst = sbase + static_cast<uint32_t>(r * 128 + ((cch ^ (r & 7)) << 4));
+        if (al >= 1) {
+            const int bytes = x < V ? 16 : 0;
+            const float *src = x < V ? vec + x : vec;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(bytes) : "memory");
+        } else {
+            float4 q;
+            q.x = x < V ? __ldcg(vec + x) : 0.0f;
+            q.y = x + 1 < V ? __ldcg(vec + x + 1) : 0.0f;
+            q.z = x + 2 < V ? __ldcg(vec + x + 2) : 0.0f;
+            q.w = x + 3 < V ? __ldcg(vec + x + 3) : 0.0f;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(dst), "f"(q.x), "f"(q.y), "f"(q.z), "f"(q.w) : "memory");
+        }
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// This lane's 32 entries of a staged segment (np of them present; the rest -inf).
+__device__ __forceinline__ void read_lane(const float *buf, int np, float (&v)[32])
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t row = static_cast<uint32_t>(__cvta_generic_to_shared(buf)) + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+    for (int cch = 0; cch < 8; ++cch) {
+        float4 q;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w) : "r"(row + static_cast<uint32_t>((cch ^ (lane & 7)) << 4)));
+        v[4 * cch] = q.x; v[4 * cch + 1] = q.y; v[4 * cch + 2] = q.z; v[4 * cch + 3] = q.w;
+    }
+    if (np < 32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = i < np ? v[i] : -INFINITY;
+    }
 }
 
-__device__ __forceinline__ bool block_full(int V, int blk) { return (V & 3) == 0 && (blk + 1) * kBlock <= V; }
-
-// Leaf maximum and leaf sum across the four lanes sharing a leaf.
-__device__ __forceinline__ float leaf_max4(float m)
+__device__ __forceinline__ float max3(float a, float b, float c)
 {
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
-__device__ __forceinline__ float leaf_sum4(float s)
-{
-    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));   // Q0 + Q1 | Q2 + Q3
-    return __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2)); // (Q0 + Q1) + (Q2 + Q3)
-}
-__device__ __forceinline__ float quad_max(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
 
-// Canonical base-2 exponents t(x) = fma(l(x), c, -mz) of a quarter, exponentiated.
-__device__ __forceinline__ void quad_exp2(float4 v, float c, float mz, float2 &e01, float2 &e23)
+__device__ __forceinline__ float pair_sum(unsigned long long eo)
 {
-    const unsigned long long c2 = f2_pack(c, c), nmz = f2_pack(-mz, -mz);
-    e01 = exp2_canon_x2(f2_fma(f2_pack(v.x, v.y), c2, nmz));
-    e23 = exp2_canon_x2(f2_fma(f2_pack(v.z, v.w), c2, nmz));
+    const float2 v = f2_unpack(eo);
+    return __fadd_rn(v.x, v.y);
 }
 
 // Pairwise tree over 32 lanes (lane i holds node i of the level below).
@@ -245,215 +300,219 @@ __device__ __forceinline__ float warp_tree_sum(float a, int levels)
     return a;
 }
 
+__device__ __forceinline__ float warp_max(float m)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
+}
+
+// (mz, s) of one segment; every lane of the warp calls it with its 32 entries,
+// np of which are present.  `finite` becomes NaN if a present entry's
+// exponent t is not finite (a non-finite logit or segment maximum).
+__device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float c, float &finite)
+{
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) mx = max3(mx, v[i], v[i + 1]);
+    const float mz = __fmul_rn(warp_max(mx), c);
+    const unsigned long long c2 = f2_pack(c, c), nmz = f2_pack(-mz, -mz), z2 = f2_pack(0.0f, 0.0f);
+    unsigned long long fin = z2, eo[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const unsigned long long t = f2_fma(f2_pack(v[16 * h + 2 * p], v[16 * h + 2 * p + 1]), c2, nmz);
+            fin = f2_fma(z2, t, fin);
+            const float2 e = exp2_canon_x2(t);
+            eo[h] = p == 0 ? f2_pack(e.x, e.y) : f2_add(eo[h], f2_pack(e.x, e.y));
+        }
+    }
+    if (np == 32) {
+        const float2 f = f2_unpack(fin);
+        finite = __fadd_rn(finite, __fadd_rn(f.x, f.y));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < np) finite = __fmaf_rn(0.0f, __fmaf_rn(v[i], c, -mz), finite);
+    }
+    const float s = warp_tree_sum(__fadd_rn(pair_sum(eo[0]), pair_sum(eo[1])), 5);
+    return MaxSum{mz, s};
+}
+
 struct RowRoots { float M, inv_s; };
 
-__device__ __forceinline__ float leaf_factor(float mz_leaf, float M, float inv_s)
+__device__ __forceinline__ float seg_factor(float mz_seg, float M, float inv_s)
 {
-    return __fmul_rn(exp2_canon(__fsub_rn(mz_leaf, M)), inv_s);
+    return __fmul_rn(exp2_canon(__fsub_rn(mz_seg, M)), inv_s);
 }
 
-// p(x) of entry x of one vector (recipe: RN(e2(t(x)) F_leaf), with the
-// maximum of the 16-entry leaf that holds x).
-__device__ __forceinline__ float prob_at(const float *vec, int V, int x, float c, RowRoots root)
+// p(x) of entry x of one vector (recipe: RN(e2(t(x)) F_seg)).
+__device__ __forceinline__ float prob_at(const float *vec, const float *segm, int x, float c, RowRoots root)
 {
-    const int leaf = x >> 4, r_x = (x & 15) >> 2, j_x = x & 3;
-    float mx = -INFINITY, lx = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const float4 v = load_quarter(vec, V, false, kLeaf * leaf + 4 * r);
-        mx = fmaxf(mx, quad_max(v));
-        if (r == r_x) lx = j_x == 0 ? v.x : (j_x == 1 ? v.y : (j_x == 2 ? v.z : v.w));
-    }
-    const float mz = __fmul_rn(mx, c);
-    return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz)), leaf_factor(mz, root.M, root.inv_s));
+    const float mz = __ldcg(segm + (x >> 10));
+    const float lx = __ldcg(vec + x);
+    return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz)), seg_factor(mz, root.M, root.inv_s));
 }
 
-// ---- pass A: one block of one vector; the last CTA of a row decides.
-// Warp w covers leaves 128 w .. 128 w + 127 of the block; lane group g (four
-// lanes) covers 16 of them, 16 g + n, in four batches b (n = 4 i + b,
-// i = 0..3, one load each).  After batch b, lane qq keeps leaf 4 qq + b, so
-// each lane ends with four consecutive leaves, 4 qq .. 4 qq + 3 of its group:
-// lane index = position of its 4-leaf node, and the warp tree over lanes is
-// the pairwise tree over the warp's 128 leaves.
-__global__ void __launch_bounds__(kThreads, 6)
+// ---- pass A: warp w of CTA (blk, v, b) reduces segments 2 g and 2 g + 1
+// (g = 8 blk + w) of vector v of row b; the last warp of the row decides.
+__global__ void __launch_bounds__(kThreads, kSampleCtas)
 sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
-                int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
-                unsigned int *__restrict__ counters, float2 *__restrict__ part, SampleRec *__restrict__ rec,
+                int k, int V, float c, int al, const uint64_t *__restrict__ seeds, uint64_t round,
+                unsigned int *__restrict__ counters, unsigned int *__restrict__ vcount, float2 *__restrict__ part,
+                float *__restrict__ segmax, float2 *__restrict__ roots, SampleRec *__restrict__ rec,
                 unsigned int *status)
 {
     // the resample pass may be scheduled now; it waits (griddepcontrol.wait) for
     // this grid to complete before reading anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ MaxSum red[kThreads / 32];
-    __shared__ RowRoots roots[2 * kMaxK + 1];
-    __shared__ bool last;
+    extern __shared__ __align__(128) float smem_s[];
     const int NBK = gridDim.x, blk = blockIdx.x, v = blockIdx.y, b = blockIdx.z;
-    const int NV = 2 * k + 1;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, qq = lane & 3;
+    const int NV = 2 * k + 1, NSP = NBK * kSegPerBlock, NW = NBK * kWarpsS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blk * kWarpsS + warp;
+    float *buf = smem_s + warp * 2 * kSeg;
     // vectors 0..k: target positions 0..k; k+1..2k: draft positions 0..k-1
     const float *vec = v <= k ? tlog + (static_cast<size_t>(b) * (k + 1) + v) * V
                               : dlog + (static_cast<size_t>(b) * k + (v - k - 1)) * V;
+    float *segm = segmax + (static_cast<size_t>(b) * NV + v) * NSP;
+    bool last;
     {
-        const bool full = block_full(V, blk);
-        const int gleaf = blk * (kBlock / kLeaf) + 128 * warp + 16 * (lane >> 2);   // the group's first leaf
-        float finite = 0.0f;   // becomes NaN if a present entry or leaf maximum is not finite
-        MaxSum mine[4];
 #pragma unroll
-        for (int bt = 0; bt < 4; ++bt) {
-            float4 x4[4];
+        for (int i = 0; i < 2; ++i) {
+            if ((2 * g + i) * kSeg < V) stage_segment(buf + i * kSeg, vec, V, (2 * g + i) * kSeg, al);
+            cp_async_commit();
+        }
+        float finite = 0.0f;
+        MaxSum seg[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x4[i] = load_quarter(vec, V, full, kLeaf * (gleaf + 4 * i + bt) + 4 * qq);
-            MaxSum keep{-INFINITY, 0.0f};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int leaf = gleaf + 4 * i + bt, x = kLeaf * leaf + 4 * qq;
-                const bool present = full || kLeaf * leaf < V;
-                const float4 q = x4[i];
-                if (full) {
-                    finite = __fmaf_rn(0.0f, q.x, finite); finite = __fmaf_rn(0.0f, q.y, finite);
-                    finite = __fmaf_rn(0.0f, q.z, finite); finite = __fmaf_rn(0.0f, q.w, finite);
-                } else {
-                    if (x < V) finite = __fmaf_rn(0.0f, q.x, finite);
-                    if (x + 1 < V) finite = __fmaf_rn(0.0f, q.y, finite);
-                    if (x + 2 < V) finite = __fmaf_rn(0.0f, q.z, finite);
-                    if (x + 3 < V) finite = __fmaf_rn(0.0f, q.w, finite);
-                }
-                const float mz = __fmul_rn(leaf_max4(quad_max(q)), c);
-                float2 e01, e23;
-                quad_exp2(q, c, mz, e01, e23);
-                const float s = leaf_sum4(__fadd_rn(__fadd_rn(__fadd_rn(e01.x, e01.y), e23.x), e23.y));
-                if (present) finite = __fmaf_rn(0.0f, mz, finite);
-                if (i == qq) keep = present ? MaxSum{mz, s} : MaxSum{-INFINITY, 0.0f};
+        for (int i = 0; i < 2; ++i) {
+            if (i == 0) cp_async_wait<1>(); else cp_async_wait<0>();
+            __syncwarp();
+            const int sg = 2 * g + i;
+            seg[i] = MaxSum{-INFINITY, 0.0f};
+            if (sg * kSeg < V) {                          // warp-uniform
+                const int np = min(max(V - (sg * kSeg + 32 * lane), 0), 32);
+                float l[32];
+                read_lane(buf + i * kSeg, np, l);
+                seg[i] = segment_ms(l, np, c, finite);
+                if (lane == 0) segm[sg] = seg[i].m;
             }
-            mine[bt] = keep;
         }
         if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
-        MaxSum a = ms_merge(ms_merge(mine[0], mine[1]), ms_merge(mine[2], mine[3]));
-        a = warp_tree_ms(a, lane, 5);
-        if (lane == 0) red[warp] = a;
-        __syncthreads();
-        if (warp == 0) {
-            MaxSum w8 = lane < kThreads / 32 ? red[lane] : MaxSum{-INFINITY, 0.0f};
-            w8 = warp_tree_ms(w8, lane, 3);
-            if (lane == 0) {
-                part[(static_cast<size_t>(b) * NV + v) * NBK + blk] = make_float2(w8.m, w8.s);
-                __threadfence();
-                const unsigned int prev = atomicAdd(&counters[b], 1u);
-                last = prev == static_cast<unsigned int>(NV * NBK - 1);
+        const MaxSum a = ms_merge(seg[0], seg[1]);
+        unsigned int prev = 0;
+        if (lane == 0) {
+            part[(static_cast<size_t>(b) * NV + v) * NW + g] = make_float2(a.m, a.s);
+            __threadfence();
+            prev = atomicAdd(&vcount[static_cast<size_t>(b) * NV + v], 1u);
+        }
+        last = __shfl_sync(0xffffffffu, prev, 0) == static_cast<unsigned int>(NW - 1);
+    }
+    if (!last) return;
+    __threadfence();
+
+    // ---- last warp of vector v: its root (M, 1/S); lane l holds the partials
+    // 8 l .. 8 l + 7 (pairwise in the lane, then across lanes).  The vectors'
+    // last warps run in parallel; the last of them takes the row's decisions.
+    {
+        MaxSum n[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int gi = 8 * lane + i;
+            n[i] = MaxSum{-INFINITY, 0.0f};
+            if (gi < NW) {
+                const float2 p = __ldcg(part + (static_cast<size_t>(b) * NV + v) * NW + gi);
+                n[i] = MaxSum{p.x, p.y};
             }
         }
-        __syncthreads();
-        if (!last) return;
+        MaxSum a = ms_merge(ms_merge(ms_merge(n[0], n[1]), ms_merge(n[2], n[3])),
+                            ms_merge(ms_merge(n[4], n[5]), ms_merge(n[6], n[7])));
+        a = warp_tree_ms(a, lane, 5);
+        unsigned int prev = 0;
+        if (lane == 0) {
+            roots[static_cast<size_t>(b) * NV + v] = make_float2(a.m, __frcp_rn(a.s));
+            vcount[static_cast<size_t>(b) * NV + v] = 0;   // ready for the next call
+            __threadfence();
+            prev = atomicAdd(&counters[b], 1u);
+        }
+        if (__shfl_sync(0xffffffffu, prev, 0) != static_cast<unsigned int>(NV - 1)) return;
         __threadfence();
     }
 
-    // ---- last CTA of row b: roots (M, 1/S) of the 2k+1 vectors (lane = block)
-    for (int vv = warp; vv < NV; vv += kThreads / 32) {
-        MaxSum a{-INFINITY, 0.0f};
-        if (lane < NBK) {
-            const float2 p = __ldcg(part + (static_cast<size_t>(b) * NV + vv) * NBK + lane);
-            a = MaxSum{p.x, p.y};
+    // ---- last warp of row b.  Decisions: accept d_j iff u_j < p_j(d_j) /
+    // q_j(d_j); first rejection j*
+    const float2 *rrow = roots + static_cast<size_t>(b) * NV;
+    auto root_of = [&](int vv) { const float2 r = __ldcg(rrow + vv); return RowRoots{r.x, r.y}; };
+    const uint64_t seed = seeds[b];
+    const float *segrow = segmax + static_cast<size_t>(b) * NV * NSP;
+    bool reject = false;
+    if (lane < k) {
+        const int j = lane;
+        const int d = draft[static_cast<size_t>(b) * k + j];
+        if (d < 0 || d >= V) {
+            set_status(status, NQ_DEV_BAD_TOKEN);
+            reject = true;
+        } else {
+            const float p = prob_at(tlog + (static_cast<size_t>(b) * (k + 1) + j) * V,
+                                    segrow + static_cast<size_t>(j) * NSP, d, c, root_of(j));
+            const float q = prob_at(dlog + (static_cast<size_t>(b) * k + j) * V,
+                                    segrow + static_cast<size_t>(k + 1 + j) * NSP, d, c, root_of(k + 1 + j));
+            const float ratio = __fdiv_rn(p, q);
+            const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
+            reject = !(u < ratio);
         }
-        a = warp_tree_ms(a, lane, 5);
-        if (lane == 0) roots[vv] = RowRoots{a.m, __frcp_rn(a.s)};
     }
-    __syncthreads();
+    const unsigned int rej = __ballot_sync(0xffffffffu, reject);
+    if (lane == 0) {
+        const int js = rej ? __ffs(rej) - 1 : k;
+        const RowRoots rp = root_of(js);
+        SampleRec r;
+        r.js = js;
+        r.resid = js < k;
+        r.u = philox_uniform(seed, static_cast<uint32_t>(js), js < k ? 1u : 2u, round);
+        r.Mp = rp.M;
+        r.invSp = rp.inv_s;
+        if (js < k) {
+            const RowRoots rq = root_of(k + 1 + js);
+            r.Mq = rq.M;
+            r.invSq = rq.inv_s;
+        } else {
+            r.Mq = 0.0f;
+            r.invSq = 0.0f;
+        }
+        r.pad = 0;
+        rec[b] = r;
+        counters[b] = 0;   // ready for the next call
+    }
+}
 
-    // ---- decisions: accept d_j iff u_j < p_j(d_j) / q_j(d_j); first rejection j*
-    if (warp == 0) {
-        const uint64_t seed = seeds[b];
-        bool reject = false;
-        if (lane < k) {
-            const int j = lane;
-            const int d = draft[static_cast<size_t>(b) * k + j];
-            if (d < 0 || d >= V) {
-                set_status(status, NQ_DEV_BAD_TOKEN);
-                reject = true;
-            } else {
-                const float p = prob_at(tlog + (static_cast<size_t>(b) * (k + 1) + j) * V, V, d, c, roots[j]);
-                const float q = prob_at(dlog + (static_cast<size_t>(b) * k + j) * V, V, d, c, roots[k + 1 + j]);
-                const float ratio = __fdiv_rn(p, q);
-                const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
-                reject = !(u < ratio);
+// Sampling weights of a lane's 32 entries of row b's chosen position,
+// max(0, RN(p - q)) (resid) or p, with p = RN(e2(t_p) Fp); returns the two
+// leaf sums (entries 0..15 and 16..31).
+__device__ __forceinline__ float2 lane_leaf_sums(const float (&lp)[32], const float (&lq)[32], bool resid,
+                                                 float c, float mzp, float Fp, float mzq, float Fq)
+{
+    const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp), nmzq = f2_pack(-mzq, -mzq);
+    unsigned long long eo[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int i = 16 * h + 2 * p;
+            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[i], lp[i + 1]), c2, nmzp));
+            float w0 = __fmul_rn(ep.x, Fp), w1 = __fmul_rn(ep.y, Fp);
+            if (resid) {
+                const float2 eq = exp2_canon_x2(f2_fma(f2_pack(lq[i], lq[i + 1]), c2, nmzq));
+                const float d0 = __fsub_rn(w0, __fmul_rn(eq.x, Fq)), d1 = __fsub_rn(w1, __fmul_rn(eq.y, Fq));
+                w0 = d0 > 0.0f ? d0 : 0.0f;
+                w1 = d1 > 0.0f ? d1 : 0.0f;
             }
-        }
-        const unsigned int rej = __ballot_sync(0xffffffffu, reject);
-        if (lane == 0) {
-            const int js = rej ? __ffs(rej) - 1 : k;
-            SampleRec r;
-            r.js = js;
-            r.resid = js < k;
-            r.u = philox_uniform(seed, static_cast<uint32_t>(js), js < k ? 1u : 2u, round);
-            r.Mp = roots[js].M;
-            r.invSp = roots[js].inv_s;
-            r.Mq = js < k ? roots[k + 1 + js].M : 0.0f;
-            r.invSq = js < k ? roots[k + 1 + js].inv_s : 0.0f;
-            r.pad = 0;
-            rec[b] = r;
-            counters[b] = 0;   // ready for the next call
+            eo[h] = p == 0 ? f2_pack(w0, w1) : f2_add(eo[h], f2_pack(w0, w1));
         }
     }
-}
-
-// Sampling weights of one quarter of a leaf of row b's chosen position and
-// their serial sum: max(0, RN(p - q)) (resid) or p, with p = RN(e2(t_p) Fp).
-// Called by all four lanes of the leaf (the leaf maxima are shuffled).
-__device__ __forceinline__ float quarter_weights(float4 lp, float4 lq, bool resid, float c, const SampleRec &R,
-                                                 float (&w)[4])
-{
-    const float mzp = __fmul_rn(leaf_max4(quad_max(lp)), c);
-    const float Fp = leaf_factor(mzp, R.Mp, R.invSp);
-    float2 p01, p23;
-    quad_exp2(lp, c, mzp, p01, p23);
-    w[0] = __fmul_rn(p01.x, Fp); w[1] = __fmul_rn(p01.y, Fp);
-    w[2] = __fmul_rn(p23.x, Fp); w[3] = __fmul_rn(p23.y, Fp);
-    if (resid) {
-        const float mzq = __fmul_rn(leaf_max4(quad_max(lq)), c);
-        const float Fq = leaf_factor(mzq, R.Mq, R.invSq);
-        float2 q01, q23;
-        quad_exp2(lq, c, mzq, q01, q23);
-        const float d0 = __fsub_rn(w[0], __fmul_rn(q01.x, Fq)), d1 = __fsub_rn(w[1], __fmul_rn(q01.y, Fq));
-        const float d2 = __fsub_rn(w[2], __fmul_rn(q23.x, Fq)), d3 = __fsub_rn(w[3], __fmul_rn(q23.y, Fq));
-        w[0] = d0 > 0.0f ? d0 : 0.0f; w[1] = d1 > 0.0f ? d1 : 0.0f;
-        w[2] = d2 > 0.0f ? d2 : 0.0f; w[3] = d3 > 0.0f ? d3 : 0.0f;
-    }
-    return __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), w[2]), w[3]);
-}
-
-// Leaf sums of the 256 consecutive leaves leaf0 .. leaf0 + 255 of row b's
-// chosen position (all threads of the CTA take part): they are stored at
-// out[0..255] and the node of the pairwise sum tree over them is returned
-// (valid in warp 0).  Warp w covers leaves 32 w .. 32 w + 31; its lane group
-// g the four leaves 4 g + i (one load per lane each), of which lane qq keeps
-// leaf 4 g + qq, so lane index = leaf index within the warp.
-__device__ float quarter_block(float *warp_sum, float *out, const float *pv, const float *qv, bool resid, int V,
-                               int leaf0, float c, const SampleRec &R)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, qq = lane & 3;
-    const int gl = leaf0 + 32 * warp + 4 * (lane >> 2);
-    const bool full = (V & 3) == 0 && kLeaf * (leaf0 + kThreads) <= V;
-    float4 lp[4], lq[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        lp[i] = load_quarter(pv, V, full, kLeaf * (gl + i) + 4 * qq);
-        lq[i] = resid ? load_quarter(qv, V, full, kLeaf * (gl + i) + 4 * qq) : lp[i];
-    }
-    float keep = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float w[4];
-        const float s = leaf_sum4(quarter_weights(lp[i], lq[i], resid, c, R, w));
-        const bool present = full || kLeaf * (gl + i) < V;
-        if (i == qq) keep = present ? s : 0.0f;
-    }
-    out[32 * warp + lane] = keep;
-    const float node = warp_tree_sum(keep, 5);
-    if (lane == 0) warp_sum[warp] = node;
-    __syncthreads();
-    float tot = 0.0f;
-    if (warp == 0) tot = warp_tree_sum(lane < kThreads / 32 ? warp_sum[lane] : 0.0f, 3);
-    __syncthreads();
-    return tot;
+    return make_float2(pair_sum(eo[0]), pair_sum(eo[1]));
 }
 
 // Descend the pairwise sum tree over 32 leaves held one per lane (index =
@@ -480,122 +539,145 @@ __device__ __forceinline__ int warp_descend32(float v, float &t)
     return base;
 }
 
-// ---- pass B: one quarter (256 leaves) of one block of the chosen position
-// of one row; the last CTA of the row descends the sum tree and writes the
-// row's tokens.
-__global__ void __launch_bounds__(kThreads, 4)
+// Leaf sums of segment sg of row b's chosen position from its staged entries
+// (pbuf, and qbuf for the residual), stored at lrow[64 sg + ...]; returns the
+// segment's sum (every lane).
+__device__ __forceinline__ float segment_leaf_sums(const float *pbuf, const float *qbuf, bool resid, int V, int sg,
+                                                   float c, const SampleRec &R, const float *smp, const float *smq,
+                                                   float *lrow)
+{
+    const int lane = threadIdx.x & 31;
+    const int np = min(max(V - (sg * kSeg + 32 * lane), 0), 32);
+    const float mzp = __ldcg(smp + sg);
+    const float Fp = seg_factor(mzp, R.Mp, R.invSp);
+    float lp[32], lq[32];
+    read_lane(pbuf, np, lp);
+    float2 ls;
+    if (resid) {
+        const float mzq = __ldcg(smq + sg);
+        const float Fq = seg_factor(mzq, R.Mq, R.invSq);
+        read_lane(qbuf, np, lq);
+        ls = lane_leaf_sums(lp, lq, true, c, mzp, Fp, mzq, Fq);
+    } else {
+        ls = lane_leaf_sums(lp, lp, false, c, mzp, Fp, 0.0f, 0.0f);
+    }
+    *reinterpret_cast<float2 *>(lrow + kLeavesPerSeg * sg + 2 * lane) = ls;
+    return warp_tree_sum(__fadd_rn(ls.x, ls.y), 5);
+}
+
+// ---- pass B: warp w of CTA (x, b) forms the leaf sums of segment 8 x + w of
+// row b's chosen position; the last warp of the row descends the sum tree
+// and writes the row's tokens.
+__global__ void __launch_bounds__(kThreads, kSampleCtas)
 sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
-                int k, int V, float c, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
-                unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec, float *__restrict__ qsum,
-                float *__restrict__ lsum)
+                int k, int V, float c, int al, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
+                unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec,
+                const float *__restrict__ segmax, float *__restrict__ ssum, float *__restrict__ lsum)
 {
     // launched as a programmatic dependent of the decision pass: wait for that
     // grid to complete (its records and partials visible) before anything else
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    __shared__ float warp_sum[kThreads / 32];
-    __shared__ __align__(16) float btree[2 * kMaxBlocks];
-    __shared__ bool last;
-    __shared__ int pick;
-    constexpr int kBlockLeaves = kBlock / kLeaf;   // 1024
-    const int NBK = gridDim.x >> 2, blk = blockIdx.x >> 2, q = blockIdx.x & 3, b = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(128) float smem_s[];
+    const int NSP = gridDim.x * kWarpsS, NV = 2 * k + 1, NBK = NSP / kSegPerBlock, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sg = blockIdx.x * kWarpsS + warp;
+    float *pbuf = smem_s + warp * 2 * kSeg, *qbuf = pbuf + kSeg;
     const SampleRec R = rec[b];
     const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + R.js) * V;
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
+    const float *smp = segmax + (static_cast<size_t>(b) * NV + R.js) * NSP;
+    const float *smq = segmax + (static_cast<size_t>(b) * NV + (R.js < k ? k + 1 + R.js : R.js)) * NSP;
+    float *lrow = lsum + static_cast<size_t>(b) * NSP * kLeavesPerSeg;
+    float *srow = ssum + static_cast<size_t>(b) * NSP;
     bool resid = R.resid != 0;
 
-    // this CTA's node of the block's pairwise sum tree (leaf sums go to lsum,
-    // the node to qsum)
+    bool last;
     {
-        const float node = quarter_block(warp_sum, lsum + (static_cast<size_t>(b) * NBK + blk) * kBlockLeaves + kThreads * q,
-                                         pv, qv, resid, V, blk * kBlockLeaves + kThreads * q, c, R);
-        if (threadIdx.x == 0) {
-            qsum[(static_cast<size_t>(b) * NBK + blk) * 4 + q] = node;
-            __threadfence();
-            const unsigned int prev = atomicAdd(&counters[b], 1u);
-            last = prev == static_cast<unsigned int>(4 * NBK - 1);
+        float s = 0.0f;
+        if (sg * kSeg < V) {                              // warp-uniform
+            stage_segment(pbuf, pv, V, sg * kSeg, al);
+            if (resid) stage_segment(qbuf, qv, V, sg * kSeg, al);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncwarp();
+            s = segment_leaf_sums(pbuf, qbuf, resid, V, sg, c, R, smp, smq, lrow);
+        } else {
+            *reinterpret_cast<float2 *>(lrow + kLeavesPerSeg * sg + 2 * lane) = make_float2(0.0f, 0.0f);
         }
+        unsigned int prev = 0;
+        __syncwarp();   // every lane's leaf sums are ordered before lane 0's fence
+        if (lane == 0) {
+            srow[sg] = s;
+            __threadfence();
+            prev = atomicAdd(&counters[b], 1u);
+        }
+        last = __shfl_sync(0xffffffffu, prev, 0) == static_cast<unsigned int>(NSP - 1);
     }
-    __syncthreads();
     if (!last) return;
     __threadfence();
 
-    // block totals: the top two levels of each block's tree over its four
-    // quarter nodes, (q0 + q1) + (q2 + q3)
-    for (int bb = threadIdx.x; bb < NBK; bb += kThreads) {
-        const float4 n4 = __ldcg(reinterpret_cast<const float4 *>(qsum + (static_cast<size_t>(b) * NBK + bb) * 4));
-        btree[bb] = __fadd_rn(__fadd_rn(n4.x, n4.y), __fadd_rn(n4.z, n4.w));
-    }
-    __syncthreads();
-    // all-zero residual (rounding): draw from p_js instead (all threads rebuild the leaf sums)
-    if (resid) {
-        float r = warp == 0 ? (lane < NBK ? btree[lane] : 0.0f) : 0.0f;
-        if (warp == 0) r = warp_tree_sum(r, 5);
-        if (threadIdx.x == 0) pick = r > 0.0f ? 1 : 0;
-        __syncthreads();
-        if (pick == 0) {
-            resid = false;
-            for (int bb = 0; bb < NBK; ++bb) {
-                float n4[4];
-                for (int qb = 0; qb < 4; ++qb)
-                    n4[qb] = quarter_block(warp_sum,
-                                           lsum + (static_cast<size_t>(b) * NBK + bb) * kBlockLeaves + kThreads * qb,
-                                           pv, qv, false, V, bb * kBlockLeaves + kThreads * qb, c, R);
-                if (threadIdx.x == 0) btree[bb] = __fadd_rn(__fadd_rn(n4[0], n4[1]), __fadd_rn(n4[2], n4[3]));
+    // ---- last warp of row b.  Block totals (lane = block): pairwise over the
+    // block's 16 segment sums.
+    auto block_total = [&](int bb) {
+        float n[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) n[i] = __ldcg(srow + kSegPerBlock * bb + i);
+#pragma unroll
+        for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+            for (int i = 0; i < 16; i += 2 * w) n[i] = __fadd_rn(n[i], n[i + w]);
+        return n[0];
+    };
+    float bval = lane < NBK ? block_total(lane) : 0.0f;
+    // all-zero residual (rounding): draw from p_js instead; this warp rebuilds
+    // every segment's leaf sums from p
+    if (resid && !(warp_tree_sum(bval, 5) > 0.0f)) {
+        resid = false;
+        for (int s2 = 0; s2 < NSP; ++s2) {
+            float ssv = 0.0f;
+            if (s2 * kSeg < V) {
+                stage_segment(pbuf, pv, V, s2 * kSeg, al);
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncwarp();
+                ssv = segment_leaf_sums(pbuf, pbuf, false, V, s2, c, R, smp, smq, lrow);
+                __syncwarp();
             }
+            if (lane == 0) srow[s2] = ssv;
         }
-        __syncthreads();
+        __threadfence_block();
+        __syncwarp();
+        bval = lane < NBK ? block_total(lane) : 0.0f;
     }
-    if (warp != 0) return;
 
-    // warp 0: block tree (32 lanes, zero pads), then the chosen block's leaf tree
-    const float bval = lane < NBK ? btree[lane] : 0.0f;
+    // descent: blocks (32 lanes, zero pads), the chosen block's 16 segments,
+    // the chosen segment's 64 leaves (pairs per lane, then the pair)
     const float root = warp_tree_sum(bval, 5);
     float t = __fmul_rn(R.u, root);
     const int bstar = warp_descend32(bval, t);
-    float v[32];
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(lsum + (static_cast<size_t>(b) * NBK + bstar) * kBlockLeaves) + 8 * lane;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 x = __ldcg(src + i);
-            v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-        }
+    const float sval = lane < kSegPerBlock ? __ldcg(srow + kSegPerBlock * bstar + lane) : 0.0f;
+    const int sstar = kSegPerBlock * bstar + warp_descend32(sval, t);
+    const float2 lpair = __ldcg(reinterpret_cast<const float2 *>(lrow + kLeavesPerSeg * sstar) + lane);
+    const int pstar = warp_descend32(__fadd_rn(lpair.x, lpair.y), t);
+    const float left = __shfl_sync(0xffffffffu, lpair.x, pstar), right = __shfl_sync(0xffffffffu, lpair.y, pstar);
+    int lstar = kLeavesPerSeg * sstar + 2 * pstar;      // global leaf index
+    if (!(t < left || !(right > 0.0f))) {
+        t = __fsub_rn(t, left);
+        lstar += 1;
     }
-    float lsum32[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) lsum32[i] = v[i];
-#pragma unroll
-    for (int w = 1; w < 32; w <<= 1)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2 * w) v[i] = __fadd_rn(v[i], v[i + w]);
-    const int lane_star = warp_descend32(v[0], t);
-    float mine = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float x = __shfl_sync(0xffffffffu, lsum32[i], lane_star);
-        if (lane == i) mine = x;
-    }
-    const int lstar = bstar * kBlockLeaves + 32 * lane_star + warp_descend32(mine, t);   // global leaf index
 
     // the chosen leaf: lanes e and e + 16 reload entry e, the weights are
-    // formed exactly as in the leaf sums, lane 0 scans them in entry order
+    // formed exactly as in the leaf sums, then the entries are scanned in order
     const int e = lane & 15;
     const int x = kLeaf * lstar + e;
     const bool present = x < V;
     const float lp = present ? __ldcg(pv + x) : -INFINITY;
-    const float lq = present && resid ? __ldcg(qv + x) : -INFINITY;
-    float mp = lp, mq = lq;
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
-    }
-    const float mzp = __fmul_rn(mp, c);
-    float we = __fmul_rn(exp2_canon(__fmaf_rn(lp, c, -mzp)), leaf_factor(mzp, R.Mp, R.invSp));
+    const float mzp = __ldcg(smp + sstar);
+    float we = __fmul_rn(exp2_canon(__fmaf_rn(lp, c, -mzp)), seg_factor(mzp, R.Mp, R.invSp));
     if (resid) {
-        const float mzq = __fmul_rn(mq, c);
-        const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq, c, -mzq)), leaf_factor(mzq, R.Mq, R.invSq));
+        const float lq = present ? __ldcg(qv + x) : -INFINITY;
+        const float mzq = __ldcg(smq + sstar);
+        const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq, c, -mzq)), seg_factor(mzq, R.Mq, R.invSq));
         const float d = __fsub_rn(we, qe);
         we = d > 0.0f ? d : 0.0f;
     }
@@ -625,6 +707,23 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         out_cnt[b] = js + 1;
         counters[b] = 0;
     }
+}
+
+// Opt the two sampling kernels into their 64 KB of dynamic shared memory,
+// once per device.
+cudaError_t allow_sampling_smem()
+{
+    static std::mutex mu;
+    static bool done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(sample_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(sample_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
 }
 
 nq_status check_accept(int B, int k, int V, const void *ws, size_t ws_bytes)
@@ -683,10 +782,16 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     const nq::WsLayout L = nq::ws_layout(B, k, V);
     char *w = static_cast<char *>(ws);
     auto *rec = reinterpret_cast<nq::SampleRec *>(w + L.rec);
+    auto *segmax = reinterpret_cast<float *>(w + L.segmax);
+    // staging: cp.async of 16-byte pieces when every vector starts on a
+    // 16-byte boundary (V % 4 == 0; the pointers are 16-byte aligned)
+    const int al = (V % 4) == 0 ? 1 : 0;
+    if (nq::allow_sampling_smem() != cudaSuccess) return NQ_ERR_CUDA;
     dim3 grid_a(nq::n_blocks(V), 2 * k + 1, B);
-    nq::sample_a_kernel<<<grid_a, nq::kThreads, 0, stream>>>(draft, draft_logits, tgt_logits, k, V, c, seeds, round,
-                                                             reinterpret_cast<unsigned int *>(w + L.counters_a),
-                                                             reinterpret_cast<float2 *>(w + L.part), rec, status);
+    nq::sample_a_kernel<<<grid_a, nq::kThreads, nq::kSmemS, stream>>>(
+        draft, draft_logits, tgt_logits, k, V, c, al, seeds, round, reinterpret_cast<unsigned int *>(w + L.counters_a),
+        reinterpret_cast<unsigned int *>(w + L.vcount), reinterpret_cast<float2 *>(w + L.part), segmax,
+        reinterpret_cast<float2 *>(w + L.roots), rec, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return NQ_ERR_CUDA;
     // pass B as a programmatic dependent launch when pass A fills the GPU: its
@@ -696,18 +801,19 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     // the dependent launch); griddepcontrol.wait returns at once then.
     const bool dependent = static_cast<long long>(grid_a.x) * grid_a.y * grid_a.z >= nq::sm_count();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(4 * nq::n_blocks(V), B);   // one CTA per (block, leaf quarter q)
+    cfg.gridDim = dim3(nq::n_segments_padded(V) / nq::kWarpsS, B);   // one warp per segment
     cfg.blockDim = dim3(nq::kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = nq::kSmemS;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, out_tok, out_cnt,
+    e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, al, out_tok, out_cnt,
                            reinterpret_cast<unsigned int *>(w + L.counters_b), static_cast<const nq::SampleRec *>(rec),
-                           reinterpret_cast<float *>(w + L.qsum), reinterpret_cast<float *>(w + L.lsum));
+                           static_cast<const float *>(segmax), reinterpret_cast<float *>(w + L.ssum),
+                           reinterpret_cast<float *>(w + L.lsum));
     return nq::cuda_status(e);
 }
 

@@ -54,18 +54,22 @@ def test_packed_bytes(L):
 
 def test_workspace_bytes(L):
     from quantized_self_speculative_gb300 import nq
-    # sections, each starting on a 256-byte boundary: two ticket arrays, (2k+1)
-    # partials per 4096-entry chunk per row, a 32-B decision record per row,
-    # four quarter-block sums per 16384-entry block per row, 1024 leaf sums per
-    # block per row
+    # sections, each starting on a 256-byte boundary: two ticket arrays,
+    # (2k+1) partials per row of max(4096-entry chunks, 2048-entry segment
+    # pairs), a 32-B decision record per row, one maximum per 1024-entry
+    # segment (16 per 16384-entry block) per vector per row, one sum per
+    # segment per row, 64 leaf sums per segment per row, a ticket and a root
+    # (max, 1/sum) per vector per row
     a = lambda n: (n + 255) // 256 * 256
 
     def expect(B, k, V):
-        C, NB = -(-V // 4096), -(-V // 16384)
-        return a(4 * B) * 2 + a(B * (2 * k + 1) * C * 8) + a(32 * B) + a(16 * B * NB) + 4096 * B * NB
+        C, NSP, NV = -(-V // 4096), 16 * -(-V // 16384), 2 * k + 1
+        P = max(C, NSP // 2)
+        return (a(4 * B) * 2 + a(B * NV * P * 8) + a(32 * B) + a(B * NV * NSP * 4)
+                + a(4 * B * NSP) + a(256 * B * NSP) + a(4 * B * NV) + 8 * B * NV)
 
-    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 2964992
-    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 5376
+    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 4070656
+    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 6984
     assert nq.workspace_bytes(3, 16, 4099) == expect(3, 16, 4099)
     for bad in [(0, 4, 10), (1, 0, 10), (1, 17, 10), (1, 4, 0), (1, 4, 524289), (65536, 1, 1)]:
         assert nq.workspace_bytes(*bad) == 0

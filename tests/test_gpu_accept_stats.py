@@ -45,8 +45,11 @@ def softmax64(l):
 def test_gpu_matches_fp64_textbook_round(nq, k, noise):
     """Acceptance-sweep shape: B = 64, V = 152064, target ~ N(0, 3), draft =
     target + N(0, noise) at the noise levels that give alpha ~ 0.6 and ~ 0.95.
-    Every row whose uniforms are not within 1e-5 of a decision boundary must
-    get the same count and ids as the fp64 round."""
+    Every row must get the same count and ids as the fp64 round unless one of
+    its uniforms lies within fp32 rounding of a decision boundary: the fp32
+    recipe's probabilities and tree sums carry a relative error of a few
+    units of 2^-24 (about 1e-6 of the total at most), so a row may differ
+    only where the fp64 margin is below 1e-6."""
     B, V = 64, 152064
     tl = synth.target_logits(9100 + k, B, k, V, 3.0)
     dl = synth.draft_logits_from(tl, 9101 + k, noise)
@@ -58,11 +61,11 @@ def test_gpu_matches_fp64_textbook_round(nq, k, noise):
         out, cnt = out.cpu().numpy(), cnt.cpu().numpy()
         out64, cnt64, margin = O.accept_sample_f64(d, dl, tl, 1.0, seeds, rnd)
         differ = np.any(out != out64, axis=1) | (cnt != cnt64)
-        assert np.all(margin[differ] < 1e-5), (rnd, np.nonzero(differ))
-        near += int((margin < 1e-5).sum())
+        assert np.all(margin[differ] < 1e-6), (rnd, np.nonzero(differ), margin[differ])
+        near += int((margin < 1e-6).sum())
         total += int(differ.sum())
     assert nq.device_status() == 0
-    assert total <= 1, (total, near)
+    assert total <= near, (total, near)
 
 
 def gpu_rounds(nq, p_logits, q_logits, rows, seed, calls=2, T=1.0):
