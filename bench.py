@@ -280,6 +280,170 @@ def eq2_report(t_draft_us, t_verify_us, t_accept_us, t_target_us, k=K_DRAFT):
     return out
 
 
+# ------------------------------------------------------------------ the round, measured
+class RoundLoop:
+    """Whole speculative rounds on the device ("Drafting and checking
+    tokens"; Eq. (2)): LLaMA-2-7B-shaped linears with q|k|v and gate|up fused
+    (one weight stream per layer input: 32 x {qkv 4096->12288, o 4096x4096,
+    gate|up 4096->22016, down 11008->4096} + lm_head 4096->32000), nested
+    4+4-bit, group 128, batch 1, k = 4, greedy.  Per round: k draft passes
+    (base plane, M = 1), each drafted token the argmax of the previous draft
+    pass's lm_head output and the next pass's lm_head input (its embedding
+    row); one verify pass over the k+1 positions (both planes, M = k+1); greedy
+    acceptance; the emitted tokens committed on the device.  The linears other
+    than lm_head take fixed synthetic activations (the attention, norms and
+    MLP nonlinearity between linears are not part of this hot path), so the
+    token dependency runs through lm_head.  One round is captured in a CUDA
+    graph and replayed; the emitted count is read back once at the end."""
+
+    def __init__(self, device, seed=23, k=K_DRAFT, max_rounds=512):
+        import torch
+        from quantized_self_speculative_gb300 import nq
+        self.torch, self.nq, self.dev, self.k = torch, nq, device, k
+        h, f = 4096, 11008
+        layer = [("qkv", 3 * h, h), ("o", h, h), ("gate_up", 2 * f, h), ("down", h, f)]
+        self.shapes = [(f"L{i}.{nm}", n, kk) for i in range(32) for nm, n, kk in layer] + [("lm_head", V_LM, h)]
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed)
+        self.layers = []
+        for _, n, kk in self.shapes:
+            w = torch.randn((n, kk), generator=gen, device=device, dtype=torch.float32).mul_(0.02)
+            self.layers.append(nq.pack_weights(w, nq.FMT_NESTED44, GROUP))
+            del w
+        self.table = torch.randn((V_LM, h), generator=gen, device=device).to(torch.bfloat16)
+        B = 1
+        self.x_lm = torch.empty((B, h), dtype=torch.bfloat16, device=device)
+        self.y_lm = torch.empty((B, V_LM), dtype=torch.float32, device=device)
+        self.x_v = torch.empty((B * (k + 1), h), dtype=torch.bfloat16, device=device)
+        self.tl = torch.empty((B, k + 1, V_LM), dtype=torch.float32, device=device)
+
+        def batch(M, x_last, y_last, verify):
+            xs, ys = [], []
+            for name, n, kk in self.shapes:
+                if name == "lm_head":
+                    xs.append(x_last)
+                    ys.append(y_last)
+                else:
+                    xs.append(torch.randn((M, kk), generator=gen, device=device).to(torch.bfloat16))
+                    ys.append(torch.empty((M, n), dtype=torch.float32, device=device))
+            return nq.LinearBatch(verify, self.layers, xs, ys)
+        self.draft_batch = batch(B, self.x_lm, self.y_lm, False)
+        self.verify_batch = batch(B * (k + 1), self.x_v, self.tl.view(B * (k + 1), V_LM), True)
+        self.target_batch = batch(B, self.x_lm, self.y_lm, True)
+        self.max_len = 1 + max_rounds * (k + 1)
+        self.seq = torch.full((B, self.max_len), -1, dtype=torch.int32, device=device)
+        self.seq_len = torch.ones(B, dtype=torch.int32, device=device)
+        self.x0 = torch.tensor([7], dtype=torch.int32, device=device)
+        self.seq[0, 0] = 7
+        self.draft = torch.zeros((B, k), dtype=torch.int32, device=device)
+        self.out_tok = torch.empty((B, k + 1), dtype=torch.int32, device=device)
+        self.out_cnt = torch.empty(B, dtype=torch.int32, device=device)
+        self.ws_arg = nq.accept_workspace(B, 0, V_LM, device)
+        self.ws_acc = nq.accept_workspace(B, k, V_LM, device)
+        self.bytes_draft = sum(draft_bytes(n, kk, 1) for _, n, kk in self.shapes)
+        self.bytes_verify = sum(verify_bytes(n, kk, k + 1) for _, n, kk in self.shapes)
+        self.graph = None
+
+    def one_round(self, ev=None):
+        nq, k = self.nq, self.k
+        for j in range(k):
+            if ev is not None:
+                ev[j].record()
+            if j == 0:
+                nq.embed_rows(self.table, self.x0, 1, out=self.x_lm)
+            else:
+                nq.embed_rows(self.table, self.draft.view(-1)[j - 1:], 1, ids_stride=k, out=self.x_lm)
+            self.draft_batch()
+            nq.draft_argmax(self.y_lm, self.draft.view(-1)[j:], tok_stride=k, ws=self.ws_arg)
+        if ev is not None:
+            ev[k].record()
+        nq.embed_round(self.table, self.x0, self.draft, 1, k, out=self.x_v)
+        self.verify_batch()
+        if ev is not None:
+            ev[k + 1].record()
+        nq.accept_greedy(self.draft, self.tl, ws=self.ws_acc, out_tok=self.out_tok, out_cnt=self.out_cnt)
+        nq.round_commit(self.out_tok, self.out_cnt, self.seq, self.seq_len, self.x0)
+        if ev is not None:
+            ev[k + 2].record()
+
+    def reset(self):
+        self.seq_len.fill_(1)
+        self.x0.fill_(7)
+
+    def capture(self):
+        torch = self.torch
+        self.one_round()                      # warm-up outside the capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=s):
+                self.one_round()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+    def measure(self, rounds=100):
+        """Rounds replayed from the graph; time per round and per emitted token,
+        with the pass times of the same round (events, eager) for Eq. (2)."""
+        torch, k = self.torch, self.k
+        if self.graph is None:
+            self.capture()
+        self.reset()
+        for _ in range(3):
+            self.graph.replay()
+        self.reset()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(rounds):
+            self.graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us_round = e0.elapsed_time(e1) * 1e3 / rounds
+        tokens = int(self.seq_len[0].item()) - 1
+        # pass times of the same round (eager, events between the launches)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(k + 3)] for _ in range(10)]
+        for ev in evs:
+            self.one_round(ev)
+        torch.cuda.synchronize()
+        t_draft = statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in evs for j in range(k)) * 1e3
+        t_verify = statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in evs) * 1e3
+        t_accept = statistics.mean(ev[k + 1].elapsed_time(ev[k + 2]) for ev in evs) * 1e3
+        # the target alone: one verify pass over one position per token (M = 1)
+        for _ in range(3):
+            self.target_batch()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(20):
+            self.target_batch()
+        e1.record()
+        torch.cuda.synchronize()
+        t_target = e0.elapsed_time(e1) * 1e3 / 20
+        E = tokens / rounds
+        # acceptance rate implied by Eq. (1) at the measured tokens per round
+        lo, hi = 0.0, 1.0
+        for _ in range(60):
+            a = 0.5 * (lo + hi)
+            if (1 - a ** (k + 1)) / (1 - a) < E:
+                lo = a
+            else:
+                hi = a
+        alpha = 0.5 * (lo + hi)
+        eq2 = (t_verify + t_accept + k * t_draft) / E
+        return {"rounds": rounds, "tokens": tokens, "tokens_per_round": round(E, 4),
+                "alpha_from_eq1": round(alpha, 4), "us_per_round": round(us_round, 1),
+                "us_per_token": round(us_round / E, 1),
+                "eq2_us_per_token_from_pass_times": round(eq2, 1),
+                "t_draft_pass_us": round(t_draft, 1), "t_verify_pass_us": round(t_verify, 1),
+                "t_accept_commit_us": round(t_accept, 1), "t_target_only_us": round(t_target, 1),
+                "speedup_vs_target_only": round(t_target / (us_round / E), 3),
+                "draft_pass_gbs": round(self.bytes_draft / (t_draft * 1e-6) / 1e9, 1),
+                "verify_pass_gbs": round(self.bytes_verify / (t_verify * 1e-6) / 1e9, 1),
+                "layout": "q|k|v and gate|up fused: 129 linears per pass",
+                "launches_per_round": 3 * k + 5}
+
+
 # ------------------------------------------------------------------ per-linear times (LLaMA-2-7B shapes)
 def per_linear_table(R, reps=3):
     """Device time of one linear per launch, for each linear shape of the
@@ -738,10 +902,14 @@ def run_ours(args):
     }
     if not args.no_extras:
         line["per_linear_llama2_7b"] = per_linear_table(R)
-        line["accept_sweep_B64_V152064"] = accept_sweep(device)
-    if args.extras == "full" and not args.no_extras:
         del R
         torch.cuda.empty_cache()
+        RL = RoundLoop(device)
+        line["round_measured"] = RL.measure()
+        del RL
+        torch.cuda.empty_cache()
+        line["accept_sweep_B64_V152064"] = accept_sweep(device)
+    if args.extras == "full" and not args.no_extras:
         line["config3_llama3_8b_b16_k8"] = config3_sweep(device)
         line["config4_qwen25_7b_tiers"] = config4_sweep(device)
         line["config5_tokens_per_round"] = config5_tokens(device)

@@ -70,6 +70,7 @@ typedef enum {
 #define NQ_DEV_BAD_TOKEN 0x2u
 #define NQ_DEV_TIMEOUT   0x4u
 #define NQ_DEV_ACT_RANGE 0x8u   /* an activation exceeded the fp16 range (|x| > 65504) */
+#define NQ_DEV_SEQ_FULL  0x10u  /* spec_round_commit: a sequence buffer was full, tokens dropped */
 
 /*
  * Weight formats (SpecQuant Sec. III.A tiers; BitNest Fig. 3 planes).
@@ -189,7 +190,8 @@ NQ_API nq_status nq_verify_gemm_batch_ws(int count, const nq_weights *w, const u
  * workspace must be zero-filled once before its first use; every call leaves
  * it ready for the next one.  Calls that share a workspace must not overlap
  * on the GPU (use one stream, or one workspace per stream).
- * Limits: 1 <= B <= 65535, 1 <= k <= 16, 1 <= V <= 524288.  Returns 0 on bad sizes.
+ * Limits: 1 <= B <= 65535, 1 <= k <= 16, 1 <= V <= 524288; k = 0 gives the
+ * workspace of spec_draft_argmax over B rows.  Returns 0 on bad sizes.
  */
 NQ_API size_t spec_accept_workspace_bytes(int B, int k, int V);
 
@@ -230,6 +232,52 @@ NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_log
                              int B, int k, int V, float temperature, const uint64_t *seeds,
                              uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
                              size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Round bookkeeping ("Drafting and checking tokens": the draft proposes k
+ * tokens one at a time, each from the previous one; the target checks the
+ * k+1 positions in one pass; the kept prefix plus the target's token extend
+ * the sequence and that last token starts the next round).  These four calls
+ * keep a whole round on the device, so that it can be queued (or captured in
+ * a CUDA graph) with no host round trip.  Token arrays are int32 and need
+ * 4-byte alignment only; tables and activations 16-byte alignment.
+ *
+ * spec_draft_argmax: the draft model's greedy choice per row,
+ *   tok[m * tok_stride] = argmax_x logits[m][x] (lowest index on ties).
+ *   logits fp32 [M][V]; workspace spec_accept_workspace_bytes(M, 0, V),
+ *   zero-filled once (calls leave it ready).  Non-finite logits set
+ *   NQ_DEV_NONFINITE.  1 <= M <= 65535.
+ */
+NQ_API nq_status spec_draft_argmax(const float *logits, int M, int V, int32_t *tok, int tok_stride, void *ws,
+                                   size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * nq_embed_rows: input rows of a pass from token ids,
+ *   out[m][:] = table[ids[m * ids_stride]][:],  m = 0..M-1.
+ * nq_embed_round: the verify pass's k+1 input rows per sequence b, position 0
+ *   the last committed token x0[b], positions 1..k the drafted tokens:
+ *   out[b][j][:] = table[j == 0 ? x0[b] : draft[b][j-1]][:].
+ * table: bf16 bits [V][d], d a multiple of 8; out: bf16 bits, rows of d.  An
+ * id outside [0, V) writes a zero row and sets NQ_DEV_BAD_TOKEN.
+ */
+NQ_API nq_status nq_embed_rows(const uint16_t *table, int V, int d, const int32_t *ids, int ids_stride, int M,
+                               uint16_t *out, cudaStream_t stream);
+NQ_API nq_status nq_embed_round(const uint16_t *table, int V, int d, const int32_t *x0, const int32_t *draft,
+                                int B, int k, uint16_t *out, cudaStream_t stream);
+
+/*
+ * spec_round_commit: after an acceptance call (out_tok [B][k+1], out_cnt [B]),
+ *   seq[b][L .. L + c - 1] = out_tok[b][0 .. c - 1]   (c = out_cnt[b], L = seq_len[b])
+ *   seq_len[b] = L + c;   x0[b] = out_tok[b][c - 1]   (the next round's first input).
+ * seq: int32 [B][max_len]; seq_len, x0: int32 [B] (in/out).  Tokens beyond
+ * max_len are dropped and set NQ_DEV_SEQ_FULL; a count outside 1..k+1 appends
+ * nothing and sets NQ_DEV_BAD_TOKEN.  The verify pass computed KV entries for
+ * its k+1 positions x0, d_0 .. d_{k-1}; the first c of them stay and the
+ * rejected suffix (positions c .. k) is discarded (BitNest, Fig. 4), so a
+ * caller's cache length becomes seq_len[b] - 1.
+ */
+NQ_API nq_status spec_round_commit(const int32_t *out_tok, const int32_t *out_cnt, int B, int k, int32_t *seq,
+                                   int32_t *seq_len, int max_len, int32_t *x0, cudaStream_t stream);
 
 /*
  * Greedy acceptance that allocates nothing and takes no workspace: the same

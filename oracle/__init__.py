@@ -75,6 +75,9 @@ def lib():
             L.orc_softmax_canonical.argtypes = [vp, i32, f32, vp]
             L.orc_tree_sample.argtypes = [vp, i32, f32]
             L.orc_softmax_stats.argtypes = [vp, i32, f32, vp, vp, vp, vp]
+            L.orc_draft_argmax.argtypes = [vp, i32, i32, vp]
+            L.orc_sample_p.argtypes = [vp, i32, f32, f32]
+            L.orc_round_commit.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp]
             L.orc_f32_to_f16_n.argtypes = [vp, vp, i32]
             L.orc_f16_to_f32_n.argtypes = [vp, vp, i32]
             L.orc_f32_to_e4m3_n.argtypes = [vp, vp, i32]
@@ -293,3 +296,52 @@ def softmax_stats(logits, temperature: float = 1.0):
                                C.byref(M), C.byref(S)) < 0:
         raise ValueError("non-finite logits")
     return mz, s, np.float32(M.value), np.float32(S.value)
+
+
+# ------------------------------------------------------------------ round bookkeeping
+# "How Speculative Decoding Speeds Up Inference", "Drafting and checking
+# tokens"; BitNest Fig. 4 (the rejected suffix's cache entries are dropped).
+
+def draft_argmax(logits):
+    """The draft's greedy choice per row of logits [M][V] (lowest index on ties)."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    M, V = l.shape
+    tok = np.empty(M, np.int32)
+    if lib().orc_draft_argmax(l.ctypes.data, M, V, tok.ctypes.data) < 0:
+        raise ValueError("non-finite logits")
+    return tok
+
+
+def round_commit(out_tok, out_cnt, seq, seq_len, x0):
+    """Append the emitted tokens; returns (seq, seq_len, x0, rc) updated copies
+    (rc 1: a sequence ran out of room, -1: a count outside 1..k+1)."""
+    out_tok = np.ascontiguousarray(out_tok, dtype=np.int32)
+    out_cnt = np.ascontiguousarray(out_cnt, dtype=np.int32)
+    B, k1 = out_tok.shape
+    seq = np.array(seq, dtype=np.int32, copy=True)
+    seq_len = np.array(seq_len, dtype=np.int32, copy=True)
+    x0 = np.array(x0, dtype=np.int32, copy=True)
+    rc = lib().orc_round_commit(out_tok.ctypes.data, out_cnt.ctypes.data, B, k1 - 1, seq.ctypes.data,
+                                seq_len.ctypes.data, seq.shape[1], x0.ctypes.data)
+    return seq, seq_len, x0, rc
+
+
+def embed_rows(table, ids):
+    """Rows of table [V][d] (bf16 bits) for the token ids; a plain gather."""
+    return np.ascontiguousarray(np.asarray(table)[np.asarray(ids, dtype=np.int64)])
+
+
+def embed_round(table, x0, draft):
+    """The verify pass's rows per sequence: x0[b], then draft[b][0..k-1]."""
+    ids = np.concatenate([np.asarray(x0, np.int64)[:, None], np.asarray(draft, np.int64)], axis=1)
+    return embed_rows(table, ids.reshape(-1))
+
+
+def sample_p(logits, temperature: float, u: float) -> int:
+    """A draw from the canonical p of one logits vector with uniform u (the
+    bonus draw's two-level rule: segment weights, then the segment's leaves)."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    r = lib().orc_sample_p(l.ctypes.data, l.shape[0], float(temperature), float(u))
+    if r < 0:
+        raise ValueError("non-finite logits")
+    return r

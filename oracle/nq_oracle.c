@@ -338,6 +338,41 @@ int orc_accept_greedy(const int32_t *draft, const float *tgt_logits, int B, int 
 }
 
 /* ======================================================================== */
+/* Round bookkeeping [Erge, "Drafting and checking tokens"; BitNest Fig. 4]. */
+/* ======================================================================== */
+
+/* The draft model's greedy choice of each of M rows (lowest index on ties). */
+int orc_draft_argmax(const float *logits, int M, int V, int32_t *tok)
+{
+    for (int m = 0; m < M; m++) {
+        tok[m] = argmax_lowest(logits + (size_t)m * V, V);
+        if (tok[m] < 0) return -1;
+    }
+    return 0;
+}
+
+/* Append each row's emitted tokens (the first out_cnt[b] of out_tok[b]) to
+ * its sequence, up to max_len; the last emitted token is the next round's
+ * first input.  Returns 1 if some sequence ran out of room, -1 on a count
+ * outside 1..k+1 (that row is left unchanged), else 0. */
+int orc_round_commit(const int32_t *out_tok, const int32_t *out_cnt, int B, int k, int32_t *seq,
+                     int32_t *seq_len, int max_len, int32_t *x0)
+{
+    int rc = 0;
+    for (int b = 0; b < B; b++) {
+        int c = out_cnt[b];
+        if (c < 1 || c > k + 1) { rc = -1; continue; }
+        for (int i = 0; i < c; i++) {
+            if (seq_len[b] >= max_len) { if (rc == 0) rc = 1; break; }
+            seq[(size_t)b * max_len + seq_len[b]] = out_tok[(size_t)b * (k + 1) + i];
+            seq_len[b] += 1;
+        }
+        x0[b] = out_tok[(size_t)b * (k + 1) + c - 1];
+    }
+    return rc;
+}
+
+/* ======================================================================== */
 /* C4: sampled acceptance (Leviathan et al.; Chen et al.)  [Erge, "The same  */
 /*     output as the large model alone"]; canonical fp32 arithmetic (R5).    */
 /* ======================================================================== */
@@ -405,6 +440,12 @@ float orc_uniform(uint64_t seed, uint32_t j, uint32_t purpose, uint64_t round)
  *            t -= L and go right), then scan the leaf for the first x whose
  *            running sum exceeds t (fallback: last x of the leaf with w > 0).
  *            R == 0 for the residual -> sample from p_j instead.
+ *   sampling from p (the bonus draw, and the residual's fallback): the first
+ *            level picks a segment by the pairwise tree over the segment
+ *            weights W = RN(s_seg * F_seg) (the (max, sum) pass's own
+ *            segment sums rescaled to p; pads 0), t = RN(u R_W); the second
+ *            level descends the chosen segment's pairwise tree over its 64
+ *            leaf sums of p with the remaining t and scans the leaf as above.
  *   uniforms: purpose 0 = accept test at j, 1 = resample at j, 2 = bonus at k.
  */
 static const float ORC_LOG2E = 1.44269504088896340736f;
@@ -605,6 +646,88 @@ int orc_tree_sample(const float *w, int V, float u)
     return result;
 }
 
+/* Descend a pairwise sum tree level by level: node i of level l is
+ * level[l][i]; at each level go left if t < left or the right sum is not
+ * positive, else t -= left.  Returns the leaf index; *t is updated. */
+static int tree_descend(float **level, int levels, float *t)
+{
+    int node = 0;
+    for (int l = levels; l >= 1; l--) {
+        float left = level[l - 1][2 * node], right = level[l - 1][2 * node + 1];
+        if (*t < left || !(right > 0.0f)) node = 2 * node;
+        else { *t = *t - left; node = 2 * node + 1; }
+    }
+    return node;
+}
+
+/* Pairwise tree levels over n values (padded with zeros to a power of two). */
+static int tree_build(const float *v, int n, float ***out)
+{
+    int P = pow2_at_least(n), levels = 0;
+    while ((1 << levels) < P) levels++;
+    float **level = malloc(sizeof(float *) * (levels + 1));
+    for (int l = 0; l <= levels; l++) level[l] = calloc((size_t)(P >> l), sizeof(float));
+    for (int i = 0; i < n; i++) level[0][i] = v[i];
+    for (int l = 1; l <= levels; l++)
+        for (int i = 0; i < (P >> l); i++) level[l][i] = level[l - 1][2 * i] + level[l - 1][2 * i + 1];
+    *out = level;
+    return levels;
+}
+static void tree_free(float **level, int levels)
+{
+    for (int l = 0; l <= levels; l++) free(level[l]);
+    free(level);
+}
+
+/* Draw from p of one logits vector with uniform u by the two-level rule of
+ * R5 (segment weights from the (max, sum) pass, then the chosen segment's
+ * leaf tree).  Returns -1 if the vector is not valid. */
+int orc_sample_p(const float *l, int V, float T, float u)
+{
+    float c = orc_temper_coef(T);
+    for (int x = 0; x < V; x++) if (!isfinite(l[x])) return -1;
+    int NS = n_segments(V), LPS = ORC_SEG / ORC_LEAF;
+    ms_t *seg = malloc(sizeof(ms_t) * NS);
+    seg_stats(l, V, c, seg);
+    for (int i = 0; i < NS; i++) if (!isfinite(seg[i].m)) { free(seg); return -1; }
+    ms_t root = ms_tree(seg, NS);
+    float inv_s = 1.0f / root.s;
+    float *W = malloc(sizeof(float) * NS), *F = malloc(sizeof(float) * NS);
+    for (int i = 0; i < NS; i++) {
+        F[i] = orc_exp2c(seg[i].m - root.m) * inv_s;
+        W[i] = seg[i].s * F[i];
+    }
+    float **lv;
+    int levels = tree_build(W, NS, &lv);
+    float t = u * lv[levels][0];
+    int sg = tree_descend(lv, levels, &t);
+    tree_free(lv, levels);
+    /* the chosen segment: p(x), leaf sums, leaf tree, scan */
+    float pw[ORC_SEG], ls[ORC_SEG / ORC_LEAF];
+    for (int e = 0; e < ORC_SEG; e++) {
+        int x = ORC_SEG * sg + e;
+        pw[e] = x < V ? orc_exp2c(fmaf(l[x], c, -seg[sg].m)) * F[sg] : 0.0f;
+    }
+    for (int i = 0; i < LPS; i++) ls[i] = leaf_sum(pw + ORC_LEAF * i);
+    levels = tree_build(ls, LPS, &lv);
+    int leaf = tree_descend(lv, levels, &t);
+    tree_free(lv, levels);
+    int result = -1;
+    float run = 0.0f;
+    for (int e = 0; e < ORC_LEAF && result < 0; e++) {
+        int x = ORC_SEG * sg + ORC_LEAF * leaf + e;
+        if (x >= V) continue;
+        run = run + pw[ORC_LEAF * leaf + e];
+        if (t < run) result = x;
+    }
+    for (int e = ORC_LEAF - 1; e >= 0 && result < 0; e--) {
+        int x = ORC_SEG * sg + ORC_LEAF * leaf + e;
+        if (x < V && pw[ORC_LEAF * leaf + e] > 0.0f) result = x;
+    }
+    free(seg); free(W); free(F);
+    return result;
+}
+
 /*
  * Speculative sampling for B rows: draft tokens d_0..d_{k-1} drawn from q,
  * draft logits [B][k][V], target logits [B][k+1][V].  For j = 0..k-1 accept
@@ -633,14 +756,15 @@ int orc_accept_sample(const int32_t *draft, const float *draft_logits, const flo
             for (int x = 0; x < V; x++) { float dlt = p[x] - q[x]; r[x] = dlt > 0.0f ? dlt : 0.0f; }
             float u1 = orc_uniform(seeds[b], (uint32_t)j, 1, round);
             tok = orc_tree_sample(r, V, u1);
-            if (tok < 0) tok = orc_tree_sample(p, V, u1);
+            if (tok < 0) tok = orc_sample_p(tgt_logits + ((size_t)b * (k + 1) + j) * V, V, T, u1);
             n = j;
             break;
         }
         if (rc) break;
         if (n == k) {
-            if (orc_softmax_canonical(tgt_logits + ((size_t)b * (k + 1) + k) * V, V, T, p)) { rc = -1; break; }
-            tok = orc_tree_sample(p, V, orc_uniform(seeds[b], (uint32_t)k, 2, round));
+            tok = orc_sample_p(tgt_logits + ((size_t)b * (k + 1) + k) * V, V, T,
+                               orc_uniform(seeds[b], (uint32_t)k, 2, round));
+            if (tok < 0) { rc = -1; break; }
         }
         for (int j = 0; j <= k; j++)
             out_tok[b * (k + 1) + j] = j < n ? draft[b * k + j] : (j == n ? tok : -1);

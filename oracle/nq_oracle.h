@@ -45,6 +45,10 @@ float orc_exp2_coef(int i);
 float orc_temper_coef(float T);
 int orc_softmax_canonical(const float *l, int V, float T, float *p);
 int orc_tree_sample(const float *w, int V, float u);
+int orc_sample_p(const float *l, int V, float T, float u);
+int orc_draft_argmax(const float *logits, int M, int V, int32_t *tok);
+int orc_round_commit(const int32_t *out_tok, const int32_t *out_cnt, int B, int k, int32_t *seq,
+                     int32_t *seq_len, int max_len, int32_t *x0);
 int orc_softmax_stats(const float *l, int V, float T, float *seg_mz, float *seg_s, float *M, float *S);
 int orc_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
                       int B, int k, int V, float T, const uint64_t *seeds, uint64_t round,

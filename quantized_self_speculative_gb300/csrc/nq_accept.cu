@@ -59,7 +59,7 @@ __device__ __forceinline__ ValIdx warp_best(ValIdx a)
 
 __global__ void __launch_bounds__(kThreads)
 greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, int k, int V,
-              int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
+              int32_t *__restrict__ out_tok, int tok_stride, int32_t *__restrict__ out_cnt,
               unsigned int *__restrict__ counters, float2 *__restrict__ part, unsigned int *status)
 {
     __shared__ ValIdx red[kThreads / 32];
@@ -140,8 +140,8 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
             if (d != tj[jj] && n == k) n = jj;
         }
         for (int jj = 0; jj <= k; ++jj)
-            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < n ? draft[static_cast<size_t>(b) * k + jj] : (jj == n ? tj[n] : -1);
-        out_cnt[b] = n + 1;
+            out_tok[static_cast<size_t>(b) * tok_stride + jj] = jj < n ? draft[static_cast<size_t>(b) * k + jj] : (jj == n ? tj[n] : -1);
+        if (out_cnt) out_cnt[b] = n + 1;
         counters[b] = 0;   // ready for the next call
     }
 }
@@ -176,9 +176,16 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 constexpr int kSeg = 1024;                       // entries per segment
 constexpr int kSegPerBlock = kBlock / kSeg;      // 16 per pass-A CTA (two per warp)
 constexpr int kLeavesPerSeg = kSeg / kLeaf;      // 64
-constexpr int kWarpsS = kThreads / 32;           // 8 warps per sampling CTA
-constexpr int kSmemS = kWarpsS * 2 * kSeg * 4;   // 64 KB: two segment buffers per warp
-constexpr int kSampleCtas = 3;                   // resident CTAs per SM (shared memory bound)
+#ifndef NQ_SAMPLE_WARPS
+#define NQ_SAMPLE_WARPS 2
+#endif
+#ifndef NQ_SAMPLE_CTAS
+#define NQ_SAMPLE_CTAS 14
+#endif
+constexpr int kWarpsS = NQ_SAMPLE_WARPS;         // warps per sampling CTA
+constexpr int kThreadsS = 32 * kWarpsS;
+constexpr int kSmemS = kWarpsS * 2 * kSeg * 4;   // two 4 KB segment buffers per warp
+constexpr int kSampleCtas = NQ_SAMPLE_CTAS;      // resident CTAs per SM (launch bounds)
 
 inline int n_segments_padded(int V) { return n_blocks(V) * kSegPerBlock; }
 
@@ -187,12 +194,12 @@ struct SampleRec {      // per-row decision, written by pass A, read by pass B
     int resid;          // 1: draw from max(0, p_js - q_js); 0: draw from p_js
     float u;            // the draw's uniform
     float Mp, invSp, Mq, invSq;
-    int pad;
+    int done;           // 1: pass A already drew the token (bonus draw from p_k)
 };
 
 // Workspace layout shared by the greedy and sampled calls.
 struct WsLayout {
-    size_t counters_a, counters_b, part, rec, segmax, ssum, lsum, vcount, roots, total;
+    size_t counters_a, counters_b, part, rec, segmax, segsum, ssum, lsum, vcount, roots, total;
 };
 
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
@@ -213,7 +220,8 @@ inline WsLayout ws_layout(int B, int k, int V)
     const size_t P = C > NSP / 2 ? C : NSP / 2;
     L.rec = L.part + align256(static_cast<size_t>(B) * NV * P * sizeof(float2));
     L.segmax = L.rec + align256(static_cast<size_t>(B) * sizeof(SampleRec));        // per (row, vector, segment)
-    L.ssum = L.segmax + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));
+    L.segsum = L.segmax + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));   // per (row, vector, segment)
+    L.ssum = L.segsum + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));
     L.lsum = L.ssum + align256(static_cast<size_t>(B) * NSP * sizeof(float));         // per (row, segment)
     L.vcount = L.lsum + align256(static_cast<size_t>(B) * NSP * kLeavesPerSeg * sizeof(float));
     L.roots = L.vcount + align256(static_cast<size_t>(B) * NV * sizeof(unsigned int));  // per (row, vector)
@@ -355,28 +363,188 @@ __device__ __forceinline__ float prob_at(const float *vec, const float *segm, in
     return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz)), seg_factor(mz, root.M, root.inv_s));
 }
 
-// ---- pass A: warp w of CTA (blk, v, b) reduces segments 2 g and 2 g + 1
-// (g = 8 blk + w) of vector v of row b; the last warp of the row decides.
-__global__ void __launch_bounds__(kThreads, kSampleCtas)
+// Sampling weights of a lane's 32 entries of row b's chosen position,
+// max(0, RN(p - q)) (resid) or p, with p = RN(e2(t_p) Fp); returns the two
+// leaf sums (entries 0..15 and 16..31).
+__device__ __forceinline__ float2 lane_leaf_sums(const float (&lp)[32], const float (&lq)[32], bool resid,
+                                                 float c, float mzp, float Fp, float mzq, float Fq)
+{
+    const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp), nmzq = f2_pack(-mzq, -mzq);
+    unsigned long long eo[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int i = 16 * h + 2 * p;
+            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[i], lp[i + 1]), c2, nmzp));
+            float w0 = __fmul_rn(ep.x, Fp), w1 = __fmul_rn(ep.y, Fp);
+            if (resid) {
+                const float2 eq = exp2_canon_x2(f2_fma(f2_pack(lq[i], lq[i + 1]), c2, nmzq));
+                const float d0 = __fsub_rn(w0, __fmul_rn(eq.x, Fq)), d1 = __fsub_rn(w1, __fmul_rn(eq.y, Fq));
+                w0 = d0 > 0.0f ? d0 : 0.0f;
+                w1 = d1 > 0.0f ? d1 : 0.0f;
+            }
+            eo[h] = p == 0 ? f2_pack(w0, w1) : f2_add(eo[h], f2_pack(w0, w1));
+        }
+    }
+    return make_float2(pair_sum(eo[0]), pair_sum(eo[1]));
+}
+
+// Descend the pairwise sum tree over 32 leaves held one per lane (index =
+// lane; pads are zeros).  Level sums are formed as left + right by xor
+// shuffles (fp addition commutes exactly); at each level go left if t < left
+// or the right sum is not positive, else t -= left.  Returns the chosen lane;
+// every lane computes the same result and t.
+__device__ __forceinline__ int warp_descend32(float v, float &t)
+{
+    float s[6];
+    s[0] = v;
+#pragma unroll
+    for (int l = 0; l < 5; ++l) s[l + 1] = __fadd_rn(s[l], __shfl_xor_sync(0xffffffffu, s[l], 1 << l));
+    int base = 0;
+#pragma unroll
+    for (int l = 4; l >= 0; --l) {
+        const float left = __shfl_sync(0xffffffffu, s[l], base);
+        const float right = __shfl_sync(0xffffffffu, s[l], base + (1 << l));
+        if (!(t < left || !(right > 0.0f))) {
+            t = __fsub_rn(t, left);
+            base += 1 << l;
+        }
+    }
+    return base;
+}
+
+// The row's emitted tokens: draft[b][0..js-1], then tok, then -1 pads.
+__device__ __forceinline__ void write_row(int32_t *out_tok, int32_t *out_cnt, const int32_t *draft, int b, int k,
+                                          int js, int tok)
+{
+    for (int jj = 0; jj <= k; ++jj)
+        out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? tok : -1);
+    out_cnt[b] = js + 1;
+}
+
+// Scan leaf `leaf` of the chosen position with the remaining t (one warp):
+// lanes e and e + 16 form entry e's weight exactly as in the leaf sums, the
+// entries are scanned in order; the first whose running sum exceeds t is the
+// token (fallback: the last entry of the leaf with a positive weight).
+__device__ int scan_leaf(const float *pv, const float *qv, bool resid, int V, int leaf, float c, float mzp, float Fp,
+                         float mzq, float Fq, float t)
+{
+    const int lane = threadIdx.x & 31;
+    const int x = kLeaf * leaf + (lane & 15);
+    const bool present = x < V;
+    const float lp = present ? __ldcg(pv + x) : -INFINITY;
+    float we = __fmul_rn(exp2_canon(__fmaf_rn(lp, c, -mzp)), Fp);
+    if (resid) {
+        const float lq = present ? __ldcg(qv + x) : -INFINITY;
+        const float d = __fsub_rn(we, __fmul_rn(exp2_canon(__fmaf_rn(lq, c, -mzq)), Fq));
+        we = d > 0.0f ? d : 0.0f;
+    }
+    if (!present) we = 0.0f;
+    int pk = -1;
+    float run = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLeaf; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, we, i);
+        const int xi = kLeaf * leaf + i;
+        if (xi < V && pk < 0) {
+            run = __fadd_rn(run, wi);
+            if (t < run) pk = xi;
+        }
+    }
+#pragma unroll
+    for (int i = kLeaf - 1; i >= 0; --i) {
+        const float wi = __shfl_sync(0xffffffffu, we, i);
+        const int xi = kLeaf * leaf + i;
+        if (pk < 0 && xi < V && wi > 0.0f) pk = xi;
+    }
+    return pk;
+}
+
+// Choose one of the 64 leaves of segment sg from this lane's pair of leaf
+// sums (leaves 2 l and 2 l + 1): the pairwise tree over the lanes' pairs,
+// then the pair; returns the global leaf index and updates t.
+__device__ __forceinline__ int descend_segment(float2 lpair, int sg, float &t)
+{
+    const int pstar = warp_descend32(__fadd_rn(lpair.x, lpair.y), t);
+    const float left = __shfl_sync(0xffffffffu, lpair.x, pstar), right = __shfl_sync(0xffffffffu, lpair.y, pstar);
+    int leaf = kLeavesPerSeg * sg + 2 * pstar;
+    if (!(t < left || !(right > 0.0f))) {
+        t = __fsub_rn(t, left);
+        leaf += 1;
+    }
+    return leaf;
+}
+
+// A draw from p of one target vector by the recipe's two-level rule (one warp;
+// every lane returns the token): segment weights W = RN(s_seg F_seg) from the
+// segment maxima and sums of the (max, sum) pass, the pairwise tree over the
+// (up to 512) segments with 16 consecutive segments per lane, t = RN(u R);
+// then the chosen segment's 64 leaf sums of p, its leaf tree and the scan of
+// the chosen leaf.
+__device__ int sample_p_warp(const float *pv, int V, const float *smz, const float *ssum, int NSP, float c, float M,
+                             float invS, float u)
+{
+    const int lane = threadIdx.x & 31;
+    float w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int sg = 16 * lane + i;
+        w[i] = 0.0f;
+        if (sg < NSP && sg * kSeg < V) w[i] = __fmul_rn(__ldcg(ssum + sg), seg_factor(__ldcg(smz + sg), M, invS));
+    }
+    float n[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) n[i] = w[i];
+#pragma unroll
+    for (int wd = 1; wd < 16; wd <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; i += 2 * wd) n[i] = __fadd_rn(n[i], n[i + wd]);
+    const float root = warp_tree_sum(n[0], 5);
+    float t = __fmul_rn(u, root);
+    const int lstar = warp_descend32(n[0], t);
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float x = __shfl_sync(0xffffffffu, w[i], lstar);
+        if (lane == i) mine = x;
+    }
+    const int sg = 16 * lstar + warp_descend32(mine, t);   // lanes 16..31 hold zeros
+    const float mz = __ldcg(smz + sg);
+    const float F = seg_factor(mz, M, invS);
+    const int x0 = sg * kSeg + 32 * lane;
+    float l[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) l[i] = x0 + i < V ? __ldcg(pv + x0 + i) : -INFINITY;
+    const float2 lpair = lane_leaf_sums(l, l, false, c, mz, F, 0.0f, 0.0f);
+    const int leaf = descend_segment(lpair, sg, t);
+    return scan_leaf(pv, pv, false, V, leaf, c, mz, F, 0.0f, 0.0f, t);
+}
+
+// ---- pass A: warp w of CTA (x, v, b) reduces segments 2 g and 2 g + 1
+// (g = kWarpsS x + w) of vector v of row b; the last warp of the row decides.
+__global__ void __launch_bounds__(kThreadsS, kSampleCtas)
 sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int al, const uint64_t *__restrict__ seeds, uint64_t round,
                 unsigned int *__restrict__ counters, unsigned int *__restrict__ vcount, float2 *__restrict__ part,
-                float *__restrict__ segmax, float2 *__restrict__ roots, SampleRec *__restrict__ rec,
+                float *__restrict__ segmax, float *__restrict__ segsum, float2 *__restrict__ roots,
+                SampleRec *__restrict__ rec, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
                 unsigned int *status)
 {
     // the resample pass may be scheduled now; it waits (griddepcontrol.wait) for
     // this grid to complete before reading anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(128) float smem_s[];
-    const int NBK = gridDim.x, blk = blockIdx.x, v = blockIdx.y, b = blockIdx.z;
-    const int NV = 2 * k + 1, NSP = NBK * kSegPerBlock, NW = NBK * kWarpsS;
+    const int v = blockIdx.y, b = blockIdx.z;
+    const int NV = 2 * k + 1, NW = gridDim.x * kWarpsS, NSP = 2 * NW;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blk * kWarpsS + warp;
+    const int g = blockIdx.x * kWarpsS + warp;
     float *buf = smem_s + warp * 2 * kSeg;
     // vectors 0..k: target positions 0..k; k+1..2k: draft positions 0..k-1
     const float *vec = v <= k ? tlog + (static_cast<size_t>(b) * (k + 1) + v) * V
                               : dlog + (static_cast<size_t>(b) * k + (v - k - 1)) * V;
     float *segm = segmax + (static_cast<size_t>(b) * NV + v) * NSP;
+    float *segs = segsum + (static_cast<size_t>(b) * NV + v) * NSP;
     bool last;
     {
 #pragma unroll
@@ -397,7 +565,10 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                 float l[32];
                 read_lane(buf + i * kSeg, np, l);
                 seg[i] = segment_ms(l, np, c, finite);
-                if (lane == 0) segm[sg] = seg[i].m;
+                if (lane == 0) {
+                    segm[sg] = seg[i].m;
+                    segs[sg] = seg[i].s;
+                }
             }
         }
         if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
@@ -465,8 +636,18 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         }
     }
     const unsigned int rej = __ballot_sync(0xffffffffu, reject);
+    const int js = rej ? __ffs(rej) - 1 : k;
+    if (js == k) {
+        // every draft accepted: the bonus token from p_k is drawn here (the
+        // segment weights come from this pass), and the resample pass skips the row
+        const RowRoots rk = root_of(k);
+        const int pk = sample_p_warp(tlog + (static_cast<size_t>(b) * (k + 1) + k) * V, V,
+                                     segrow + static_cast<size_t>(k) * NSP,
+                                     segsum + (static_cast<size_t>(b) * NV + k) * NSP, NSP, c, rk.M, rk.inv_s,
+                                     philox_uniform(seed, static_cast<uint32_t>(k), 2u, round));
+        if (lane == 0) write_row(out_tok, out_cnt, draft, b, k, k, pk);
+    }
     if (lane == 0) {
-        const int js = rej ? __ffs(rej) - 1 : k;
         const RowRoots rp = root_of(js);
         SampleRec r;
         r.js = js;
@@ -482,61 +663,10 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
             r.Mq = 0.0f;
             r.invSq = 0.0f;
         }
-        r.pad = 0;
+        r.done = js == k;
         rec[b] = r;
         counters[b] = 0;   // ready for the next call
     }
-}
-
-// Sampling weights of a lane's 32 entries of row b's chosen position,
-// max(0, RN(p - q)) (resid) or p, with p = RN(e2(t_p) Fp); returns the two
-// leaf sums (entries 0..15 and 16..31).
-__device__ __forceinline__ float2 lane_leaf_sums(const float (&lp)[32], const float (&lq)[32], bool resid,
-                                                 float c, float mzp, float Fp, float mzq, float Fq)
-{
-    const unsigned long long c2 = f2_pack(c, c), nmzp = f2_pack(-mzp, -mzp), nmzq = f2_pack(-mzq, -mzq);
-    unsigned long long eo[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int i = 16 * h + 2 * p;
-            const float2 ep = exp2_canon_x2(f2_fma(f2_pack(lp[i], lp[i + 1]), c2, nmzp));
-            float w0 = __fmul_rn(ep.x, Fp), w1 = __fmul_rn(ep.y, Fp);
-            if (resid) {
-                const float2 eq = exp2_canon_x2(f2_fma(f2_pack(lq[i], lq[i + 1]), c2, nmzq));
-                const float d0 = __fsub_rn(w0, __fmul_rn(eq.x, Fq)), d1 = __fsub_rn(w1, __fmul_rn(eq.y, Fq));
-                w0 = d0 > 0.0f ? d0 : 0.0f;
-                w1 = d1 > 0.0f ? d1 : 0.0f;
-            }
-            eo[h] = p == 0 ? f2_pack(w0, w1) : f2_add(eo[h], f2_pack(w0, w1));
-        }
-    }
-    return make_float2(pair_sum(eo[0]), pair_sum(eo[1]));
-}
-
-// Descend the pairwise sum tree over 32 leaves held one per lane (index =
-// lane; pads are zeros).  Level sums are formed as left + right by xor
-// shuffles (fp addition commutes exactly); at each level go left if t < left
-// or the right sum is not positive, else t -= left.  Returns the chosen lane;
-// every lane computes the same result and t.
-__device__ __forceinline__ int warp_descend32(float v, float &t)
-{
-    float s[6];
-    s[0] = v;
-#pragma unroll
-    for (int l = 0; l < 5; ++l) s[l + 1] = __fadd_rn(s[l], __shfl_xor_sync(0xffffffffu, s[l], 1 << l));
-    int base = 0;
-#pragma unroll
-    for (int l = 4; l >= 0; --l) {
-        const float left = __shfl_sync(0xffffffffu, s[l], base);
-        const float right = __shfl_sync(0xffffffffu, s[l], base + (1 << l));
-        if (!(t < left || !(right > 0.0f))) {
-            t = __fsub_rn(t, left);
-            base += 1 << l;
-        }
-    }
-    return base;
 }
 
 // Leaf sums of segment sg of row b's chosen position from its staged entries
@@ -565,14 +695,15 @@ __device__ __forceinline__ float segment_leaf_sums(const float *pbuf, const floa
     return warp_tree_sum(__fadd_rn(ls.x, ls.y), 5);
 }
 
-// ---- pass B: warp w of CTA (x, b) forms the leaf sums of segment 8 x + w of
+// ---- pass B: warp w of CTA (x, b) forms the leaf sums of segment kWarpsS x + w of
 // row b's chosen position; the last warp of the row descends the sum tree
 // and writes the row's tokens.
-__global__ void __launch_bounds__(kThreads, kSampleCtas)
+__global__ void __launch_bounds__(kThreadsS, kSampleCtas)
 sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int al, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
                 unsigned int *__restrict__ counters, const SampleRec *__restrict__ rec,
-                const float *__restrict__ segmax, float *__restrict__ ssum, float *__restrict__ lsum)
+                const float *__restrict__ segmax, const float *__restrict__ segsum, float *__restrict__ ssum,
+                float *__restrict__ lsum)
 {
     // launched as a programmatic dependent of the decision pass: wait for that
     // grid to complete (its records and partials visible) before anything else
@@ -583,6 +714,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const int sg = blockIdx.x * kWarpsS + warp;
     float *pbuf = smem_s + warp * 2 * kSeg, *qbuf = pbuf + kSeg;
     const SampleRec R = rec[b];
+    if (R.done) return;                                  // the bonus draw was taken in pass A
     const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + R.js) * V;
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
     const float *smp = segmax + (static_cast<size_t>(b) * NV + R.js) * NSP;
@@ -629,82 +761,36 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         return n[0];
     };
     float bval = lane < NBK ? block_total(lane) : 0.0f;
-    // all-zero residual (rounding): draw from p_js instead; this warp rebuilds
-    // every segment's leaf sums from p
-    if (resid && !(warp_tree_sum(bval, 5) > 0.0f)) {
-        resid = false;
-        for (int s2 = 0; s2 < NSP; ++s2) {
-            float ssv = 0.0f;
-            if (s2 * kSeg < V) {
-                stage_segment(pbuf, pv, V, s2 * kSeg, al);
-                cp_async_commit();
-                cp_async_wait<0>();
-                __syncwarp();
-                ssv = segment_leaf_sums(pbuf, pbuf, false, V, s2, c, R, smp, smq, lrow);
-                __syncwarp();
-            }
-            if (lane == 0) srow[s2] = ssv;
+    // all-zero residual (rounding): draw from p_js instead, by the two-level rule
+    const float root = warp_tree_sum(bval, 5);
+    if (resid && !(root > 0.0f)) {
+        const int pk = sample_p_warp(pv, V, smp, segsum + (static_cast<size_t>(b) * NV + R.js) * NSP, NSP, c, R.Mp,
+                                     R.invSp, R.u);
+        if (lane == 0) {
+            write_row(out_tok, out_cnt, draft, b, k, R.js, pk);
+            counters[b] = 0;
         }
-        __threadfence_block();
-        __syncwarp();
-        bval = lane < NBK ? block_total(lane) : 0.0f;
+        return;
     }
 
     // descent: blocks (32 lanes, zero pads), the chosen block's 16 segments,
     // the chosen segment's 64 leaves (pairs per lane, then the pair)
-    const float root = warp_tree_sum(bval, 5);
     float t = __fmul_rn(R.u, root);
     const int bstar = warp_descend32(bval, t);
     const float sval = lane < kSegPerBlock ? __ldcg(srow + kSegPerBlock * bstar + lane) : 0.0f;
     const int sstar = kSegPerBlock * bstar + warp_descend32(sval, t);
     const float2 lpair = __ldcg(reinterpret_cast<const float2 *>(lrow + kLeavesPerSeg * sstar) + lane);
-    const int pstar = warp_descend32(__fadd_rn(lpair.x, lpair.y), t);
-    const float left = __shfl_sync(0xffffffffu, lpair.x, pstar), right = __shfl_sync(0xffffffffu, lpair.y, pstar);
-    int lstar = kLeavesPerSeg * sstar + 2 * pstar;      // global leaf index
-    if (!(t < left || !(right > 0.0f))) {
-        t = __fsub_rn(t, left);
-        lstar += 1;
-    }
-
-    // the chosen leaf: lanes e and e + 16 reload entry e, the weights are
-    // formed exactly as in the leaf sums, then the entries are scanned in order
-    const int e = lane & 15;
-    const int x = kLeaf * lstar + e;
-    const bool present = x < V;
-    const float lp = present ? __ldcg(pv + x) : -INFINITY;
+    const int lstar = descend_segment(lpair, sstar, t);
     const float mzp = __ldcg(smp + sstar);
-    float we = __fmul_rn(exp2_canon(__fmaf_rn(lp, c, -mzp)), seg_factor(mzp, R.Mp, R.invSp));
+    const float Fp = seg_factor(mzp, R.Mp, R.invSp);
+    float mzq = 0.0f, Fq = 0.0f;
     if (resid) {
-        const float lq = present ? __ldcg(qv + x) : -INFINITY;
-        const float mzq = __ldcg(smq + sstar);
-        const float qe = __fmul_rn(exp2_canon(__fmaf_rn(lq, c, -mzq)), seg_factor(mzq, R.Mq, R.invSq));
-        const float d = __fsub_rn(we, qe);
-        we = d > 0.0f ? d : 0.0f;
+        mzq = __ldcg(smq + sstar);
+        Fq = seg_factor(mzq, R.Mq, R.invSq);
     }
-    if (!present) we = 0.0f;
-    int pk = -1;
-    float run = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kLeaf; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, we, i);
-        const int xi = kLeaf * lstar + i;
-        if (xi < V && pk < 0) {
-            run = __fadd_rn(run, wi);
-            if (t < run) pk = xi;
-        }
-    }
-    // fallback: the last entry of the leaf with a positive weight
-#pragma unroll
-    for (int i = kLeaf - 1; i >= 0; --i) {
-        const float wi = __shfl_sync(0xffffffffu, we, i);
-        const int xi = kLeaf * lstar + i;
-        if (pk < 0 && xi < V && wi > 0.0f) pk = xi;
-    }
+    const int pk = scan_leaf(pv, qv, resid, V, lstar, c, mzp, Fp, mzq, Fq, t);
     if (lane == 0) {
-        const int js = R.js;
-        for (int jj = 0; jj <= k; ++jj)
-            out_tok[static_cast<size_t>(b) * (k + 1) + jj] = jj < js ? draft[static_cast<size_t>(b) * k + jj] : (jj == js ? pk : -1);
-        out_cnt[b] = js + 1;
+        write_row(out_tok, out_cnt, draft, b, k, R.js, pk);
         counters[b] = 0;
     }
 }
@@ -726,9 +812,10 @@ cudaError_t allow_sampling_smem()
     return e;
 }
 
+// k = 0 only for the draft argmax (no drafts, one position per row).
 nq_status check_accept(int B, int k, int V, const void *ws, size_t ws_bytes)
 {
-    if (B < 1 || B > 65535 || k < 1 || k > kMaxK || V < 1 || V > kMaxChunks * kChunk) return NQ_ERR_ARG;
+    if (B < 1 || B > 65535 || k < 0 || k > kMaxK || V < 1 || V > kMaxChunks * kChunk) return NQ_ERR_ARG;
     if (!ws) return NQ_ERR_ARG;
     if (!aligned16(ws)) return NQ_ERR_ALIGN;
     if (ws_bytes < ws_layout(B, k, V).total) return NQ_ERR_WORKSPACE;
@@ -740,7 +827,7 @@ nq_status check_accept(int B, int k, int V, const void *ws, size_t ws_bytes)
 
 extern "C" size_t spec_accept_workspace_bytes(int B, int k, int V)
 {
-    if (B < 1 || B > 65535 || k < 1 || k > nq::kMaxK || V < 1 || V > nq::kMaxChunks * nq::kChunk) return 0;
+    if (B < 1 || B > 65535 || k < 0 || k > nq::kMaxK || V < 1 || V > nq::kMaxChunks * nq::kChunk) return 0;
     return nq::ws_layout(B, k, V).total;
 }
 
@@ -748,6 +835,7 @@ extern "C" nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_l
                                         int32_t *out_tok, int32_t *out_cnt, void *ws, size_t ws_bytes,
                                         cudaStream_t stream)
 {
+    if (k < 1) return NQ_ERR_ARG;
     nq_status st = nq::check_accept(B, k, V, ws, ws_bytes);
     if (st != NQ_OK) return st;
     if (!draft || !tgt_logits || !out_tok || !out_cnt) return NQ_ERR_ARG;
@@ -758,7 +846,26 @@ extern "C" nq_status spec_accept_greedy(const int32_t *draft, const float *tgt_l
     const nq::WsLayout L = nq::ws_layout(B, k, V);
     char *w = static_cast<char *>(ws);
     dim3 grid(nq::n_greedy_chunks(V), k + 1, B);
-    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
+    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, k + 1, out_cnt,
+                                                         reinterpret_cast<unsigned int *>(w + L.counters_a),
+                                                         reinterpret_cast<float2 *>(w + L.part), status);
+    return nq::cuda_status(cudaGetLastError());
+}
+
+extern "C" nq_status spec_draft_argmax(const float *logits, int M, int V, int32_t *tok, int tok_stride, void *ws,
+                                       size_t ws_bytes, cudaStream_t stream)
+{
+    // the greedy kernel with no drafts: t_0 = argmax of each row, emitted alone
+    nq_status st = nq::check_accept(M, 0, V, ws, ws_bytes);
+    if (st != NQ_OK) return st;
+    if (!logits || !tok || tok_stride < 1) return NQ_ERR_ARG;
+    if (!nq::aligned16(logits) || (reinterpret_cast<uintptr_t>(tok) & 3u) != 0) return NQ_ERR_ALIGN;
+    unsigned int *status = nq::device_status_ptr();
+    if (!status) return NQ_ERR_CUDA;
+    const nq::WsLayout L = nq::ws_layout(M, 0, V);
+    char *w = static_cast<char *>(ws);
+    dim3 grid(nq::n_greedy_chunks(V), 1, M);
+    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(nullptr, logits, 0, V, tok, tok_stride, nullptr,
                                                          reinterpret_cast<unsigned int *>(w + L.counters_a),
                                                          reinterpret_cast<float2 *>(w + L.part), status);
     return nq::cuda_status(cudaGetLastError());
@@ -769,6 +876,7 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
                                         uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
                                         size_t ws_bytes, cudaStream_t stream)
 {
+    if (k < 1) return NQ_ERR_ARG;
     nq_status st = nq::check_accept(B, k, V, ws, ws_bytes);
     if (st != NQ_OK) return st;
     if (!(temperature > 0.0f) || !(temperature < INFINITY)) return NQ_ERR_ARG;
@@ -787,11 +895,13 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     // 16-byte boundary (V % 4 == 0; the pointers are 16-byte aligned)
     const int al = (V % 4) == 0 ? 1 : 0;
     if (nq::allow_sampling_smem() != cudaSuccess) return NQ_ERR_CUDA;
-    dim3 grid_a(nq::n_blocks(V), 2 * k + 1, B);
-    nq::sample_a_kernel<<<grid_a, nq::kThreads, nq::kSmemS, stream>>>(
+    const int nsp = nq::n_segments_padded(V);
+    dim3 grid_a(nsp / (2 * nq::kWarpsS), 2 * k + 1, B);   // one warp per segment pair
+    nq::sample_a_kernel<<<grid_a, nq::kThreadsS, nq::kSmemS, stream>>>(
         draft, draft_logits, tgt_logits, k, V, c, al, seeds, round, reinterpret_cast<unsigned int *>(w + L.counters_a),
         reinterpret_cast<unsigned int *>(w + L.vcount), reinterpret_cast<float2 *>(w + L.part), segmax,
-        reinterpret_cast<float2 *>(w + L.roots), rec, status);
+        reinterpret_cast<float *>(w + L.segsum), reinterpret_cast<float2 *>(w + L.roots), rec, out_tok, out_cnt,
+        status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return NQ_ERR_CUDA;
     // pass B as a programmatic dependent launch when pass A fills the GPU: its
@@ -801,8 +911,8 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     // the dependent launch); griddepcontrol.wait returns at once then.
     const bool dependent = static_cast<long long>(grid_a.x) * grid_a.y * grid_a.z >= nq::sm_count();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nq::n_segments_padded(V) / nq::kWarpsS, B);   // one warp per segment
-    cfg.blockDim = dim3(nq::kThreads);
+    cfg.gridDim = dim3(nsp / nq::kWarpsS, B);   // one warp per segment
+    cfg.blockDim = dim3(nq::kThreadsS);
     cfg.dynamicSmemBytes = nq::kSmemS;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -812,8 +922,8 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     cfg.numAttrs = dependent ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, al, out_tok, out_cnt,
                            reinterpret_cast<unsigned int *>(w + L.counters_b), static_cast<const nq::SampleRec *>(rec),
-                           static_cast<const float *>(segmax), reinterpret_cast<float *>(w + L.ssum),
-                           reinterpret_cast<float *>(w + L.lsum));
+                           static_cast<const float *>(segmax), static_cast<const float *>(reinterpret_cast<float *>(w + L.segsum)),
+                           reinterpret_cast<float *>(w + L.ssum), reinterpret_cast<float *>(w + L.lsum));
     return nq::cuda_status(e);
 }
 
@@ -871,7 +981,7 @@ extern "C" nq_status spec_accept_greedy_noalloc(const int32_t *draft, const floa
     // the per-row tickets must start at zero; the partials are overwritten
     if (cudaMemsetAsync(scratch, 0, counters, stream) != cudaSuccess) return NQ_ERR_CUDA;
     dim3 grid(nq::n_greedy_chunks(V), k + 1, B);
-    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, out_cnt,
+    nq::greedy_kernel<<<grid, nq::kThreads, 0, stream>>>(draft, tgt_logits, k, V, out_tok, k + 1, out_cnt,
                                                          reinterpret_cast<unsigned int *>(scratch),
                                                          reinterpret_cast<float2 *>(scratch + counters), status);
     return nq::cuda_status(cudaGetLastError());

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libnq.so")
 
 NQ_OK, NQ_ERR_ARG, NQ_ERR_SHAPE, NQ_ERR_ALIGN, NQ_ERR_CUDA = 0, 1, 2, 3, 4
 NQ_ERR_NONFINITE, NQ_ERR_TIMEOUT, NQ_ERR_WORKSPACE, NQ_ERR_TOKEN = 5, 6, 7, 8
-NQ_DEV_NONFINITE, NQ_DEV_BAD_TOKEN, NQ_DEV_TIMEOUT, NQ_DEV_ACT_RANGE = 0x1, 0x2, 0x4, 0x8
+NQ_DEV_NONFINITE, NQ_DEV_BAD_TOKEN, NQ_DEV_TIMEOUT, NQ_DEV_ACT_RANGE, NQ_DEV_SEQ_FULL = 0x1, 0x2, 0x4, 0x8, 0x10
 FMT_NESTED44, FMT_INT4, FMT_FP8E4M3_ROW, FMT_FP16 = 0, 1, 2, 3
 
 _lock = threading.Lock()
@@ -67,6 +67,12 @@ def lib():
             L.nq_status_string.argtypes = [i32]
             L.nq_status_string.restype = C.c_char_p
             L.nq_get_device_status.argtypes = [vp, C.POINTER(C.c_uint32)]
+            L.spec_draft_argmax.argtypes = [vp, i32, i32, vp, i32, vp, sz, vp]
+            L.nq_embed_rows.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp]
+            L.nq_embed_round.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp]
+            L.spec_round_commit.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, vp]
+            for name in ("spec_draft_argmax", "nq_embed_rows", "nq_embed_round", "spec_round_commit"):
+                getattr(L, name).restype = i32
             L.nq_selftest_bounded_wait.argtypes = [C.c_uint32, vp]
             L.nq_selftest_bounded_wait.restype = i32
             for name in ("nq_packed_bytes", "nq_pack_weights", "nq_draft_gemv", "nq_verify_gemm",
@@ -261,6 +267,48 @@ def accept_sample(draft: torch.Tensor, draft_logits: torch.Tensor, tgt_logits: t
                                     _dev(out_cnt, torch.int32, "out_cnt"), _dev(ws, torch.uint8, "ws"), ws.numel(),
                                     _stream(stream)), "spec_accept_sample")
     return out_tok, out_cnt
+
+
+# ---------------------------------------------------------------- round bookkeeping
+def draft_argmax(logits: torch.Tensor, tok: torch.Tensor, tok_stride: int = 1, ws: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """tok[m * tok_stride] = argmax of logits row m (fp32 [M][V]); tok is an
+    int32 tensor viewed flat (it may be a strided slice's base)."""
+    M, V = logits.shape
+    ws = ws if ws is not None else accept_workspace(M, 0, V, logits.device)
+    _check(lib().spec_draft_argmax(_dev(logits, torch.float32, "logits"), M, V, tok.data_ptr(), int(tok_stride),
+                                   _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "spec_draft_argmax")
+    return tok
+
+
+def embed_rows(table: torch.Tensor, ids: torch.Tensor, M: int, ids_stride: int = 1, out=None, stream=None):
+    """out[m] = table[ids[m * ids_stride]] (table bf16 [V][d]); ids int32."""
+    V, d = table.shape
+    out = out if out is not None else torch.empty((M, d), dtype=torch.bfloat16, device=table.device)
+    _check(lib().nq_embed_rows(_dev(table, torch.bfloat16, "table"), V, d, ids.data_ptr(), int(ids_stride), M,
+                               _dev(out, torch.bfloat16, "out"), _stream(stream)), "nq_embed_rows")
+    return out
+
+
+def embed_round(table: torch.Tensor, x0: torch.Tensor, draft: Optional[torch.Tensor], B: int, k: int, out=None,
+                stream=None):
+    """The verify rows of a round: out[b][0] = table[x0[b]], out[b][j] = table[draft[b][j-1]]."""
+    V, d = table.shape
+    out = out if out is not None else torch.empty((B * (k + 1), d), dtype=torch.bfloat16, device=table.device)
+    _check(lib().nq_embed_round(_dev(table, torch.bfloat16, "table"), V, d, x0.data_ptr(),
+                                None if draft is None else draft.data_ptr(), B, k, _dev(out, torch.bfloat16, "out"),
+                                _stream(stream)), "nq_embed_round")
+    return out
+
+
+def round_commit(out_tok: torch.Tensor, out_cnt: torch.Tensor, seq: torch.Tensor, seq_len: torch.Tensor,
+                 x0: torch.Tensor, stream=None) -> None:
+    """Append the emitted tokens to seq [B][max_len] (int32), advance seq_len,
+    set x0 to each row's last emitted token (all in place, on the device)."""
+    B, k1 = out_tok.shape
+    _check(lib().spec_round_commit(_dev(out_tok, torch.int32, "out_tok"), _dev(out_cnt, torch.int32, "out_cnt"), B,
+                                   k1 - 1, _dev(seq, torch.int32, "seq"), _dev(seq_len, torch.int32, "seq_len"),
+                                   seq.shape[1], _dev(x0, torch.int32, "x0"), _stream(stream)), "spec_round_commit")
 
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> None:

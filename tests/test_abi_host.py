@@ -56,8 +56,8 @@ def test_workspace_bytes(L):
     from quantized_self_speculative_gb300 import nq
     # sections, each starting on a 256-byte boundary: two ticket arrays,
     # (2k+1) partials per row of max(4096-entry chunks, 2048-entry segment
-    # pairs), a 32-B decision record per row, one maximum per 1024-entry
-    # segment (16 per 16384-entry block) per vector per row, one sum per
+    # pairs), a 32-B decision record per row, one maximum and one sum per
+    # 1024-entry segment (16 per 16384-entry block) per vector per row, one sum per
     # segment per row, 64 leaf sums per segment per row, a ticket and a root
     # (max, 1/sum) per vector per row
     a = lambda n: (n + 255) // 256 * 256
@@ -65,13 +65,15 @@ def test_workspace_bytes(L):
     def expect(B, k, V):
         C, NSP, NV = -(-V // 4096), 16 * -(-V // 16384), 2 * k + 1
         P = max(C, NSP // 2)
-        return (a(4 * B) * 2 + a(B * NV * P * 8) + a(32 * B) + a(B * NV * NSP * 4)
+        return (a(4 * B) * 2 + a(B * NV * P * 8) + a(32 * B) + 2 * a(B * NV * NSP * 4)
                 + a(4 * B * NSP) + a(256 * B * NSP) + a(4 * B * NV) + 8 * B * NV)
 
-    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 4070656
-    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 6984
+    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 4766976
+    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 7752
     assert nq.workspace_bytes(3, 16, 4099) == expect(3, 16, 4099)
-    for bad in [(0, 4, 10), (1, 0, 10), (1, 17, 10), (1, 4, 0), (1, 4, 524289), (65536, 1, 1)]:
+    # k = 0 sizes the draft argmax's workspace (no drafts, one position per row)
+    assert nq.workspace_bytes(5, 0, 32000) == expect(5, 0, 32000) > 0
+    for bad in [(0, 4, 10), (1, -1, 10), (1, 17, 10), (1, 4, 0), (1, 4, 524289), (65536, 1, 1)]:
         assert nq.workspace_bytes(*bad) == 0
 
 

@@ -266,3 +266,33 @@ def test_canonical_round_agrees_with_fp64_round_sweep_shape(k, noise):
         differ = np.any(out != out64, axis=1) | (cnt != cnt64)
         assert np.all(margin[differ] < 1e-5)
         assert differ.sum() == 0
+
+
+@pytest.mark.parametrize("V", [1, 5, 1023, 1024, 1025, 4096, 40000, 152064])
+def test_sample_p_is_inverse_cdf_of_softmax(V):
+    """The bonus draw's two-level rule (segment weights from the (max, sum)
+    pass, then the chosen segment's leaves) picks the textbook fp64 inverse
+    CDF of softmax(l / T) over the vocabulary in index order, except where
+    u * total lies within fp32 rounding (1e-6 of the total) of a boundary."""
+    g = synth.rng(700 + V)
+    l = (g.standard_normal(V) * 3.0).astype(np.float32)
+    for T in (1.0, 0.7):
+        cdf = np.cumsum(softmax64(l, T))
+        us = g.random(60).astype(np.float32)
+        checked = 0
+        for u in us:
+            got = O.sample_p(l, T, float(u))
+            t = float(u) * cdf[-1]
+            if np.min(np.abs(cdf - t)) < 1e-6:
+                continue
+            assert got == int(np.searchsorted(cdf, t, side="right")), (V, T, u)
+            checked += 1
+        assert checked >= 50
+
+
+def test_sample_p_extremes_and_underflow():
+    l = np.array([0.0, -1000.0, 3.0, -500.0, 3.0], np.float32)
+    assert O.sample_p(l, 1.0, 0.0) == 0                       # u = 0: the first entry with p > 0
+    assert O.sample_p(l, 1.0, float(np.float32(1 - 2**-24))) == 4   # the last entry with p > 0
+    draws = {O.sample_p(l, 1.0, float(u)) for u in np.linspace(0, 0.999, 400, dtype=np.float32)}
+    assert draws <= {0, 2, 4}                                  # underflowed entries are never drawn
