@@ -234,6 +234,24 @@ NQ_API nq_status spec_accept_sample(const int32_t *draft, const float *draft_log
                              size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * spec_accept_sample plus the draft features SpecKV feeds its acceptance-rate
+ * predictor (SpecKV, "How it works": mean and maximum draft entropy, mean and
+ * minimum draft confidence over a step's drafted positions), taken from the
+ * same pass over the draft logits at no extra read:
+ *   features[b] = (mean_j H(q_j), mean_j q_j(d_j), max_j H(q_j), min_j q_j(d_j)),
+ * j = 0..k-1, H in nats of q_j = softmax(draft_logits[b][j] / T), q_j(d_j)
+ * the drafted token's draft probability (its canonical fp32 value, the one the
+ * acceptance test uses).  features: fp32 [B][4] device, 16-byte aligned.
+ * Token outputs are bit-identical to spec_accept_sample's; the features are
+ * floating-point values, accurate to about 1e-5 relative.
+ */
+NQ_API nq_status spec_accept_sample_features(const int32_t *draft, const float *draft_logits,
+                                             const float *tgt_logits, int B, int k, int V, float temperature,
+                                             const uint64_t *seeds, uint64_t round, int32_t *out_tok,
+                                             int32_t *out_cnt, float *features, void *ws, size_t ws_bytes,
+                                             cudaStream_t stream);
+
+/*
  * Round bookkeeping ("Drafting and checking tokens": the draft proposes k
  * tokens one at a time, each from the previous one; the target checks the
  * k+1 positions in one pass; the kept prefix plus the target's token extend
@@ -278,6 +296,59 @@ NQ_API nq_status nq_embed_round(const uint16_t *table, int V, int d, const int32
  */
 NQ_API nq_status spec_round_commit(const int32_t *out_tok, const int32_t *out_cnt, int B, int k, int32_t *seq,
                                    int32_t *seq_len, int max_len, int32_t *x0, cudaStream_t stream);
+
+/*
+ * The nested KV cache (BitNest, Fig. 4 "KV nesting during speculative
+ * decoding": the draft stage reads only the low-bit base view of the cache,
+ * verification reads the full b_kv + r_kv-bit view of the same cache, the
+ * accepted entries stay and the rejected suffix is discarded).  One layer:
+ * for each of `batch` sequences and `heads_kv` heads, `max_len` rows of
+ * `head_dim` values (64 or 128); each K or V row is quantised like a NESTED44
+ * weight row, in groups of `group` (64 or 128, <= head_dim) values along the
+ * head dimension: base and refinement planes uint8
+ * [batch][heads_kv][max_len][head_dim/2], scales fp16
+ * [batch][heads_kv][max_len][head_dim/group].  An element's draft value is
+ * s q4 (4-bit view), its target value (s/16)(16 q4 + r) (8-bit view).  The
+ * struct is host memory; the six buffers are caller-owned device memory
+ * (sizes from nq_kv_cache_bytes), 16-byte aligned.  Discarding a rejected
+ * suffix is only a length: rows at or beyond a sequence's length are never read.
+ */
+typedef struct {
+    int32_t batch, heads_kv, head_dim, group, max_len, pad;
+    void *k_base, *k_resid, *k_scales;
+    void *v_base, *v_resid, *v_scales;
+} nq_kv_cache;
+
+/* Bytes of one plane buffer and of one scale buffer (host-only). */
+NQ_API nq_status nq_kv_cache_bytes(int batch, int heads_kv, int head_dim, int group, int max_len,
+                                   size_t *plane_bytes, size_t *scale_bytes);
+
+/*
+ * Quantise and store n_new new K and V rows per (sequence, head) at rows
+ * pos[b] .. pos[b] + n_new - 1 (the positions a pass has just computed):
+ * k_new, v_new fp32 [batch][heads_kv][n_new][head_dim] (device, 16-byte
+ * aligned); pos int32 [batch] device.  Rows that would land at or beyond
+ * max_len are dropped and set NQ_DEV_SEQ_FULL.  Codes are bit-identical to
+ * nq_pack_weights' NESTED44 codes of the same rows.
+ */
+NQ_API nq_status nq_kv_append(const nq_kv_cache *cache, const float *k_new, const float *v_new, int n_new,
+                              const int32_t *pos, cudaStream_t stream);
+
+/*
+ * Decode attention of M new query rows per sequence over the nested cache:
+ *   out[b][m][h][:] = softmax_t(scale q[b][m][h] . K[b][kv(h)][t]) V[b][kv(h)][t]
+ * over rows t = 0 .. len[b] - M + m (causal: len[b] counts the M new rows,
+ * already appended), kv(h) = h / (heads_q / heads_kv) (grouped-query
+ * attention).  planes = 1 reads the 4-bit base view (draft), 2 both planes
+ * (the 8-bit target view).  q, out fp32 [batch][M][heads_q][head_dim]; len
+ * int32 [batch] device.  fp32 arithmetic (scores, exponentials, sums):
+ * agrees with an fp64 evaluation over the same dequantised rows to far
+ * inside the linears' 2e-3 normwise tolerance.  Workspace (caller-owned,
+ * no initialisation) of nq_attn_workspace_bytes() bytes; 0 on bad sizes.
+ */
+NQ_API size_t nq_attn_workspace_bytes(int batch, int M, int heads_q, int head_dim, int max_len);
+NQ_API nq_status nq_attn_decode(const nq_kv_cache *cache, const float *q, int M, int heads_q, const int32_t *len,
+                                int planes, float scale, float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Greedy acceptance that allocates nothing and takes no workspace: the same

@@ -77,6 +77,8 @@ def lib():
             L.orc_softmax_stats.argtypes = [vp, i32, f32, vp, vp, vp, vp]
             L.orc_draft_argmax.argtypes = [vp, i32, i32, vp]
             L.orc_sample_p.argtypes = [vp, i32, f32, f32]
+            L.orc_draft_features.argtypes = [vp, vp, i32, i32, i32, f32, vp]
+            L.orc_attn_decode.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32, f32, vp]
             L.orc_round_commit.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp]
             L.orc_f32_to_f16_n.argtypes = [vp, vp, i32]
             L.orc_f16_to_f32_n.argtypes = [vp, vp, i32]
@@ -345,3 +347,52 @@ def sample_p(logits, temperature: float, u: float) -> int:
     if r < 0:
         raise ValueError("non-finite logits")
     return r
+
+
+def draft_features(draft, draft_logits, temperature: float = 1.0):
+    """SpecKV's per-step draft features for each row: (mean entropy, mean
+    confidence, max entropy, min confidence) over the k drafted positions,
+    entropy in nats of softmax(draft_logits / T), confidence = the drafted
+    token's draft probability.  fp64 [B][4]."""
+    d = np.ascontiguousarray(draft, dtype=np.int32)
+    dl = np.ascontiguousarray(draft_logits, dtype=np.float32)
+    B, k, V = dl.shape
+    out = np.empty((B, 4), np.float64)
+    if lib().orc_draft_features(d.ctypes.data, dl.ctypes.data, B, k, V, float(temperature), out.ctypes.data) < 0:
+        raise ValueError("invalid draft tokens, logits or temperature")
+    return out
+
+
+# ------------------------------------------------------------------ nested KV cache
+# BitNest Fig. 4: the draft reads the low-bit base view of the cache, the
+# verification pass the full view.  Rows are quantised like NESTED44 weight
+# rows (pack_nested over head_dim, groups of G).
+
+def kv_rows_pack(rows, group: int):
+    """Quantise K or V rows fp32 [..., d] like NESTED44 weight rows: returns
+    (base, resid, scales) with the leading shape kept."""
+    r = np.ascontiguousarray(rows, dtype=np.float32)
+    lead, d = r.shape[:-1], r.shape[-1]
+    base, resid, scales = pack_nested(r.reshape(-1, d), group)
+    return (base.reshape(*lead, d // 2), resid.reshape(*lead, d // 2), scales.reshape(*lead, d // group))
+
+
+def attn_decode(q, cache, lens, planes: int, scale: float):
+    """fp64 attention of q [B][M][Hq][d] over the cache dict {k_base, k_resid,
+    k_scales, v_base, v_resid, v_scales} ([B][Hkv][L][...] arrays, scales as
+    fp16 bits) with lengths lens [B]; returns fp32 [B][M][Hq][d]."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    B, M, Hq, d = q.shape
+    kb = np.ascontiguousarray(cache["k_base"], dtype=np.uint8)
+    Hkv, L = kb.shape[1], kb.shape[2]
+    G = d // cache["k_scales"].shape[-1]
+    arrs = [np.ascontiguousarray(cache[n]) for n in ("k_resid", "k_scales", "v_base", "v_resid", "v_scales")]
+    arrs[1] = arrs[1].view(np.uint16)
+    arrs[4] = arrs[4].view(np.uint16)
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.empty_like(q)
+    if lib().orc_attn_decode(q.ctypes.data, B, M, Hq, Hkv, d, G, L, kb.ctypes.data, arrs[0].ctypes.data,
+                             arrs[1].ctypes.data, arrs[2].ctypes.data, arrs[3].ctypes.data, arrs[4].ctypes.data,
+                             ln.ctypes.data, int(planes), float(scale), out.ctypes.data) < 0:
+        raise ValueError("bad attention arguments")
+    return out

@@ -854,6 +854,106 @@ int orc_accept_sample_f64(const int32_t *draft, const float *draft_logits, const
 }
 
 /* ======================================================================== */
+/* Nested KV cache attention [BitNest Fig. 4: the draft reads the low-bit    */
+/* base view, verification the full view of the same cache].                */
+/* ======================================================================== */
+
+/* Element j of cache row `row` (head_dim d, group G): draft s q4, target
+ * (s/16)(16 q4 + r), in fp64 (exact). */
+static double kv_value(const uint8_t *base, const uint8_t *resid, const uint16_t *sc, size_t row, int d, int G,
+                       int j, int planes)
+{
+    uint8_t bb = base[row * (d / 2) + j / 2];
+    int q4 = (j & 1) ? (bb >> 4) : (bb & 15);
+    if (q4 > 7) q4 -= 16;
+    double s = (double)orc_f16_to_f32(sc[row * (d / G) + j / G]);
+    if (planes == 1) return s * q4;
+    uint8_t rb = resid[row * (d / 2) + j / 2];
+    int r = (j & 1) ? (rb >> 4) : (rb & 15);
+    if (r > 7) r -= 16;
+    return s / 16.0 * (16 * q4 + r);
+}
+
+/* out[b][m][h] = softmax_t(scale q . K_t) V_t over t = 0 .. len[b] - M + m,
+ * kv head h / (Hq / Hkv); plain fp64. */
+int orc_attn_decode(const float *q, int B, int M, int Hq, int Hkv, int d, int G, int L,
+                    const uint8_t *kb, const uint8_t *kr, const uint16_t *ks,
+                    const uint8_t *vb, const uint8_t *vr, const uint16_t *vs,
+                    const int32_t *len, int planes, float scale, float *out)
+{
+    if (Hq % Hkv != 0 || (planes != 1 && planes != 2)) return -1;
+    int g = Hq / Hkv;
+    double *w = malloc(sizeof(double) * (L > 0 ? L : 1));
+    for (int b = 0; b < B; b++)
+        for (int m = 0; m < M; m++)
+            for (int h = 0; h < Hq; h++) {
+                int kvh = h / g, lim = len[b] - (M - 1 - m);
+                if (lim > L) lim = L;
+                const float *qv = q + (((size_t)b * M + m) * Hq + h) * d;
+                float *o = out + (((size_t)b * M + m) * Hq + h) * d;
+                double mx = -INFINITY;
+                for (int t = 0; t < lim; t++) {
+                    size_t row = ((size_t)b * Hkv + kvh) * L + t;
+                    double sc = 0.0;
+                    for (int j = 0; j < d; j++) sc += (double)qv[j] * kv_value(kb, kr, ks, row, d, G, j, planes);
+                    w[t] = sc * scale;
+                    if (w[t] > mx) mx = w[t];
+                }
+                double den = 0.0;
+                for (int t = 0; t < lim; t++) { w[t] = exp(w[t] - mx); den += w[t]; }
+                for (int j = 0; j < d; j++) {
+                    double acc = 0.0;
+                    for (int t = 0; t < lim; t++) {
+                        size_t row = ((size_t)b * Hkv + kvh) * L + t;
+                        acc += w[t] * kv_value(vb, vr, vs, row, d, G, j, planes);
+                    }
+                    o[j] = lim > 0 ? (float)(acc / den) : 0.0f;
+                }
+            }
+    free(w);
+    return 0;
+}
+
+/* ======================================================================== */
+/* Draft features [SpecKV, "How it works": mean and maximum draft entropy,    */
+/* mean and minimum draft confidence over a step's drafted positions].       */
+/* ======================================================================== */
+
+/* Per row b: H_j = entropy (nats) of q_j = softmax(draft_logits[b][j] / T)
+ * and c_j = q_j(draft[b][j]) (the drafted token's probability under the
+ * draft) for j = 0..k-1; out[b] = (mean H, mean c, max H, min c).  Plain
+ * fp64 with libm exp and log. */
+int orc_draft_features(const int32_t *draft, const float *draft_logits, int B, int k, int V, float T, double *out)
+{
+    if (!(T > 0.0f) || k < 1 || V < 1) return -1;
+    double *q = malloc(sizeof(double) * V);
+    for (int b = 0; b < B; b++) {
+        double sh = 0.0, sc = 0.0, mh = -INFINITY, mc = INFINITY;
+        for (int j = 0; j < k; j++) {
+            const float *l = draft_logits + ((size_t)b * k + j) * V;
+            int d = draft[b * k + j];
+            if (d < 0 || d >= V) { free(q); return -1; }
+            double mx = -INFINITY, s = 0.0, h = 0.0;
+            for (int x = 0; x < V; x++) {
+                if (!isfinite(l[x])) { free(q); return -1; }
+                if ((double)l[x] / T > mx) mx = (double)l[x] / T;
+            }
+            for (int x = 0; x < V; x++) { q[x] = exp((double)l[x] / T - mx); s += q[x]; }
+            for (int x = 0; x < V; x++) {
+                q[x] /= s;
+                if (q[x] > 0.0) h -= q[x] * log(q[x]);
+            }
+            sh += h; sc += q[d];
+            if (h > mh) mh = h;
+            if (q[d] < mc) mc = q[d];
+        }
+        out[4 * b] = sh / k; out[4 * b + 1] = sc / k; out[4 * b + 2] = mh; out[4 * b + 3] = mc;
+    }
+    free(q);
+    return 0;
+}
+
+/* ======================================================================== */
 /* Array helpers so that callers need not loop per element.                 */
 /* ======================================================================== */
 void orc_exp2c_n(const float *t, float *out, int n) { for (int i = 0; i < n; i++) out[i] = orc_exp2c(t[i]); }

@@ -46,6 +46,11 @@ float orc_temper_coef(float T);
 int orc_softmax_canonical(const float *l, int V, float T, float *p);
 int orc_tree_sample(const float *w, int V, float u);
 int orc_sample_p(const float *l, int V, float T, float u);
+int orc_attn_decode(const float *q, int B, int M, int Hq, int Hkv, int d, int G, int L,
+                    const uint8_t *kb, const uint8_t *kr, const uint16_t *ks,
+                    const uint8_t *vb, const uint8_t *vr, const uint16_t *vs,
+                    const int32_t *len, int planes, float scale, float *out);
+int orc_draft_features(const int32_t *draft, const float *draft_logits, int B, int k, int V, float T, double *out);
 int orc_draft_argmax(const float *logits, int M, int V, int32_t *tok);
 int orc_round_commit(const int32_t *out_tok, const int32_t *out_cnt, int B, int k, int32_t *seq,
                      int32_t *seq_len, int max_len, int32_t *x0);

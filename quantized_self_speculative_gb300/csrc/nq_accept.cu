@@ -199,7 +199,7 @@ struct SampleRec {      // per-row decision, written by pass A, read by pass B
 
 // Workspace layout shared by the greedy and sampled calls.
 struct WsLayout {
-    size_t counters_a, counters_b, part, rec, segmax, segsum, ssum, lsum, vcount, roots, total;
+    size_t counters_a, counters_b, part, rec, segmax, segsum, ssum, lsum, vcount, roots, partu, ent, total;
 };
 
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
@@ -225,7 +225,9 @@ inline WsLayout ws_layout(int B, int k, int V)
     L.lsum = L.ssum + align256(static_cast<size_t>(B) * NSP * sizeof(float));         // per (row, segment)
     L.vcount = L.lsum + align256(static_cast<size_t>(B) * NSP * kLeavesPerSeg * sizeof(float));
     L.roots = L.vcount + align256(static_cast<size_t>(B) * NV * sizeof(unsigned int));  // per (row, vector)
-    L.total = L.roots + static_cast<size_t>(B) * NV * sizeof(float2);
+    L.partu = L.roots + align256(static_cast<size_t>(B) * NV * sizeof(float2));        // features: u per partial
+    L.ent = L.partu + align256(static_cast<size_t>(B) * NV * P * sizeof(float));       // features: entropy per vector
+    L.total = L.ent + static_cast<size_t>(B) * NV * sizeof(float);
     return L;
 }
 
@@ -318,14 +320,19 @@ __device__ __forceinline__ float warp_max(float m)
 // (mz, s) of one segment; every lane of the warp calls it with its 32 entries,
 // np of which are present.  `finite` becomes NaN if a present entry's
 // exponent t is not finite (a non-finite logit or segment maximum).
-__device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float c, float &finite)
+//
+// With FEAT it also returns u = sum of e2(t) t over the segment (t relative to
+// the segment maximum), from which the distribution's entropy follows; any
+// order of summation (a float feature, not a decision).
+template <bool FEAT = false>
+__device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float c, float &finite, float *u_out = nullptr)
 {
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 32; i += 2) mx = max3(mx, v[i], v[i + 1]);
     const float mz = __fmul_rn(warp_max(mx), c);
     const unsigned long long c2 = f2_pack(c, c), nmz = f2_pack(-mz, -mz), z2 = f2_pack(0.0f, 0.0f);
-    unsigned long long fin = z2, eo[2];
+    unsigned long long fin = z2, eo[2], uu = z2;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -334,8 +341,14 @@ __device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float
             fin = f2_fma(z2, t, fin);
             const float2 e = exp2_canon_x2(t);
             eo[h] = p == 0 ? f2_pack(e.x, e.y) : f2_add(eo[h], f2_pack(e.x, e.y));
+            if constexpr (FEAT) {
+                // absent entries: t = -inf, e = 0; count their product as 0
+                const float2 tv = f2_unpack(t);
+                uu = f2_fma(f2_pack(e.x, e.y), f2_pack(e.x > 0.0f ? tv.x : 0.0f, e.y > 0.0f ? tv.y : 0.0f), uu);
+            }
         }
     }
+    if constexpr (FEAT) *u_out = warp_tree_sum(pair_sum(uu), 5);
     if (np == 32) {
         const float2 f = f2_unpack(fin);
         finite = __fadd_rn(finite, __fadd_rn(f.x, f.y));
@@ -349,6 +362,19 @@ __device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float
 }
 
 struct RowRoots { float M, inv_s; };
+
+// (max, sum, u) merge for the entropy feature: the larger max survives, the
+// smaller node's sum and u are rescaled by f = e2(d), d = m_small - m_large,
+// and u also gains d s_small (its exponents move by d).  Pads: (-inf, 0, 0).
+struct MSU { float m, s, u; };
+__device__ __forceinline__ MSU msu_merge(MSU a, MSU b)
+{
+    const bool a_big = a.m >= b.m || b.m != b.m;
+    const MSU big = a_big ? a : b, sm = a_big ? b : a;
+    if (sm.m == -INFINITY) return big;
+    const float d = __fsub_rn(sm.m, big.m), f = exp2_canon(d);
+    return MSU{big.m, __fmaf_rn(sm.s, f, big.s), __fmaf_rn(__fmaf_rn(d, sm.s, sm.u), f, big.u)};
+}
 
 __device__ __forceinline__ float seg_factor(float mz_seg, float M, float inv_s)
 {
@@ -523,13 +549,18 @@ __device__ int sample_p_warp(const float *pv, int V, const float *smz, const flo
 
 // ---- pass A: warp w of CTA (x, v, b) reduces segments 2 g and 2 g + 1
 // (g = kWarpsS x + w) of vector v of row b; the last warp of the row decides.
+//
+// FEAT: the draft vectors also carry u through the same trees, and the last
+// warp of the row writes SpecKV's step features (mean and maximum draft
+// entropy, mean and minimum draft confidence q_j(d_j)) to feat[b][0..3].
+template <bool FEAT>
 __global__ void __launch_bounds__(kThreadsS, kSampleCtas)
 sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
                 int k, int V, float c, int al, const uint64_t *__restrict__ seeds, uint64_t round,
                 unsigned int *__restrict__ counters, unsigned int *__restrict__ vcount, float2 *__restrict__ part,
                 float *__restrict__ segmax, float *__restrict__ segsum, float2 *__restrict__ roots,
                 SampleRec *__restrict__ rec, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
-                unsigned int *status)
+                float *__restrict__ partu, float *__restrict__ ent, float *__restrict__ feat, unsigned int *status)
 {
     // the resample pass may be scheduled now; it waits (griddepcontrol.wait) for
     // this grid to complete before reading anything this grid writes
@@ -554,6 +585,8 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         }
         float finite = 0.0f;
         MaxSum seg[2];
+        float su[2] = {0.0f, 0.0f};
+        const bool want_u = FEAT && v > k;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             if (i == 0) cp_async_wait<1>(); else cp_async_wait<0>();
@@ -564,7 +597,8 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                 const int np = min(max(V - (sg * kSeg + 32 * lane), 0), 32);
                 float l[32];
                 read_lane(buf + i * kSeg, np, l);
-                seg[i] = segment_ms(l, np, c, finite);
+                if (want_u) seg[i] = segment_ms<true>(l, np, c, finite, &su[i]);
+                else seg[i] = segment_ms(l, np, c, finite);
                 if (lane == 0) {
                     segm[sg] = seg[i].m;
                     segs[sg] = seg[i].s;
@@ -574,6 +608,9 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
         const MaxSum a = ms_merge(seg[0], seg[1]);
         unsigned int prev = 0;
+        if (want_u && lane == 0)
+            partu[(static_cast<size_t>(b) * NV + v) * NW + g] =
+                msu_merge(MSU{seg[0].m, seg[0].s, su[0]}, MSU{seg[1].m, seg[1].s, su[1]}).u;
         if (lane == 0) {
             part[(static_cast<size_t>(b) * NV + v) * NW + g] = make_float2(a.m, a.s);
             __threadfence();
@@ -601,6 +638,25 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         MaxSum a = ms_merge(ms_merge(ms_merge(n[0], n[1]), ms_merge(n[2], n[3])),
                             ms_merge(ms_merge(n[4], n[5]), ms_merge(n[6], n[7])));
         a = warp_tree_ms(a, lane, 5);
+        if (FEAT && v > k) {
+            // entropy of the draft distribution in nats: H = ln 2 (log2 S - U / S),
+            // U = sum of 2^(l c - M) (l c - M) over the vector
+            MSU nu[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int gi = 8 * lane + i;
+                nu[i] = MSU{n[i].m, n[i].s, gi < NW ? __ldcg(partu + (static_cast<size_t>(b) * NV + v) * NW + gi) : 0.0f};
+            }
+            MSU r = msu_merge(msu_merge(msu_merge(nu[0], nu[1]), msu_merge(nu[2], nu[3])),
+                              msu_merge(msu_merge(nu[4], nu[5]), msu_merge(nu[6], nu[7])));
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const MSU other{__shfl_xor_sync(0xffffffffu, r.m, o), __shfl_xor_sync(0xffffffffu, r.s, o),
+                                __shfl_xor_sync(0xffffffffu, r.u, o)};
+                r = msu_merge(r, other);
+            }
+            if (lane == 0) ent[static_cast<size_t>(b) * NV + v] = 0.69314718f * (log2f(r.s) - r.u / r.s);
+        }
         unsigned int prev = 0;
         if (lane == 0) {
             roots[static_cast<size_t>(b) * NV + v] = make_float2(a.m, __frcp_rn(a.s));
@@ -619,6 +675,7 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const uint64_t seed = seeds[b];
     const float *segrow = segmax + static_cast<size_t>(b) * NV * NSP;
     bool reject = false;
+    float conf = 0.0f;
     if (lane < k) {
         const int j = lane;
         const int d = draft[static_cast<size_t>(b) * k + j];
@@ -630,9 +687,26 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                                     segrow + static_cast<size_t>(j) * NSP, d, c, root_of(j));
             const float q = prob_at(dlog + (static_cast<size_t>(b) * k + j) * V,
                                     segrow + static_cast<size_t>(k + 1 + j) * NSP, d, c, root_of(k + 1 + j));
+            conf = q;
             const float ratio = __fdiv_rn(p, q);
             const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
             reject = !(u < ratio);
+        }
+    }
+    if constexpr (FEAT) {
+        // the step's features over the k drafted positions (lanes 0..k-1)
+        const float h = lane < k ? __ldcg(ent + static_cast<size_t>(b) * NV + k + 1 + lane) : 0.0f;
+        float sh = h, sc = conf, mh = lane < k ? h : -INFINITY, mc = lane < k ? conf : INFINITY;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            sh += __shfl_xor_sync(0xffffffffu, sh, o);
+            sc += __shfl_xor_sync(0xffffffffu, sc, o);
+            mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, o));
+            mc = fminf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+        }
+        if (lane == 0) {
+            float *f = feat + static_cast<size_t>(b) * 4;
+            f[0] = sh / k; f[1] = sc / k; f[2] = mh; f[3] = mc;
         }
     }
     const unsigned int rej = __ballot_sync(0xffffffffu, reject);
@@ -806,7 +880,8 @@ cudaError_t allow_sampling_smem()
     if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(sample_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+    e = cudaFuncSetAttribute(sample_a_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(sample_a_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(sample_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemS);
     if (e == cudaSuccess) done[dev] = true;
     return e;
@@ -871,10 +946,11 @@ extern "C" nq_status spec_draft_argmax(const float *logits, int M, int V, int32_
     return nq::cuda_status(cudaGetLastError());
 }
 
-extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
-                                        int B, int k, int V, float temperature, const uint64_t *seeds,
-                                        uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
-                                        size_t ws_bytes, cudaStream_t stream)
+namespace nq {
+namespace {
+nq_status launch_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits, int B, int k,
+                        int V, float temperature, const uint64_t *seeds, uint64_t round, int32_t *out_tok,
+                        int32_t *out_cnt, void *ws, size_t ws_bytes, float *features, cudaStream_t stream)
 {
     if (k < 1) return NQ_ERR_ARG;
     nq_status st = nq::check_accept(B, k, V, ws, ws_bytes);
@@ -897,11 +973,12 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
     if (nq::allow_sampling_smem() != cudaSuccess) return NQ_ERR_CUDA;
     const int nsp = nq::n_segments_padded(V);
     dim3 grid_a(nsp / (2 * nq::kWarpsS), 2 * k + 1, B);   // one warp per segment pair
-    nq::sample_a_kernel<<<grid_a, nq::kThreadsS, nq::kSmemS, stream>>>(
+    auto ka = features ? nq::sample_a_kernel<true> : nq::sample_a_kernel<false>;
+    ka<<<grid_a, nq::kThreadsS, nq::kSmemS, stream>>>(
         draft, draft_logits, tgt_logits, k, V, c, al, seeds, round, reinterpret_cast<unsigned int *>(w + L.counters_a),
         reinterpret_cast<unsigned int *>(w + L.vcount), reinterpret_cast<float2 *>(w + L.part), segmax,
         reinterpret_cast<float *>(w + L.segsum), reinterpret_cast<float2 *>(w + L.roots), rec, out_tok, out_cnt,
-        status);
+        reinterpret_cast<float *>(w + L.partu), reinterpret_cast<float *>(w + L.ent), features, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return NQ_ERR_CUDA;
     // pass B as a programmatic dependent launch when pass A fills the GPU: its
@@ -925,6 +1002,30 @@ extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft
                            static_cast<const float *>(segmax), static_cast<const float *>(reinterpret_cast<float *>(w + L.segsum)),
                            reinterpret_cast<float *>(w + L.ssum), reinterpret_cast<float *>(w + L.lsum));
     return nq::cuda_status(e);
+}
+}  // namespace
+}  // namespace nq
+
+
+extern "C" nq_status spec_accept_sample(const int32_t *draft, const float *draft_logits, const float *tgt_logits,
+                                        int B, int k, int V, float temperature, const uint64_t *seeds,
+                                        uint64_t round, int32_t *out_tok, int32_t *out_cnt, void *ws,
+                                        size_t ws_bytes, cudaStream_t stream)
+{
+    return nq::launch_sample(draft, draft_logits, tgt_logits, B, k, V, temperature, seeds, round, out_tok, out_cnt,
+                             ws, ws_bytes, nullptr, stream);
+}
+
+extern "C" nq_status spec_accept_sample_features(const int32_t *draft, const float *draft_logits,
+                                                 const float *tgt_logits, int B, int k, int V, float temperature,
+                                                 const uint64_t *seeds, uint64_t round, int32_t *out_tok,
+                                                 int32_t *out_cnt, float *features, void *ws, size_t ws_bytes,
+                                                 cudaStream_t stream)
+{
+    if (!features) return NQ_ERR_ARG;
+    if (!nq::aligned16(features)) return NQ_ERR_ALIGN;
+    return nq::launch_sample(draft, draft_logits, tgt_logits, B, k, V, temperature, seeds, round, out_tok, out_cnt,
+                             ws, ws_bytes, features, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free greedy acceptance

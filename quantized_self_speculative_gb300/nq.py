@@ -38,6 +38,13 @@ class nq_weights(C.Structure):
                 ("base", C.c_void_p), ("resid", C.c_void_p), ("scales", C.c_void_p)]
 
 
+class nq_kv_cache(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("heads_kv", C.c_int32), ("head_dim", C.c_int32), ("group", C.c_int32),
+                ("max_len", C.c_int32), ("pad", C.c_int32),
+                ("k_base", C.c_void_p), ("k_resid", C.c_void_p), ("k_scales", C.c_void_p),
+                ("v_base", C.c_void_p), ("v_resid", C.c_void_p), ("v_scales", C.c_void_p)]
+
+
 def lib():
     """Load libnq.so (raises if it has not been built)."""
     global _lib
@@ -68,6 +75,16 @@ def lib():
             L.nq_status_string.restype = C.c_char_p
             L.nq_get_device_status.argtypes = [vp, C.POINTER(C.c_uint32)]
             L.spec_draft_argmax.argtypes = [vp, i32, i32, vp, i32, vp, sz, vp]
+            KV = C.POINTER(nq_kv_cache)
+            L.nq_kv_cache_bytes.argtypes = [i32, i32, i32, i32, i32, C.POINTER(sz), C.POINTER(sz)]
+            L.nq_kv_append.argtypes = [KV, vp, vp, i32, vp, vp]
+            L.nq_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.nq_attn_workspace_bytes.restype = sz
+            L.nq_attn_decode.argtypes = [KV, vp, i32, i32, vp, i32, f32, vp, vp, sz, vp]
+            for name in ("nq_kv_cache_bytes", "nq_kv_append", "nq_attn_decode"):
+                getattr(L, name).restype = i32
+            L.spec_accept_sample_features.argtypes = [vp, vp, vp, i32, i32, i32, f32, vp, u64, vp, vp, vp, vp, sz, vp]
+            L.spec_accept_sample_features.restype = i32
             L.nq_embed_rows.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp]
             L.nq_embed_round.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp]
             L.spec_round_commit.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, vp]
@@ -309,6 +326,79 @@ def round_commit(out_tok: torch.Tensor, out_cnt: torch.Tensor, seq: torch.Tensor
     _check(lib().spec_round_commit(_dev(out_tok, torch.int32, "out_tok"), _dev(out_cnt, torch.int32, "out_cnt"), B,
                                    k1 - 1, _dev(seq, torch.int32, "seq"), _dev(seq_len, torch.int32, "seq_len"),
                                    seq.shape[1], _dev(x0, torch.int32, "x0"), _stream(stream)), "spec_round_commit")
+
+
+def accept_sample_features(draft: torch.Tensor, draft_logits: torch.Tensor, tgt_logits: torch.Tensor,
+                           temperature: float, seeds: torch.Tensor, round_: int, ws: Optional[torch.Tensor] = None,
+                           out_tok=None, out_cnt=None, features=None, stream=None):
+    """spec_accept_sample plus SpecKV's step features per row: (mean entropy,
+    mean confidence, max entropy, min confidence) of the k drafted positions."""
+    B, k = draft.shape
+    V = tgt_logits.shape[-1]
+    ws = ws if ws is not None else accept_workspace(B, k, V, draft.device)
+    out_tok = out_tok if out_tok is not None else torch.empty((B, k + 1), dtype=torch.int32, device=draft.device)
+    out_cnt = out_cnt if out_cnt is not None else torch.empty(B, dtype=torch.int32, device=draft.device)
+    features = features if features is not None else torch.empty((B, 4), dtype=torch.float32, device=draft.device)
+    seeds_p = _dev(seeds, torch.int64, "seeds") if seeds.dtype == torch.int64 else _dev(seeds, torch.uint64, "seeds")
+    _check(lib().spec_accept_sample_features(
+        _dev(draft, torch.int32, "draft"), _dev(draft_logits, torch.float32, "draft_logits"),
+        _dev(tgt_logits, torch.float32, "tgt_logits"), B, k, V, float(temperature), seeds_p, int(round_) & (2**64 - 1),
+        _dev(out_tok, torch.int32, "out_tok"), _dev(out_cnt, torch.int32, "out_cnt"),
+        _dev(features, torch.float32, "features"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+        "spec_accept_sample_features")
+    return out_tok, out_cnt, features
+
+
+# ---------------------------------------------------------------- nested KV cache
+class KVCache:
+    """One layer's nested KV cache (device buffers allocated here, uint8;
+    BitNest Fig. 4): planes [batch][heads_kv][max_len][head_dim/2], fp16
+    scales [batch][heads_kv][max_len][head_dim/group], for K and for V."""
+
+    def __init__(self, batch: int, heads_kv: int, head_dim: int, group: int, max_len: int, device=None):
+        device = device or torch.device("cuda")
+        pb, sb = C.c_size_t(), C.c_size_t()
+        _check(lib().nq_kv_cache_bytes(batch, heads_kv, head_dim, group, max_len, C.byref(pb), C.byref(sb)),
+               "nq_kv_cache_bytes")
+        self.batch, self.heads_kv, self.head_dim, self.group, self.max_len = batch, heads_kv, head_dim, group, max_len
+        mk = lambda n: torch.zeros(n, dtype=torch.uint8, device=device)
+        self.k_base, self.k_resid, self.k_scales = mk(pb.value), mk(pb.value), mk(sb.value)
+        self.v_base, self.v_resid, self.v_scales = mk(pb.value), mk(pb.value), mk(sb.value)
+        self.plane_bytes, self.scale_bytes = pb.value, sb.value
+
+    def struct(self) -> nq_kv_cache:
+        return nq_kv_cache(self.batch, self.heads_kv, self.head_dim, self.group, self.max_len, 0,
+                           self.k_base.data_ptr(), self.k_resid.data_ptr(), self.k_scales.data_ptr(),
+                           self.v_base.data_ptr(), self.v_resid.data_ptr(), self.v_scales.data_ptr())
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor, stream=None) -> None:
+        """Quantise k_new, v_new fp32 [batch][heads_kv][n][head_dim] into rows pos[b] .."""
+        n = k_new.shape[2]
+        st = self.struct()
+        _check(lib().nq_kv_append(C.byref(st), _dev(k_new, torch.float32, "k_new"), _dev(v_new, torch.float32, "v_new"),
+                                  n, _dev(pos, torch.int32, "pos"), _stream(stream)), "nq_kv_append")
+
+    def attention(self, q: torch.Tensor, lens: torch.Tensor, planes: int, scale: float, out=None, ws=None,
+                  stream=None) -> torch.Tensor:
+        """softmax(scale q K^T) V over the 4-bit (planes=1) or 8-bit (planes=2)
+        view; q fp32 [batch][M][heads_q][head_dim]."""
+        B, M, Hq, d = q.shape
+        out = out if out is not None else torch.empty_like(q)
+        need = lib().nq_attn_workspace_bytes(B, M, Hq, d, self.max_len)
+        ws = ws if ws is not None else torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = self.struct()
+        _check(lib().nq_attn_decode(C.byref(st), _dev(q, torch.float32, "q"), M, Hq, _dev(lens, torch.int32, "lens"),
+                                    int(planes), float(scale), _dev(out, torch.float32, "out"),
+                                    _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "nq_attn_decode")
+        return out
+
+    def host_dict(self):
+        """The cache buffers as numpy arrays shaped for the oracle."""
+        sh = (self.batch, self.heads_kv, self.max_len)
+        p = lambda t: t.cpu().numpy().reshape(*sh, self.head_dim // 2)
+        sc = lambda t: t.cpu().numpy().view("uint16").reshape(*sh, self.head_dim // self.group)
+        return dict(k_base=p(self.k_base), k_resid=p(self.k_resid), k_scales=sc(self.k_scales),
+                    v_base=p(self.v_base), v_resid=p(self.v_resid), v_scales=sc(self.v_scales))
 
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> None:

@@ -128,3 +128,21 @@ def test_gpu_acceptance_probability_is_sum_of_min(nq):
     beta = np.minimum(softmax64(p_logits[0]), softmax64(q_logits[0])).sum()
     acc = (cnt > 1).mean()
     assert abs(acc - beta) < 4 * np.sqrt(beta * (1 - beta) / cnt.size)
+
+
+@pytest.mark.parametrize("B,k,V,T", [(64, 4, 152064, 1.0), (5, 8, 32000, 0.7), (3, 2, 4099, 1.3)])
+def test_gpu_draft_features_match_fp64(nq, B, k, V, T):
+    """SpecKV's step features from the acceptance pass (mean / max draft
+    entropy, mean / min draft confidence) against the oracle's fp64
+    definition; the token outputs equal spec_accept_sample's bit for bit."""
+    tl = synth.target_logits(9500 + V, B, k, V, 3.0)
+    dl = synth.draft_logits_from(tl, 9501 + V, 0.5)
+    d = synth.draft_tokens_sampled(dl, 9502 + V, T)
+    seeds = synth.seeds_for(12, B)
+    out, cnt, feat = nq.accept_sample_features(dev(d), dev(dl), dev(tl), T, seeds_dev(seeds), 4)
+    out2, cnt2 = nq.accept_sample(dev(d), dev(dl), dev(tl), T, seeds_dev(seeds), 4)
+    assert torch.equal(out, out2) and torch.equal(cnt, cnt2)
+    ref = O.draft_features(d, dl, T)
+    got = feat.cpu().numpy().astype(np.float64)
+    assert np.allclose(got, ref, rtol=2e-5, atol=1e-6), np.abs(got - ref).max()
+    assert nq.device_status() == 0
