@@ -444,6 +444,58 @@ class RoundLoop:
                 "launches_per_round": 3 * k + 5}
 
 
+# ------------------------------------------------------------------ nested KV cache attention (long context)
+def kv_sweep(device, ctx=32768, layers=4, iters=10):
+    """Decode attention over the nested KV cache at a 32K context, batch 1
+    (BitNest Fig. 4-5, Tables 9-10: the draft reads the KV4 base view, the
+    verify pass the KV8 view): LLaMA-2-7B-32K heads (32 x 128, MHA) and
+    Qwen2.5-7B heads (28 query / 4 kv heads x 128, GQA).  Four layers' caches
+    are rotated so that every call streams from HBM.  Algorithmic bytes per
+    call: K and V rows read, len x (planes x d/2 + 2 d/G) each, plus q and out."""
+    import torch
+    from quantized_self_speculative_gb300 import nq
+    hbm, _ = peaks()
+    out = {}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(71)
+    for name, Hq, Hkv in (("llama2_7b_32k_mha", 32, 32), ("qwen25_7b_gqa", 28, 4)):
+        d, G = 128, 128
+        caches = [nq.KVCache(1, Hkv, d, G, ctx + 16, device) for _ in range(layers)]
+        for c in caches:
+            for lo in range(0, ctx, 4096):
+                k = torch.randn((1, Hkv, 4096, d), generator=gen, device=device)
+                v = torch.randn((1, Hkv, 4096, d), generator=gen, device=device)
+                c.append(k, v, torch.tensor([lo], dtype=torch.int32, device=device))
+        torch.cuda.synchronize()
+        res = {}
+        for kind, M, planes in (("draft_M1_kv4", 1, 1), ("verify_M5_kv8", K_DRAFT + 1, 2)):
+            q = torch.randn((1, M, Hq, d), generator=gen, device=device)
+            lens = torch.tensor([ctx], dtype=torch.int32, device=device)
+            o = torch.empty_like(q)
+            need = nq.lib().nq_attn_workspace_bytes(1, M, Hq, d, ctx + 16)
+            ws = torch.empty(need, dtype=torch.uint8, device=device)
+            for c in caches:
+                c.attention(q, lens, planes, d ** -0.5, out=o, ws=ws)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
+                for c in caches:
+                    c.attention(q, lens, planes, d ** -0.5, out=o, ws=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (iters * layers)
+            byts = 2 * Hkv * ctx * (planes * d // 2 + 2 * d // G) + 2 * M * Hq * d * 4
+            res[kind] = {"us_per_layer": round(us, 2), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                         "frac": round(byts / (us * 1e-6) / 1e9 / hbm, 4), "bytes": byts}
+        res["draft_speedup_kv4_vs_kv8_per_row"] = round(res["verify_M5_kv8"]["us_per_layer"] /
+                                                       res["draft_M1_kv4"]["us_per_layer"], 3)
+        out[name] = res
+        del caches
+        torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ per-linear times (LLaMA-2-7B shapes)
 def per_linear_table(R, reps=3):
     """Device time of one linear per launch, for each linear shape of the
@@ -913,6 +965,7 @@ def run_ours(args):
         line["config3_llama3_8b_b16_k8"] = config3_sweep(device)
         line["config4_qwen25_7b_tiers"] = config4_sweep(device)
         line["config5_tokens_per_round"] = config5_tokens(device)
+        line["kv_nesting_32k"] = kv_sweep(device)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)

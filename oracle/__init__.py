@@ -78,6 +78,8 @@ def lib():
             L.orc_draft_argmax.argtypes = [vp, i32, i32, vp]
             L.orc_sample_p.argtypes = [vp, i32, f32, f32]
             L.orc_draft_features.argtypes = [vp, vp, i32, i32, i32, f32, vp]
+            L.orc_quantize_act_int8.argtypes = [vp, i32, i32, vp, vp]
+            L.orc_linear_a8.argtypes = [C.POINTER(_Weights), i32, vp, vp, i32, vp]
             L.orc_attn_decode.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32, f32, vp]
             L.orc_round_commit.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp]
             L.orc_f32_to_f16_n.argtypes = [vp, vp, i32]
@@ -396,3 +398,34 @@ def attn_decode(q, cache, lens, planes: int, scale: float):
                              ln.ctypes.data, int(planes), float(scale), out.ctypes.data) < 0:
         raise ValueError("bad attention arguments")
     return out
+
+
+# ------------------------------------------------------------------ W8A8 (int8 activations)
+# BitNest Table 1 "W4A8 -> W8A8" and Table 12: the draft multiplies 4-bit base
+# codes, the target the 8-bit codes, both against int8 activations.
+
+def quantize_act_int8(x_bf16):
+    """bf16 bits [M][K] -> (int8 codes [M][K], fp32 row scales [M]):
+    s = fp32(absmax / 127), code = clamp(rint(x / s), -127, 127)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    xq = np.empty((M, K), np.int8)
+    sx = np.empty(M, np.float32)
+    if lib().orc_quantize_act_int8(x.ctypes.data, M, K, xq.ctypes.data, sx.ctypes.data) < 0:
+        raise ValueError("non-finite activation")
+    return xq, sx
+
+
+def linear_a8(fmt: int, n: int, k: int, group: int, base, resid, scales, xq, sx, verify: bool):
+    """W8A8 / W4A8 linear: exact integer group dots, fp64 scaling -> fp64 [M][n]."""
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    M = xq.shape[0]
+    base = np.ascontiguousarray(base)
+    resid = None if resid is None else np.ascontiguousarray(resid)
+    scales = np.ascontiguousarray(scales)
+    W = _Weights(n, k, group, fmt, _p(base), _p(resid) if resid is not None else None, _p(scales))
+    y = np.empty((M, n), np.float64)
+    if lib().orc_linear_a8(C.byref(W), int(verify), xq.ctypes.data, sx.ctypes.data, M, y.ctypes.data) < 0:
+        raise ValueError("bad format for an int8-activation linear")
+    return y

@@ -295,6 +295,62 @@ int orc_linear(const nq_oracle_weights *W, int use_resid, const uint16_t *x, int
 }
 
 /* ======================================================================== */
+/* W4A8 -> W8A8: int8 activations [BitNest Table 1 "W4A8 -> W8A8", Table 12]. */
+/* ======================================================================== */
+
+/* Per activation row: s_x = fp32(absmax / 127) (IEEE division), codes
+ * x_q = clamp(rint(x / s_x), -127, 127); a zero row gives s_x = 0, codes 0. */
+int orc_quantize_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *sx)
+{
+    for (int m = 0; m < M; m++) {
+        float amax = 0.0f;
+        for (int i = 0; i < K; i++) {
+            float v = fabsf(orc_bf16_to_f32(x[(size_t)m * K + i]));
+            if (!(v <= 3.0e38f)) return -1;
+            if (v > amax) amax = v;
+        }
+        float s = amax / 127.0f;
+        sx[m] = s;
+        for (int i = 0; i < K; i++) {
+            int q = 0;
+            if (s > 0.0f) {
+                float r = rintf(orc_bf16_to_f32(x[(size_t)m * K + i]) / s);
+                q = r < -127.0f ? -127 : (r > 127.0f ? 127 : (int)r);
+            }
+            xq[(size_t)m * K + i] = (int8_t)q;
+        }
+    }
+    return 0;
+}
+
+/* y[m][n] = s_x[m] * sum_g S_g * sum_{k in g} code[n][k] * x_q[m][k] with
+ * code = q4 and S = s (draft), or code = 16 q4 + r and S = s / 16 (verify);
+ * the group dot products are exact integers, the scaling fp64. */
+int orc_linear_a8(const nq_oracle_weights *W, int use_resid, const int8_t *xq, const float *sx, int M, double *y)
+{
+    if (W->format != ORC_FMT_NESTED44 && W->format != ORC_FMT_INT4) return -1;
+    if (use_resid && W->format != ORC_FMT_NESTED44) return -1;
+    int ng = W->k / W->group;
+    for (int m = 0; m < M; m++)
+        for (int row = 0; row < W->n; row++) {
+            double acc = 0.0;
+            for (int grp = 0; grp < ng; grp++) {
+                long long dot = 0;
+                for (int i = 0; i < W->group; i++) {
+                    size_t idx = (size_t)row * W->k + (size_t)grp * W->group + i;
+                    int code = orc_get_code(W->base, idx);
+                    if (use_resid) code = 16 * code + orc_get_code(W->resid, idx);
+                    dot += (long long)code * xq[(size_t)m * W->k + (size_t)grp * W->group + i];
+                }
+                double sc = (double)orc_f16_to_f32(((const uint16_t *)W->scales)[(size_t)row * ng + grp]);
+                acc += (use_resid ? sc / 16.0 : sc) * (double)dot;
+            }
+            y[(size_t)m * W->n + row] = (double)sx[m] * acc;
+        }
+    return 0;
+}
+
+/* ======================================================================== */
 /* C3: greedy acceptance  [Erge, "Drafting and checking tokens", Table 1;    */
 /*     SpecQuant III.D.4; R4]                                                */
 /* ======================================================================== */

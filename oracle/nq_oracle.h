@@ -35,6 +35,9 @@ int orc_pack_fp16(const float *w, int n, int k, uint16_t *w16);
 int orc_linear(const nq_oracle_weights *W, int use_resid, const uint16_t *x, int M,
                const int32_t *rows, int nrows, double *y);
 
+int orc_quantize_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *sx);
+int orc_linear_a8(const nq_oracle_weights *W, int use_resid, const int8_t *xq, const float *sx, int M, double *y);
+
 int orc_accept_greedy(const int32_t *draft, const float *tgt_logits, int B, int k, int V,
                       int32_t *out_tok, int32_t *out_cnt);
 

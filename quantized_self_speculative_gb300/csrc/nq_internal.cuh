@@ -69,6 +69,25 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint
         : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
+// ---------------------------------------------------------------- nested quantiser
+// BitNest Fig. 2 reading: with the group scale s = fp16(absmax / 7), base
+// q4 = clamp(rint(w / s), -8, 7) and refinement r = clamp(rint(16 (w / s - q4)),
+// -8, 7); s == 0 gives zeros.  IEEE fp32 with round to nearest throughout, so
+// the codes are reproducible bit for bit (weights and KV rows alike).
+__device__ __forceinline__ int nested_clamp(float v)
+{
+    int i = static_cast<int>(v);
+    return i < -8 ? -8 : (i > 7 ? 7 : i);
+}
+__device__ __forceinline__ void nested_quantise(float w, float s, int &q4, int &r)
+{
+    if (s == 0.0f) { q4 = 0; r = 0; return; }
+    float x = __fdiv_rn(w, s);
+    q4 = nested_clamp(rintf(x));
+    float err = __fmul_rn(__fsub_rn(x, static_cast<float>(q4)), 16.0f);
+    r = nested_clamp(rintf(err));
+}
+
 // ---------------------------------------------------------------- canonical
 // fp32 recipe of the sampled acceptance (see spec_accept_sample in nq.h):
 // base-2 exponential of t <= 0.5: 0 below -125, else P(f) 2^n with n =

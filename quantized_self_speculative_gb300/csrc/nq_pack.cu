@@ -13,21 +13,6 @@ namespace {
 
 constexpr int kPackWarps = 8;
 
-__device__ __forceinline__ int clamp_code(float v)
-{
-    int i = static_cast<int>(v);
-    return i < -8 ? -8 : (i > 7 ? 7 : i);
-}
-
-__device__ __forceinline__ void quantise(float w, float s, int &q4, int &r)
-{
-    if (s == 0.0f) { q4 = 0; r = 0; return; }
-    float x = __fdiv_rn(w, s);
-    q4 = clamp_code(rintf(x));
-    float err = __fmul_rn(__fsub_rn(x, static_cast<float>(q4)), 16.0f);
-    r = clamp_code(rintf(err));
-}
-
 // Each lane owns E = G/32 consecutive weights of the group.
 template <int G>
 __global__ void __launch_bounds__(kPackWarps * 32)
@@ -55,7 +40,7 @@ pack_nested_kernel(const float *__restrict__ w, int n, int k, uint8_t *__restric
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         int q4, r;
-        quantise(v[e], s, q4, r);
+        nested_quantise(v[e], s, q4, r);
         bb |= static_cast<uint32_t>(q4 & 15) << (4 * e);
         rr |= static_cast<uint32_t>(r & 15) << (4 * e);
     }
