@@ -444,6 +444,59 @@ class RoundLoop:
                 "launches_per_round": 3 * k + 5}
 
 
+# ------------------------------------------------------------------ int8 activations (W4A8 -> W8A8)
+def a8_sweep(device, iters=10):
+    """BitNest's own precision (Table 1, "W4A8 -> W8A8"): the LLaMA-2-7B pass
+    with int8 activation codes, draft at M = 1 (base plane) and verify at
+    M = k+1 = 5 (both planes), integer dots on the CUDA cores; plus the
+    per-row activation quantiser over one [M][4096] input.  Algorithmic bytes
+    as for the bf16-activation passes with 1-byte activations."""
+    import torch
+    from quantized_self_speculative_gb300 import nq, synth
+    hbm, _ = peaks()
+    shapes = _shapes(synth.llama2_7b_linears)
+    layers = _pass_layers(device, shapes, nq.FMT_NESTED44, GROUP, 97)
+    out = {}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(98)
+    for kind, M, verify in (("draft_w4a8_M1", 1, False), ("verify_w8a8_M5", K_DRAFT + 1, True)):
+        xqs, sxs, ys = [], [], []
+        for L in layers:
+            x = torch.randn((M, L.k_in), generator=gen, device=device).to(torch.bfloat16)
+            xq, sx = nq.quantize_act_int8(x)
+            xqs.append(xq)
+            sxs.append(sx)
+            ys.append(torch.empty((M, L.n_out), dtype=torch.float32, device=device))
+        b = nq.LinearA8Batch(verify, layers, xqs, sxs, ys)
+        for _ in range(3):
+            b()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            b()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        w = 1.0 if verify else 0.5
+        byts = sum(w * L.n_out * L.k_in + 2 * L.n_out * L.k_in // GROUP + M * L.k_in + 4 * M + 4 * M * L.n_out
+                   for L in layers)
+        out[kind] = {"us": round(us, 1), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                     "frac": round(byts / (us * 1e-6) / 1e9 / hbm, 4), "bytes": int(byts)}
+        x = torch.randn((M, 4096), generator=gen, device=device).to(torch.bfloat16)
+        xq = torch.empty((M, 4096), dtype=torch.int8, device=device)
+        sx = torch.empty(M, dtype=torch.float32, device=device)
+        e0.record()
+        for _ in range(100):
+            nq.quantize_act_int8(x, xq, sx)
+        e1.record()
+        torch.cuda.synchronize()
+        out[kind]["quantize_act_us_per_input"] = round(e0.elapsed_time(e1) * 1e3 / 100, 2)
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ nested KV cache attention (long context)
 def kv_sweep(device, ctx=32768, layers=4, iters=10):
     """Decode attention over the nested KV cache at a 32K context, batch 1
@@ -966,6 +1019,7 @@ def run_ours(args):
         line["config4_qwen25_7b_tiers"] = config4_sweep(device)
         line["config5_tokens_per_round"] = config5_tokens(device)
         line["kv_nesting_32k"] = kv_sweep(device)
+        line["w8a8_llama2_7b"] = a8_sweep(device)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -298,6 +298,28 @@ NQ_API nq_status spec_round_commit(const int32_t *out_tok, const int32_t *out_cn
                                    int32_t *seq_len, int max_len, int32_t *x0, cudaStream_t stream);
 
 /*
+ * Int8-activation linears (BitNest, Table 1 "W4A8 -> W8A8" and Table 12: the
+ * draft multiplies the 4-bit base codes, the target the 8-bit codes, both
+ * against 8-bit activations).
+ *
+ * nq_quantize_act_int8: per activation row, s_x = fp32(absmax / 127) (IEEE
+ *   division), x_q = clamp(rint(x / s_x), -127, 127); a zero row gives
+ *   s_x = 0 and zero codes.  x bf16 bits [M][K]; xq int8 [M][K]; sx fp32 [M].
+ *   A non-finite row sets NQ_DEV_NONFINITE (its codes are then zero).
+ * nq_linear_a8_batch: `count` linears at M activation rows (w, xq, sx, y are
+ *   host arrays of device pointers, as for nq_draft_gemv_batch):
+ *     draft  (verify = 0, NESTED44 base plane or INT4):
+ *       y[m][n] = s_x[m] sum_g s[n][g] sum_{k in g} q4[n][k] x_q[m][k]
+ *     verify (verify = 1, NESTED44, both planes):
+ *       y[m][n] = s_x[m] sum_g (s[n][g] / 16) sum_{k in g} (16 q4 + r)[n][k] x_q[m][k]
+ *   The products of codes are exact integers (dp4a); the group scales are
+ *   applied in fp32, 32 inputs at a time.  All layers share one group size.
+ */
+NQ_API nq_status nq_quantize_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *sx, cudaStream_t stream);
+NQ_API nq_status nq_linear_a8_batch(int count, const nq_weights *w, const int8_t *const *xq, const float *const *sx,
+                                    int M, int verify, float *const *y, cudaStream_t stream);
+
+/*
  * The nested KV cache (BitNest, Fig. 4 "KV nesting during speculative
  * decoding": the draft stage reads only the low-bit base view of the cache,
  * verification reads the full b_kv + r_kv-bit view of the same cache, the

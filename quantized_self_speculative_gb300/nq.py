@@ -75,6 +75,10 @@ def lib():
             L.nq_status_string.restype = C.c_char_p
             L.nq_get_device_status.argtypes = [vp, C.POINTER(C.c_uint32)]
             L.spec_draft_argmax.argtypes = [vp, i32, i32, vp, i32, vp, sz, vp]
+            L.nq_quantize_act_int8.argtypes = [vp, i32, i32, vp, vp, vp]
+            L.nq_linear_a8_batch.argtypes = [i32, W, C.POINTER(vp), C.POINTER(vp), i32, i32, C.POINTER(vp), vp]
+            for name in ("nq_quantize_act_int8", "nq_linear_a8_batch"):
+                getattr(L, name).restype = i32
             KV = C.POINTER(nq_kv_cache)
             L.nq_kv_cache_bytes.argtypes = [i32, i32, i32, i32, i32, C.POINTER(sz), C.POINTER(sz)]
             L.nq_kv_append.argtypes = [KV, vp, vp, i32, vp, vp]
@@ -347,6 +351,43 @@ def accept_sample_features(draft: torch.Tensor, draft_logits: torch.Tensor, tgt_
         _dev(features, torch.float32, "features"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
         "spec_accept_sample_features")
     return out_tok, out_cnt, features
+
+
+# ---------------------------------------------------------------- int8 activations (W4A8 -> W8A8)
+def quantize_act_int8(x: torch.Tensor, xq=None, sx=None, stream=None):
+    """bf16 [M][K] -> (int8 codes [M][K], fp32 row scales [M])."""
+    M, K = x.shape
+    xq = xq if xq is not None else torch.empty((M, K), dtype=torch.int8, device=x.device)
+    sx = sx if sx is not None else torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().nq_quantize_act_int8(_dev(x, torch.bfloat16, "x"), M, K, _dev(xq, torch.int8, "xq"),
+                                      _dev(sx, torch.float32, "sx"), _stream(stream)), "nq_quantize_act_int8")
+    return xq, sx
+
+
+class LinearA8Batch:
+    """Prebuilt argument arrays for nq_linear_a8_batch (one launch over many
+    linears at the same M, int8 activation codes and row scales)."""
+
+    def __init__(self, verify: bool, layers: Sequence[PackedLinear], xqs, sxs, ys):
+        n = len(layers)
+        self.verify, self.count, self.M = int(verify), n, xqs[0].shape[0]
+        self.w = (nq_weights * n)(*[L.struct() for L in layers])
+        self.xq = (C.c_void_p * n)(*[t.data_ptr() for t in xqs])
+        self.sx = (C.c_void_p * n)(*[t.data_ptr() for t in sxs])
+        self.y = (C.c_void_p * n)(*[t.data_ptr() for t in ys])
+        self._keep = (list(layers), list(xqs), list(sxs), list(ys))
+
+    def __call__(self, stream=None):
+        _check(lib().nq_linear_a8_batch(self.count, self.w, self.xq, self.sx, self.M, self.verify, self.y,
+                                        _stream(stream)), "nq_linear_a8_batch")
+
+
+def linear_a8(w: PackedLinear, xq: torch.Tensor, sx: torch.Tensor, verify: bool, y=None, stream=None):
+    """One int8-activation linear: y fp32 [M][n_out]."""
+    M = xq.shape[0]
+    y = y if y is not None else torch.empty((M, w.n_out), dtype=torch.float32, device=xq.device)
+    LinearA8Batch(verify, [w], [xq], [sx], [y])(stream)
+    return y
 
 
 # ---------------------------------------------------------------- nested KV cache
