@@ -79,7 +79,7 @@ __device__ __forceinline__ void codes8(uint32_t b, uint32_t r, uint32_t &lo, uin
 }
 
 template <int PLANES, int G, int MM>
-__global__ void __launch_bounds__(kA8Warps * 32)
+__global__ void __launch_bounds__(kA8Warps * 32, 2)
 a8_kernel(const __grid_constant__ A8Batch B)
 {
     constexpr int kOff = PLANES == 2 ? 136 : 8;
@@ -215,7 +215,11 @@ cudaError_t launch_a8(const A8Batch &b, int mm, cudaStream_t s)
     switch (mm) {
     case 1: a8_kernel<PLANES, G, 1><<<grid, kA8Warps * 32, 0, s>>>(b); break;
     case 2: a8_kernel<PLANES, G, 2><<<grid, kA8Warps * 32, 0, s>>>(b); break;
+    case 3: a8_kernel<PLANES, G, 3><<<grid, kA8Warps * 32, 0, s>>>(b); break;
     case 4: a8_kernel<PLANES, G, 4><<<grid, kA8Warps * 32, 0, s>>>(b); break;
+    case 5: a8_kernel<PLANES, G, 5><<<grid, kA8Warps * 32, 0, s>>>(b); break;
+    case 6: a8_kernel<PLANES, G, 6><<<grid, kA8Warps * 32, 0, s>>>(b); break;
+    case 7: a8_kernel<PLANES, G, 7><<<grid, kA8Warps * 32, 0, s>>>(b); break;
     default: a8_kernel<PLANES, G, 8><<<grid, kA8Warps * 32, 0, s>>>(b); break;
     }
     return cudaGetLastError();
@@ -257,7 +261,7 @@ extern "C" nq_status nq_linear_a8_batch(int count, const nq_weights *w, const in
     nq::A8Batch b{};
     for (int m0 = 0; m0 < M; m0 += nq::kA8MaxM) {
         const int Mc = std::min(nq::kA8MaxM, M - m0);
-        const int mm = Mc <= 1 ? 1 : (Mc <= 2 ? 2 : (Mc <= 4 ? 4 : 8));
+        const int mm = Mc;   // an exact instantiation for every M up to 8
         for (int i0 = 0; i0 < count; i0 += nq::kA8MaxP) {
             const int cnt = std::min(nq::kA8MaxP, count - i0);
             long long units = 0;
