@@ -287,6 +287,14 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
+// Smallest of three, NaN if any operand is NaN.
+__device__ __forceinline__ float min3_nan(float a, float b, float c)
+{
+    float d;
+    asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float pair_sum(unsigned long long eo)
 {
     const float2 v = f2_unpack(eo);
@@ -333,30 +341,56 @@ __device__ __forceinline__ MaxSum segment_ms(const float (&v)[32], int np, float
     const float mz = __fmul_rn(warp_max(mx), c);
     const unsigned long long c2 = f2_pack(c, c), nmz = f2_pack(-mz, -mz), z2 = f2_pack(0.0f, 0.0f);
     unsigned long long fin = z2, eo[2], uu = z2;
+    // A lane whose 32 entries are all present and whose smallest exponent
+    // t = l c - mz is at least -125 (t grows with l, so that one t bounds the
+    // rest; NaN fails the test) needs neither the underflow select nor the
+    // per-entry finiteness check: every t lies in [-125, 0.5].
+    bool fast = false;
+    if (np == 32) {
+        float mn = v[0];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+        for (int i = 1; i < 31; i += 2) mn = min3_nan(mn, v[i], v[i + 1]);
+        mn = min3_nan(mn, v[31], v[31]);
+        fast = __fmaf_rn(mn, c, -mz) >= -125.0f;
+    }
+    if (fast) {
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const unsigned long long t = f2_fma(f2_pack(v[16 * h + 2 * p], v[16 * h + 2 * p + 1]), c2, nmz);
-            fin = f2_fma(z2, t, fin);
-            const float2 e = exp2_canon_x2(t);
-            eo[h] = p == 0 ? f2_pack(e.x, e.y) : f2_add(eo[h], f2_pack(e.x, e.y));
-            if constexpr (FEAT) {
-                // absent entries: t = -inf, e = 0; count their product as 0
-                const float2 tv = f2_unpack(t);
-                uu = f2_fma(f2_pack(e.x, e.y), f2_pack(e.x > 0.0f ? tv.x : 0.0f, e.y > 0.0f ? tv.y : 0.0f), uu);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const unsigned long long t = f2_fma(f2_pack(v[16 * h + 2 * p], v[16 * h + 2 * p + 1]), c2, nmz);
+                const float2 e = exp2_canon_x2_inrange(t);
+                eo[h] = p == 0 ? f2_pack(e.x, e.y) : f2_add(eo[h], f2_pack(e.x, e.y));
+                if constexpr (FEAT) uu = f2_fma(f2_pack(e.x, e.y), t, uu);
             }
         }
-    }
-    if constexpr (FEAT) *u_out = warp_tree_sum(pair_sum(uu), 5);
-    if (np == 32) {
-        const float2 f = f2_unpack(fin);
-        finite = __fadd_rn(finite, __fadd_rn(f.x, f.y));
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < np) finite = __fmaf_rn(0.0f, __fmaf_rn(v[i], c, -mz), finite);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const unsigned long long t = f2_fma(f2_pack(v[16 * h + 2 * p], v[16 * h + 2 * p + 1]), c2, nmz);
+                fin = f2_fma(z2, t, fin);
+                const float2 e = exp2_canon_x2(t);
+                eo[h] = p == 0 ? f2_pack(e.x, e.y) : f2_add(eo[h], f2_pack(e.x, e.y));
+                if constexpr (FEAT) {
+                    // absent entries: t = -inf, e = 0; count their product as 0
+                    const float2 tv = f2_unpack(t);
+                    uu = f2_fma(f2_pack(e.x, e.y), f2_pack(e.x > 0.0f ? tv.x : 0.0f, e.y > 0.0f ? tv.y : 0.0f), uu);
+                }
+            }
+        }
+        if (np == 32) {
+            const float2 f = f2_unpack(fin);
+            finite = __fadd_rn(finite, __fadd_rn(f.x, f.y));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < np) finite = __fmaf_rn(0.0f, __fmaf_rn(v[i], c, -mz), finite);
+        }
     }
+    // warp-wide from here (every lane, whichever branch it took)
+    if constexpr (FEAT) *u_out = warp_tree_sum(pair_sum(uu), 5);
     const float s = warp_tree_sum(__fadd_rn(pair_sum(eo[0]), pair_sum(eo[1])), 5);
     return MaxSum{mz, s};
 }

@@ -167,6 +167,25 @@ __device__ __forceinline__ float2 exp2_canon_x2(unsigned long long t)
     return make_float2(tv.x < -125.0f ? 0.0f : ra, tv.y < -125.0f ? 0.0f : rb);
 }
 
+// exp2_canon_x2 for exponents known to lie in [-125, 0.5] (no underflow
+// select; same results as exp2_canon_x2 there).
+__device__ __forceinline__ float2 exp2_canon_x2_inrange(unsigned long long t)
+{
+    const unsigned long long mag = f2_pack(12582912.0f, 12582912.0f);
+    const unsigned long long big = f2_add(t, mag);
+    const unsigned long long f = f2_sub(t, f2_sub(big, mag));
+    unsigned long long p = f2_fma(f2_pack(0.000154035303933816099545f, 0.000154035303933816099545f), f,
+                                  f2_pack(0.00133335581464284434234f, 0.00133335581464284434234f));
+    p = f2_fma(p, f, f2_pack(0.00961812910762847716197f, 0.00961812910762847716197f));
+    p = f2_fma(p, f, f2_pack(0.0555041086648215799531f, 0.0555041086648215799531f));
+    p = f2_fma(p, f, f2_pack(0.240226506959100712333f, 0.240226506959100712333f));
+    p = f2_fma(p, f, f2_pack(0.693147180559945309417f, 0.693147180559945309417f));
+    p = f2_fma(p, f, f2_pack(1.0f, 1.0f));
+    const float2 pv = f2_unpack(p), bv = f2_unpack(big);
+    return make_float2(__int_as_float(__float_as_int(pv.x) + (__float_as_int(bv.x) << 23)),
+                       __int_as_float(__float_as_int(pv.y) + (__float_as_int(bv.y) << 23)));
+}
+
 struct MaxSum { float m, s; };
 
 // Merge two (max, sum) nodes; the larger max survives, the other sum is

@@ -48,14 +48,14 @@ namespace {
 constexpr int kRowPad = 64;           // activation row stride = 64 (mod 128) bytes -> conflict-free B loads
 constexpr int kMaxM = 16;             // activation rows per launch (two 8-column MMA tiles)
 constexpr int kXsMax = 112 * 1024;    // dynamic shared memory cap per CTA (two CTAs fit one SM)
-// Activation staging cap: whole activation rows up to K = 4096 at M <= 6
-// (and K = 11008 at M <= 2) with 16-warp units, segments beyond.  Shared
-// memory is carved out of L1, so the cap trades restaging against L1: with
-// one 16-warp CTA per SM, 56 KB measured best on whole-model passes
-// (LLaMA-2-7B verify at M = 5 and Qwen2.5-7B FP8 verify at M = 7 1.2% and 5%
-// faster than at 40 KB); with two 8-warp CTAs per SM anything above 40 KB
-// was slower.
-constexpr int kXsStageWide = 56 * 1024;   // 16-warp units (one CTA per SM)
+// Activation staging cap: whole activation rows up to K = 11008 at M <= 5
+// with 16-warp units (one CTA per SM), segments beyond.  Shared memory is
+// carved out of L1, so the cap trades restaging against L1: whole rows
+// measured best on whole-model passes (LLaMA-2-7B verify at M = 5: 0.779 of
+// the HBM roof at 112 KB against 0.736 at 56 KB, Qwen2.5-7B FP8 verify at
+// M = 9: 0.770 against 0.745; the draft unchanged); with two 8-warp CTAs per
+// SM anything above 40 KB was slower.
+constexpr int kXsStageWide = 112 * 1024;  // 16-warp units (one CTA per SM)
 constexpr int kXsStage = 40 * 1024;       // 8- and 4-warp units
 
 enum Kind { kNib = 0, kFp8 = 1, kFp16 = 2 };
