@@ -363,10 +363,13 @@ NQ_API nq_status nq_kv_append(const nq_kv_cache *cache, const float *k_new, cons
  * already appended), kv(h) = h / (heads_q / heads_kv) (grouped-query
  * attention).  planes = 1 reads the 4-bit base view (draft), 2 both planes
  * (the 8-bit target view).  q, out fp32 [batch][M][heads_q][head_dim]; len
- * int32 [batch] device.  fp32 arithmetic (scores, exponentials, sums):
- * agrees with an fp64 evaluation over the same dequantised rows to far
- * inside the linears' 2e-3 normwise tolerance.  Workspace (caller-owned,
- * no initialisation) of nq_attn_workspace_bytes() bytes; 0 on bad sizes.
+ * int32 [batch] device.  Both products run on the tensor cores with fp16
+ * operands (the scaled queries, the cache codes, the probabilities times the
+ * value rows' scales) and fp32 accumulation; exponentials and sums in fp32:
+ * agrees with an fp64 evaluation over the same dequantised rows within the
+ * linears' 2e-3 normwise tolerance (about 5e-4 measured).  Workspace
+ * (caller-owned, no initialisation) of nq_attn_workspace_bytes() bytes; 0 on
+ * bad sizes.
  */
 NQ_API size_t nq_attn_workspace_bytes(int batch, int M, int heads_q, int head_dim, int max_len);
 NQ_API nq_status nq_attn_decode(const nq_kv_cache *cache, const float *q, int M, int heads_q, const int32_t *len,

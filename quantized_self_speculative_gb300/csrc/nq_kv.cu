@@ -12,23 +12,33 @@
 // value of an element is s q4 and the target value (s / 16)(16 q4 + r).
 //
 // Attention (one launch + a combine): the cache rows of a (sequence, kv head)
-// are cut into 256-row splits; a CTA of four warps takes one split and up to
-// eight query vectors (query heads sharing the kv head, times query rows).
-// Scores: lane t of a warp owns cache row t of a 32-row block and dots its
-// decoded K row with the query vectors (held in shared memory); online
-// softmax per query vector across the blocks; values: the two half-warps take
-// alternate rows of the block, each lane 8 consecutive dimensions of the
-// decoded V row.  The splits' (max, sum, output) partials are merged by a
-// second kernel.  The cache rows are streamed once per CTA group (query-vector
-// groups of one split run side by side and share them in L2).
+// are cut into 256-row splits; a CTA of four warps takes one split and a tile
+// of 16 query vectors (query heads sharing the kv head, times query rows),
+// each warp 64 rows in four blocks of 16 with its own online softmax.  Both
+// products run on the tensor cores (warp MMA m16n8k16, fp16 operands, fp32
+// accumulators), in the manner of FlashAttention-2: S = Q K^T with the query
+// tile as the A rows and a block of K as two B tiles, then O += P V with P
+// taken straight from the S accumulators as the A operand.  The cache codes
+// enter the MMAs undequantised: an offset-binary nibble (q4 + 8) or byte
+// (16 q4 + r + 136) sits in the low bits of an fp16 half, i.e. code * 2^-24,
+// placed with integer masks and byte permutes only.  The offset leaves S
+// through the accumulator's initial value and O through a running sum of P;
+// the group scales multiply S after its MMA and P before the V product.  The
+// warps' states merge in shared memory, the splits' in a second kernel.
 #include "nq_internal.cuh"
+
+#include <atomic>
+#include <type_traits>
 
 namespace nq {
 namespace {
 
 constexpr int kKvWarps = 4;
-constexpr int kSplit = 256;                 // cache rows per CTA
-constexpr int kQvCap = 8;                   // query vectors per CTA at most
+constexpr int kBlk = 16;                    // cache rows per MMA block
+constexpr int kStages = 4;                  // cp.async ring per warp (blocks in flight)
+constexpr int kMinBlkPerWarp = 4;           // blocks per warp: 4 .. 16 (chosen per call)
+constexpr int kMaxBlkPerWarp = 16;
+constexpr int kQTile = 16;                  // query vectors per CTA (MMA rows)
 constexpr int kAppendWarps = 8;
 
 struct Cache {
@@ -90,221 +100,516 @@ kv_append_kernel(const float *__restrict__ src, int B, int H, int n_new, int d, 
     if (lane == 0) scales[row * gpr + grp] = sh;
 }
 
-// Element values of one 32-bit word per plane (8 consecutive elements, element
-// 2j in the low nibble of byte j): s q4 (PLANES == 1) or (s / 16)(16 q4 + r).
-template <int PLANES>
-__device__ __forceinline__ void decode8(uint32_t bw, uint32_t rw, float s, float (&o)[8])
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int q4 = static_cast<int>(bw << (28 - 4 * e)) >> 28;
-        if constexpr (PLANES == 2) {
-            const int r = static_cast<int>(rw << (28 - 4 * e)) >> 28;
-            o[e] = __fmul_rn(__fmul_rn(s, 0.0625f), static_cast<float>(16 * q4 + r));
-        } else {
-            o[e] = __fmul_rn(s, static_cast<float>(q4));
-        }
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t h2_pack(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 2^x by the multi-function unit (about 2 ulp; the probabilities enter the
+// products as fp16 anyway)
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Codes of nibbles i (low half) and i + 4 (high half) of a word of eight
+// elements, as fp16 subnormals: KV4 (q4 + 8); KV8 from the base and
+// refinement words, 16 (q4 + 8) + (r + 8) = q8 + 136.
+template <int PLANES>
+__device__ __forceinline__ uint32_t code_pair(uint32_t xb, uint32_t xr, int i)
+{
+    if constexpr (PLANES == 1) {
+        return ((xb >> (4 * i)) & 0x000F000Fu) ^ 0x00080008u;
+    } else {
+        // xb, xr already have every nibble's sign bit flipped (offset binary)
+        const uint32_t hi = i == 0 ? (xb << 4) : (xb >> (4 * i - 4));
+        return (hi & 0x00F000F0u) | ((xr >> (4 * i)) & 0x000F000Fu);
     }
 }
 
-// Partial attention of one split of cache rows for up to kQvMax query vectors.
-// Query vector v (0..nqv-1 of this CTA's group) = (query row m, query head hq)
-// with hq = kvh * g + (v' % g), m = v' / g for v' = qv0 + v.
-template <int PLANES, int D, int QV>
-__global__ void __launch_bounds__(kKvWarps * 32)
-attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int32_t *__restrict__ len, float scale,
-                  float *__restrict__ part, int nsplit)
+// Byte offset of (row r, byte o) of a 16-row tile of rows of RB bytes in
+// shared memory: 16-byte chunks, chunk q = r RB / 16 + o / 16 stored at
+// position (q mod 8) xor (q / 8 mod 8) of its 128-byte line (the MMA operand
+// reads of both products are then free of bank conflicts).
+template <int RB>
+__device__ __forceinline__ uint32_t swz(int r, int o)
 {
-    static_assert(D == 128 || D == 64, "head_dim 64 or 128");
-    constexpr int kQvMax = QV;                // query vectors per CTA (1, 2, 4 or 8)
-    constexpr int DW = D / 8;                 // 32-bit words per plane per row
-    const int g = Hq / C.H, nq_all = M * g, qgroups = (nq_all + QV - 1) / QV;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / qgroups, qg = blockIdx.z % qgroups;
-    const int qv0 = qg * kQvMax, nqv = min(kQvMax, nq_all - qv0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ __align__(16) float qs[kQvMax][D];
-    __shared__ float red_m[kKvWarps][kQvMax], red_l[kKvWarps][kQvMax];
-    __shared__ __align__(16) float red_o[kKvWarps][kQvMax][D];
-    const int Lb = min(len[b], C.L);
-    int lim[kQvMax];                          // rows < lim[v] are visible to query vector v
-#pragma unroll
-    for (int v = 0; v < kQvMax; ++v) {
-        const int vv = qv0 + (v < nqv ? v : 0);
-        const int m = vv / g;
-        lim[v] = v < nqv ? Lb - (M - 1 - m) : 0;
-    }
-    for (int i = threadIdx.x; i < kQvMax * D; i += kKvWarps * 32) {
-        const int v = i / D, j = i % D;
-        float x = 0.0f;
-        if (v < nqv) {
-            const int vv = qv0 + v, m = vv / g, hq = kvh * g + vv % g;
-            x = __fmul_rn(q[((static_cast<size_t>(b) * M + m) * Hq + hq) * D + j], scale);
-        }
-        qs[v][j] = x;
-    }
-    __syncthreads();
+    const int q = r * (RB / 16) + (o >> 4), line = q >> 3;
+    return static_cast<uint32_t>((line << 7) + (((q & 7) ^ (line & 7)) << 4) + (o & 15));
+}
 
+template <int PLANES, int D>
+struct AttnGeo {
+    static constexpr int RB = D / 2;                          // bytes per row and plane
+    static constexpr int TILE = kBlk * RB;                    // one plane of one block
+    static constexpr int STAGE = 2 * PLANES * TILE;           // K and V planes of one block
+    static constexpr int SCALES = 2 * kBlk * 2 * (D / 64);    // K and V scales of one block (fp16, up to 2 groups)
+    static constexpr int WARP = kStages * STAGE + kMaxBlkPerWarp * SCALES;
+    static constexpr int MERGE = kKvWarps * kQTile * (D + 2) * 4;
+    static constexpr int SMEM = kKvWarps * WARP > MERGE ? kKvWarps * WARP : MERGE;
+};
+
+// Partial attention of one split of cache rows for one tile of 16 query
+// vectors.  Query vector v = 16 z' + r (z' the tile index) = (query row m,
+// query head hq) with m = v / g, hq = kvh g + v % g.  NG = D / G groups per
+// row (1, or 2 when G = 64 < D = 128).  RR = 1 when the call has at most 8
+// query vectors per kv head (rows 8..15 of the tile stay empty), else 2.
+template <int PLANES, int D, int NG, int RR>
+__global__ void __launch_bounds__(kKvWarps * 32, 3)
+attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int32_t *__restrict__ len, float scale,
+                  float *__restrict__ part, int nsplit, int qtiles, int nbw)
+{
+    using Geo = AttnGeo<PLANES, D>;
+    constexpr int RB = Geo::RB, TILE = Geo::TILE, HALVES = D / 64;
+    constexpr int OFF = PLANES == 2 ? 136 : 8;
+    constexpr float FK = PLANES == 2 ? 1048576.0f : 16777216.0f;   // 2^24 undoes the code scale; s/16 for KV8
+    static_assert(NG == 1 || (NG == 2 && D == 128), "groups");
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int g8 = C.H == 0 ? 1 : Hq / C.H, nq_all = M * g8;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / qtiles, qt = blockIdx.z % qtiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // the combine may be scheduled now; it waits (griddepcontrol.wait) for
+    // this grid to complete before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int Lb = min(len[b], C.L);
+    const int t_begin = split * kKvWarps * kBlk * nbw, t_end = min(t_begin + kKvWarps * kBlk * nbw, Lb);
+    if (t_begin >= Lb) return;                // past the sequence: the combine does not read this split
     const size_t rowbase = (static_cast<size_t>(b) * C.H + kvh) * C.L;
     const int gpr = D / C.G;
-    float mrun[kQvMax], lrun[kQvMax], acc[kQvMax][8];
+
+    // ---- this warp's blocks: K and V planes through a ring of kStages
+    // shared-memory stages (cp.async), all of its scales up front (by lanes)
+    unsigned char *wsm = sm + warp * Geo::WARP;
+    const int key_w = t_begin + warp * nbw * kBlk;               // first cache row of the warp
+    const int nblk = t_end > key_w ? min(nbw, (t_end - key_w + kBlk - 1) / kBlk) : 0;
+    const uint8_t *planes[4] = {C.kb, C.vb, C.kr, C.vr};
+    auto issue = [&](int bi) {
+        const uint32_t st = static_cast<uint32_t>(__cvta_generic_to_shared(wsm + (bi % kStages) * Geo::STAGE));
 #pragma unroll
-    for (int v = 0; v < kQvMax; ++v) {
-        mrun[v] = -INFINITY;
-        lrun[v] = 0.0f;
+        for (int pl = 0; pl < 2 * PLANES; ++pl) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[v][e] = 0.0f;
+            for (int qq = lane; qq < TILE / 16; qq += 32) {
+                const int r = qq / (RB / 16), c = qq % (RB / 16);
+                const int key = min(key_w + bi * kBlk + r, C.L - 1);
+                const uint8_t *src = planes[pl] + (rowbase + key) * RB + 16 * c;
+                const uint32_t dst = st + pl * TILE + swz<RB>(r, 16 * c);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+            }
+        }
+    };
+#pragma unroll
+    for (int bi = 0; bi < kStages; ++bi) {
+        if (bi < nblk) issue(bi);
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    const int t_begin = split * kSplit, t_end = min(t_begin + kSplit, Lb);
-    constexpr int LPR = D / 8, RPS = 32 / LPR;           // values: lanes per row, rows per step
-    const int half = lane / LPR, dl = lane % LPR;        // row offset within a step, dims 8 dl .. 8 dl + 7
-    for (int tb = t_begin + 32 * warp; tb < t_end; tb += 32 * kKvWarps) {
-        // ---- scores: lane = cache row tb + lane
-        const int t = tb + lane;
-        float sc[kQvMax];
+    // scales: [block][K / V][row][group] fp16
+    constexpr int PER_BLK = 2 * kBlk * NG;
+    unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + kStages * Geo::STAGE);
+    {
+        // every load first, then the stores (one exposed latency, not one per load)
+        constexpr int NSC = kMaxBlkPerWarp * PER_BLK / 32;
+        unsigned short sv[NSC];
 #pragma unroll
-        for (int v = 0; v < kQvMax; ++v) sc[v] = 0.0f;
-        if (t < t_end) {
-            const uint4 *kb4 = reinterpret_cast<const uint4 *>(C.kb + (rowbase + t) * (D / 2));
-            const uint4 *kr4 = reinterpret_cast<const uint4 *>(C.kr + (rowbase + t) * (D / 2));
+        for (int k = 0; k < NSC; ++k) {
+            const int e = lane + 32 * k;
+            const int bi = e / PER_BLK, rem = e % PER_BLK, which = rem / (kBlk * NG), idx = rem % (kBlk * NG);
+            const int key = min(key_w + bi * kBlk + idx / NG, C.L - 1);
+            const unsigned short *src = reinterpret_cast<const unsigned short *>(which ? C.vs : C.ks);
+            sv[k] = bi < nblk ? ld_nc_u16(src + (rowbase + key) * gpr + idx % NG) : static_cast<unsigned short>(0);
+        }
 #pragma unroll
-            for (int c4 = 0; c4 < DW / 4; ++c4) {
-                const uint4 bw = __ldg(kb4 + c4);
-                const uint4 rw = PLANES == 2 ? __ldg(kr4 + c4) : make_uint4(0, 0, 0, 0);
-                const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w}, rws[4] = {rw.x, rw.y, rw.z, rw.w};
+        for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
+    }
+
+    // ---- query fragments (A operand): rows g and g + 8 of the tile, scaled by
+    // scale log2(e) (scores in base 2), fp16, in the dimension order of the
+    // K fragments; and per group the offset term of the scores
+    uint32_t qa[HALVES][4][4];
+    float cinit[NG][2];
+    int lim[2];
+    {
+        float qsum[NG][2];
 #pragma unroll
-                for (int w4 = 0; w4 < 4; ++w4) {
-                    const int e0 = 8 * (4 * c4 + w4);
-                    const float s = __half2float(C.ks[(rowbase + t) * gpr + e0 / C.G]);
-                    float kv[8];
-                    decode8<PLANES>(bws[w4], rws[w4], s, kv);
+        for (int gr = 0; gr < NG; ++gr) qsum[gr][0] = qsum[gr][1] = 0.0f;
+        const float qs = scale * 1.4426950408889634f;
 #pragma unroll
-                    for (int v = 0; v < kQvMax; ++v) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(&qs[v][e0]);
-                        const float4 qb = *reinterpret_cast<const float4 *>(&qs[v][e0 + 4]);
-                        float a = sc[v];
-                        a = fmaf(qa.x, kv[0], a); a = fmaf(qa.y, kv[1], a); a = fmaf(qa.z, kv[2], a);
-                        a = fmaf(qa.w, kv[3], a); a = fmaf(qb.x, kv[4], a); a = fmaf(qb.y, kv[5], a);
-                        a = fmaf(qb.z, kv[6], a); a = fmaf(qb.w, kv[7], a);
-                        sc[v] = a;
-                    }
+        for (int rr = 0; rr < 2; ++rr) {
+            const int v = qt * kQTile + g + 8 * rr;
+            const bool valid = v < nq_all;
+            const int m = valid ? v / g8 : 0, hq = kvh * g8 + (valid ? v % g8 : 0);
+            lim[rr] = valid ? Lb - (M - 1 - m) : Lb;
+            const float *qrow = q + ((static_cast<size_t>(b) * M + m) * Hq + hq) * D;
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                float x[16];
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    float4 f = valid ? *reinterpret_cast<const float4 *>(qrow + 64 * h + 16 * t + 4 * j4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[4 * j4] = __half2float(__float2half_rn(__fmul_rn(f.x, qs)));
+                    x[4 * j4 + 1] = __half2float(__float2half_rn(__fmul_rn(f.y, qs)));
+                    x[4 * j4 + 2] = __half2float(__float2half_rn(__fmul_rn(f.z, qs)));
+                    x[4 * j4 + 3] = __half2float(__float2half_rn(__fmul_rn(f.w, qs)));
+                }
+                float sum = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sum += x[j];
+                qsum[NG == 2 ? h : 0][rr] += sum;
+                // slice sl: word w = sl / 2 of the lane's 16 dimensions, nibbles
+                // i0, i0 + 4 (k = 2t, 2t + 1) and i0 + 1, i0 + 5 (k = 2t + 8, 2t + 9)
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) {
+                    const int w = sl >> 1, i0 = 2 * (sl & 1);
+                    // A-fragment registers: (row g, k 2t..2t+1), (row g + 8, same),
+                    // (row g, k 2t+8..2t+9), (row g + 8, same)
+                    qa[h][sl][rr] = h2_pack(x[8 * w + i0], x[8 * w + i0 + 4]);
+                    qa[h][sl][2 + rr] = h2_pack(x[8 * w + i0 + 1], x[8 * w + i0 + 5]);
                 }
             }
         }
-        // ---- online softmax per query vector (rows beyond a vector's limit: -inf)
-        float p[kQvMax];
 #pragma unroll
-        for (int v = 0; v < kQvMax; ++v) {
-            const float s = (t < t_end && t < lim[v]) ? sc[v] : -INFINITY;
-            float mb = s;
+        for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-            const float mn = fmaxf(mrun[v], mb);
-            const float alpha = mn == -INFINITY ? 1.0f : __expf(mrun[v] - mn);
-            p[v] = mn == -INFINITY ? 0.0f : __expf(s - mn);
-            float ps = p[v];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            lrun[v] = fmaf(lrun[v], alpha, ps);
-            mrun[v] = mn;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[v][e] *= alpha;
-        }
-        // ---- values: row tb + RPS i + half, dims 8 dl .. 8 dl + 7
-        const int nrow = min(32, t_end - tb);
-        for (int i = 0; RPS * i < nrow; ++i) {
-            const int r = RPS * i + half;
-            const int tt = tb + r;
-            float vv[8];
-            if (r < nrow) {
-                const size_t row = rowbase + tt;
-                const uint32_t bw = __ldg(reinterpret_cast<const uint32_t *>(C.vb + row * (D / 2)) + dl);
-                const uint32_t rw = PLANES == 2 ? __ldg(reinterpret_cast<const uint32_t *>(C.vr + row * (D / 2)) + dl) : 0u;
-                decode8<PLANES>(bw, rw, __half2float(C.vs[row * gpr + (8 * dl) / C.G]), vv);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vv[e] = 0.0f;
+            for (int rr = 0; rr < 2; ++rr) {
+                float v = qsum[gr][rr];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                cinit[gr][rr] = -static_cast<float>(OFF) * 5.9604644775390625e-08f * v;
             }
-#pragma unroll
-            for (int v = 0; v < kQvMax; ++v) {
-                const float pr = __shfl_sync(0xffffffffu, p[v], r < 32 ? r : 0);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[v][e] = fmaf(pr, vv[e], acc[v][e]);
-            }
-        }
     }
-    // ---- merge the row groups of the warp, then the warps of the CTA
+
+    float o[HALVES * 8][4];
 #pragma unroll
-    for (int o = LPR; o < 32; o <<= 1)
+    for (int nt = 0; nt < HALVES * 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.0f, 0.0f}, sig[NG][4];
 #pragma unroll
-        for (int v = 0; v < kQvMax; ++v)
+    for (int gr = 0; gr < NG; ++gr) sig[gr][0] = sig[gr][1] = sig[gr][2] = sig[gr][3] = 0.0f;
+    // the lowest row limit of the warp's query rows: blocks below it need no mask
+    int limw = min(t_end, RR == 2 ? min(lim[0], lim[1]) : lim[0]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[v][e] += __shfl_xor_sync(0xffffffffu, acc[v][e], o);
-    if (lane == 0)
-        for (int v = 0; v < kQvMax; ++v) { red_m[warp][v] = mrun[v]; red_l[warp][v] = lrun[v]; }
-    if (half == 0)
-        for (int v = 0; v < kQvMax; ++v)
+    for (int o2 = 1; o2 < 32; o2 <<= 1) limw = min(limw, __shfl_xor_sync(0xffffffffu, limw, o2));
+    for (int bi = 0; bi < nblk; ++bi) {
+        // kStages groups are outstanding here; block bi's is the oldest
+        asm volatile("cp.async.wait_group %0;" :: "n"(kStages - 1) : "memory");
+        __syncwarp();
+        const unsigned char *st = wsm + (bi % kStages) * Geo::STAGE;
+        const int key0 = key_w + bi * kBlk;
+        // ---- S = Q K^T: key tile kt holds cache rows kappa(8 kt + n) = 4 (n / 2) + 2 kt + n % 2
+        // one accumulator per (half, key tile): four independent MMA chains;
+        // the offset term enters through the first half of each group
+        float acc[HALVES][2][4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) red_o[warp][v][8 * dl + e] = acc[v][e];
+        for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                const bool first = NG == 2 || h == 0;
+                acc[h][kt][0] = acc[h][kt][1] = first ? cinit[NG == 2 ? h : 0][0] : 0.0f;
+                acc[h][kt][2] = acc[h][kt][3] = first ? cinit[NG == 2 ? h : 0][1] : 0.0f;
+            }
+        uint32_t xb[2][HALVES][2], xr[2][HALVES][2];
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+            const int kr = 4 * (g >> 1) + 2 * kt + (g & 1);
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                const uint2 wb = *reinterpret_cast<const uint2 *>(st + swz<RB>(kr, 32 * h + 8 * t));
+                uint2 wr = make_uint2(0u, 0u);
+                if constexpr (PLANES == 2) wr = *reinterpret_cast<const uint2 *>(st + 2 * TILE + swz<RB>(kr, 32 * h + 8 * t));
+                xb[kt][h][0] = PLANES == 2 ? wb.x ^ 0x88888888u : wb.x;
+                xb[kt][h][1] = PLANES == 2 ? wb.y ^ 0x88888888u : wb.y;
+                xr[kt][h][0] = wr.x ^ 0x88888888u;
+                xr[kt][h][1] = wr.y ^ 0x88888888u;
+            }
+        }
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const int w = sl >> 1, i0 = 2 * (sl & 1);
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t b0 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0);
+                    const uint32_t b1 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0 + 1);
+                    mma16816(acc[h][kt], qa[h][sl], b0, b1);
+                }
+        }
+        // ---- scores of rows (g, g + 8) x cache rows 4t + kk, kk = 0..3, then the
+        // online softmax (base 2) and P' = p times the V row's group scale.
+        // Masking (rows past the split or past a query row's causal limit)
+        // is only needed where the block reaches the warp's lowest limit.
+        float sk[4][NG], sv[4][NG];
+        {
+            const unsigned short *sc = ssm + bi * 2 * kBlk * NG;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    sk[kk][gr] = __fmul_rn(__half2float(__ushort_as_half(sc[(4 * t + kk) * NG + gr])), FK);
+                    const float v = __half2float(__ushort_as_half(sc[kBlk * NG + (4 * t + kk) * NG + gr]));
+                    sv[kk][gr] = PLANES == 2 ? __fmul_rn(v, 0.0625f) : v;
+                }
+        }
+        float alpha[2] = {1.0f, 1.0f};
+        uint32_t pa[NG][4];
+        auto softmax_block = [&](auto mask_c) {
+            constexpr bool MASK = decltype(mask_c)::value;
+#pragma unroll
+            for (int rr = 0; rr < RR; ++rr) {
+                float sr[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    float v = 0.0f;
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        v = fmaf(sk[kk][NG == 2 ? h : 0], acc[h][kk >> 1][(kk & 1) + 2 * rr], v);
+                    if constexpr (MASK) {
+                        const int key = key0 + 4 * t + kk;
+                        v = (key < t_end && key < lim[rr]) ? v : -INFINITY;
+                    }
+                    sr[kk] = v;
+                }
+                float mx = fmaxf(fmaxf(sr[0], sr[1]), fmaxf(sr[2], sr[3]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mn = fmaxf(mrun[rr], mx);
+                // no earlier row: the state is all zeros, any factor does
+                alpha[rr] = mrun[rr] == -INFINITY ? 0.0f : ex2(mrun[rr] - mn);
+                mrun[rr] = mn;
+                float pr[4], ps = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    pr[kk] = MASK ? (sr[kk] == -INFINITY ? 0.0f : ex2(sr[kk] - mn)) : ex2(sr[kk] - mn);
+                    ps += pr[kk];
+                }
+                lrun[rr] = fmaf(lrun[rr], alpha[rr], ps);
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    float pw[4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)     // masked rows may hold any scale bits: keep them out
+                        pw[kk] = MASK ? (pr[kk] > 0.0f ? __fmul_rn(pr[kk], sv[kk][gr]) : 0.0f) : __fmul_rn(pr[kk], sv[kk][gr]);
+                    pa[gr][rr] = h2_pack(pw[0], pw[1]);       // (row, cache rows 4t, 4t + 1) = k 2t, 2t + 1
+                    pa[gr][2 + rr] = h2_pack(pw[2], pw[3]);   // (row, cache rows 4t + 2, 4t + 3) = k 2t + 8, 2t + 9
+                }
+            }
+            if constexpr (RR == 1) {
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) pa[gr][1] = pa[gr][3] = 0u;   // rows 8..15 hold no query
+            }
+        };
+        if (key0 + kBlk <= limw) softmax_block(std::false_type{});
+        else softmax_block(std::true_type{});
+        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+            for (int nt = 0; nt < HALVES * 8; ++nt) {
+                o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
+                o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+            }
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                sig[gr][0] *= alpha[0]; sig[gr][1] *= alpha[0];
+                sig[gr][2] *= alpha[1]; sig[gr][3] *= alpha[1];
+            }
+        }
+        // sum of P' per row and group through the tensor cores: B = all ones
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) mma16816(sig[gr], pa[gr], 0x3C003C00u, 0x3C003C00u);
+        // ---- O += P' V: n-tile (h, i) holds dimension 64 h + 8 n + i in column n
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            uint32_t vb[4], vr[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                vb[kk] = *reinterpret_cast<const uint32_t *>(st + TILE + swz<RB>(4 * t + kk, 32 * h + 4 * g));
+                if constexpr (PLANES == 2) {
+                    vr[kk] = *reinterpret_cast<const uint32_t *>(st + 3 * TILE + swz<RB>(4 * t + kk, 32 * h + 4 * g)) ^ 0x88888888u;
+                    vb[kk] ^= 0x88888888u;
+                } else {
+                    vr[kk] = 0u;
+                }
+            }
+            // byte-interleave cache rows (4t, 4t + 1) and (4t + 2, 4t + 3): nibble i
+            // of the first row of a pair lands at bit 4 i, of the second at 16 + 4 i
+            const uint32_t u0[2] = {__byte_perm(vb[0], vb[1], 0x5410), __byte_perm(vb[0], vb[1], 0x7632)};
+            const uint32_t u1[2] = {__byte_perm(vb[2], vb[3], 0x5410), __byte_perm(vb[2], vb[3], 0x7632)};
+            uint32_t r0[2] = {0u, 0u}, r1[2] = {0u, 0u};
+            if constexpr (PLANES == 2) {
+                r0[0] = __byte_perm(vr[0], vr[1], 0x5410); r0[1] = __byte_perm(vr[0], vr[1], 0x7632);
+                r1[0] = __byte_perm(vr[2], vr[3], 0x5410); r1[1] = __byte_perm(vr[2], vr[3], 0x7632);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t b0 = code_pair<PLANES>(u0[i >> 2], r0[i >> 2], i & 3);
+                const uint32_t b1 = code_pair<PLANES>(u1[i >> 2], r1[i >> 2], i & 3);
+                mma16816(o[8 * h + i], pa[NG == 2 ? h : 0], b0, b1);
+            }
+        }
+        __syncwarp();                           // every lane is done with this stage: refill it
+        if (bi + kStages < nblk) issue(bi + kStages);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    // finish the pipeline (blocks past this warp's range were committed empty)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+    // ---- the warp's state: l summed over the four lanes of a row; the P'
+    // sums (every column of sig holds its row's sum); O = 2^24 acc - off sum(P')
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 1);
+        lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 2);
+    }
+    __syncthreads();                           // every warp is done with its stages
+    float *red_m = reinterpret_cast<float *>(sm);                 // [warp][row]
+    float *red_l = red_m + kKvWarps * kQTile;                     // [warp][row]
+    float *red_o = red_l + kKvWarps * kQTile;                     // [warp][row][D]
+#pragma unroll
+    for (int rr = 0; rr < RR; ++rr) {
+        const int row = g + 8 * rr;
+        if (t == 0) {
+            red_m[warp * kQTile + row] = mrun[rr];
+            red_l[warp * kQTile + row] = lrun[rr];
+        }
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int n = 2 * t + cc, dim = 64 * h + 8 * n + i;
+                    const float val = fmaf(16777216.0f, o[8 * h + i][2 * rr + cc],
+                                           -static_cast<float>(OFF) * sig[NG == 2 ? h : 0][2 * rr]);
+                    red_o[(warp * kQTile + row) * D + dim] = val;
+                }
+    }
     __syncthreads();
+    const int nqv = min(kQTile, nq_all - qt * kQTile);
     for (int i = threadIdx.x; i < nqv * (D + 2); i += kKvWarps * 32) {
-        const int v = i / (D + 2), j = i % (D + 2);
+        const int r = i / (D + 2), j = i % (D + 2);
         float M2 = -INFINITY;
-        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w][v]);
+#pragma unroll
+        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w * kQTile + r]);
         float val = 0.0f;
         if (j == D) {
             val = M2;
         } else {
+#pragma unroll
             for (int w = 0; w < kKvWarps; ++w) {
-                const float f = red_m[w][v] == -INFINITY ? 0.0f : __expf(red_m[w][v] - M2);
-                val += f * (j == D + 1 ? red_l[w][v] : red_o[w][v][j]);
+                const float mw = red_m[w * kQTile + r];
+                const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M2);
+                val = fmaf(f, j == D + 1 ? red_l[w * kQTile + r] : red_o[(w * kQTile + r) * D + j], val);
             }
         }
-        const int vv = qv0 + v, m = vv / g, hq = kvh * g + vv % g;
+        const int v = qt * kQTile + r, m = v / g8, hq = kvh * g8 + v % g8;
         part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
     }
 }
 
-// out[b][m][hq][:] = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s over the splits.
+// out[b][m][hq][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the
+// splits that hold rows of the sequence (maxima in base 2).  One CTA per
+// output vector: warp w merges splits w, w + 8, ... (lane l holds dimensions
+// l, l + 32, ...), then the eight warps merge in shared memory.
+constexpr int kCombWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(D)
-attn_combine_kernel(const float *__restrict__ part, int nsplit, float *__restrict__ out)
+__global__ void __launch_bounds__(kCombWarps * 32)
+attn_combine_kernel(const float *__restrict__ part, int nsplit, int split_rows, const int32_t *__restrict__ len,
+                    int L, int MHq, float *__restrict__ out)
 {
+    constexpr int DPL = D / 32;
+    __shared__ float sm_m[kCombWarps], sm_l[kCombWarps], sm_o[kCombWarps][D];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t vec = blockIdx.x;            // (b, m, hq)
-    const float *p = part + vec * nsplit * (D + 2);
-    float M2 = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M2 = fmaxf(M2, p[static_cast<size_t>(s) * (D + 2) + D]);
-    float num = 0.0f, den = 0.0f;
-    for (int s = 0; s < nsplit; ++s) {
-        const float ms = p[static_cast<size_t>(s) * (D + 2) + D];
-        if (ms == -INFINITY) continue;
-        const float f = __expf(ms - M2);
-        num = fmaf(f, p[static_cast<size_t>(s) * (D + 2) + threadIdx.x], num);
-        den = fmaf(f, p[static_cast<size_t>(s) * (D + 2) + D + 1], den);
+    const int b = static_cast<int>(vec / MHq);
+    const int Lb = min(len[b], L);
+    const int ns = min(nsplit, (Lb + split_rows - 1) / split_rows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float m = -INFINITY, l = 0.0f, o[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = 0.0f;
+    for (int sp = warp; sp < ns; sp += kCombWarps) {
+        const float *p = part + (vec * nsplit + sp) * (D + 2);
+        const float ms = p[D];
+        if (ms == -INFINITY) continue;        // no visible row in this split (warp-uniform)
+        const float ls = p[D + 1];
+        const float mn = fmaxf(m, ms);
+        const float a = m == -INFINITY ? 0.0f : exp2f(m - mn), f = exp2f(ms - mn);
+        l = fmaf(l, a, f * ls);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = fmaf(o[e], a, f * p[lane + 32 * e]);
+        m = mn;
     }
-    out[vec * D + threadIdx.x] = den > 0.0f ? num / den : 0.0f;
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) sm_o[warp][lane + 32 * e] = o[e];
+    __syncthreads();
+    for (int j = threadIdx.x; j < D; j += kCombWarps * 32) {
+        float M2 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCombWarps; ++w) M2 = fmaxf(M2, sm_m[w]);
+        float num = 0.0f, den = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kCombWarps; ++w) {
+            if (sm_m[w] == -INFINITY) continue;
+            const float f = exp2f(sm_m[w] - M2);
+            num = fmaf(f, sm_o[w][j], num);
+            den = fmaf(f, sm_l[w], den);
+        }
+        out[vec * D + j] = den > 0.0f ? num / den : 0.0f;
+    }
 }
 
-template <int PLANES, int D>
-void launch_attn_qv(int qv, dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq, const int32_t *len,
-                    float scale, float *part, int nsplit)
+template <int PLANES, int D, int NG, int RR>
+cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq, const int32_t *len,
+                          float scale, float *part, int nsplit, int qtiles, int nbw)
 {
-    switch (qv) {
-    case 1: attn_split_kernel<PLANES, D, 1><<<grid, kKvWarps * 32, 0, s>>>(C, q, M, Hq, len, scale, part, nsplit); break;
-    case 2: attn_split_kernel<PLANES, D, 2><<<grid, kKvWarps * 32, 0, s>>>(C, q, M, Hq, len, scale, part, nsplit); break;
-    case 4: attn_split_kernel<PLANES, D, 4><<<grid, kKvWarps * 32, 0, s>>>(C, q, M, Hq, len, scale, part, nsplit); break;
-    default: attn_split_kernel<PLANES, D, kQvCap><<<grid, kKvWarps * 32, 0, s>>>(C, q, M, Hq, len, scale, part, nsplit); break;
+    constexpr int smem = AttnGeo<PLANES, D>::SMEM;
+    static std::atomic<bool> done[64];          // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev].load()) {
+        e = cudaFuncSetAttribute(attn_split_kernel<PLANES, D, NG, RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem);
+        if (e != cudaSuccess) return e;
+        done[dev].store(true);
     }
+    attn_split_kernel<PLANES, D, NG, RR><<<grid, kKvWarps * 32, smem, s>>>(C, q, M, Hq, len, scale, part, nsplit,
+                                                                           qtiles, nbw);
+    return cudaGetLastError();
 }
-void launch_attn(int planes, int d, int qv, dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq,
-                 const int32_t *len, float scale, float *part, int nsplit)
+template <int PLANES, int D, int NG>
+cudaError_t launch_attn_r(int rr, dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq,
+                          const int32_t *len, float scale, float *part, int nsplit, int qtiles, int nbw)
+{
+    return rr == 1 ? launch_attn_t<PLANES, D, NG, 1>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                   : launch_attn_t<PLANES, D, NG, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
+}
+cudaError_t launch_attn(int planes, int d, int ng, int rr, dim3 grid, cudaStream_t s, Cache C, const float *q, int M,
+                        int Hq, const int32_t *len, float scale, float *part, int nsplit, int qtiles, int nbw)
 {
     if (d == 128) {
-        if (planes == 1) launch_attn_qv<1, 128>(qv, grid, s, C, q, M, Hq, len, scale, part, nsplit);
-        else launch_attn_qv<2, 128>(qv, grid, s, C, q, M, Hq, len, scale, part, nsplit);
-    } else {
-        if (planes == 1) launch_attn_qv<1, 64>(qv, grid, s, C, q, M, Hq, len, scale, part, nsplit);
-        else launch_attn_qv<2, 64>(qv, grid, s, C, q, M, Hq, len, scale, part, nsplit);
+        if (ng == 2)
+            return planes == 1 ? launch_attn_r<1, 128, 2>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                               : launch_attn_r<2, 128, 2>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
+        return planes == 1 ? launch_attn_r<1, 128, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                           : launch_attn_r<2, 128, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
     }
+    return planes == 1 ? launch_attn_r<1, 64, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                       : launch_attn_r<2, 64, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
 }
 
 nq_status check_cache(const nq_kv_cache *c)
@@ -319,7 +624,9 @@ nq_status check_cache(const nq_kv_cache *c)
     return NQ_OK;
 }
 
-int n_splits(int max_len) { return (max_len + kSplit - 1) / kSplit; }
+// splits of a call with nbw blocks per warp; the workspace is sized for the
+// smallest split (most of them)
+int n_splits(int max_len, int nbw = kMinBlkPerWarp) { return (max_len + kKvWarps * kBlk * nbw - 1) / (kKvWarps * kBlk * nbw); }
 
 }  // namespace
 }  // namespace nq
@@ -385,22 +692,42 @@ extern "C" nq_status nq_attn_decode(const nq_kv_cache *cache, const float *q, in
     if (!nq::aligned16(q) || !nq::aligned16(out) || (reinterpret_cast<uintptr_t>(len) & 3u)) return NQ_ERR_ALIGN;
     if (!ws || ws_bytes < nq_attn_workspace_bytes(c.batch, M, heads_q, c.head_dim, c.max_len)) return NQ_ERR_WORKSPACE;
     if (!nq::aligned16(ws)) return NQ_ERR_ALIGN;
-    const int nsplit = nq::n_splits(c.max_len);
     const int g = heads_q / c.heads_kv, nq_all = M * g;
-    const int qv = nq_all <= 1 ? 1 : (nq_all <= 2 ? 2 : (nq_all <= 4 ? 4 : nq::kQvCap));
-    const int qgroups = (nq_all + qv - 1) / qv;
-    if (static_cast<long long>(c.batch) * qgroups > 65535) return NQ_ERR_SHAPE;
+    const int qtiles = (nq_all + nq::kQTile - 1) / nq::kQTile;
+    if (static_cast<long long>(c.batch) * qtiles > 65535 || c.heads_kv > 65535) return NQ_ERR_SHAPE;
+    // the longest splits (fewest CTAs, least per-CTA work) that still give
+    // every SM about six CTAs
+    const long long units = static_cast<long long>(c.batch) * c.heads_kv * qtiles;
+    int nbw = nq::kMaxBlkPerWarp;
+    while (nbw > nq::kMinBlkPerWarp && units * nq::n_splits(c.max_len, nbw) < 6LL * nq::sm_count()) nbw /= 2;
+    const int nsplit = nq::n_splits(c.max_len, nbw);
     nq::Cache C{c.batch, c.heads_kv, c.head_dim, c.group, c.max_len,
                 static_cast<const uint8_t *>(c.k_base), static_cast<const uint8_t *>(c.k_resid),
                 static_cast<const uint8_t *>(c.v_base), static_cast<const uint8_t *>(c.v_resid),
                 static_cast<const __half *>(c.k_scales), static_cast<const __half *>(c.v_scales)};
     float *part = static_cast<float *>(ws);
-    dim3 grid(nsplit, c.heads_kv, c.batch * qgroups);
-    nq::launch_attn(planes, c.head_dim, qv, grid, stream, C, q, M, heads_q, len, scale, part, nsplit);
-    cudaError_t e = cudaGetLastError();
+    dim3 grid(nsplit, c.heads_kv, c.batch * qtiles);
+    cudaError_t e = nq::launch_attn(planes, c.head_dim, c.head_dim / c.group, nq_all <= 8 ? 1 : 2, grid, stream, C,
+                                    q, M, heads_q, len, scale, part, nsplit, qtiles, nbw);
     if (e != cudaSuccess) return NQ_ERR_CUDA;
     const int nvec = c.batch * M * heads_q;
-    if (c.head_dim == 128) nq::attn_combine_kernel<128><<<nvec, 128, 0, stream>>>(part, nsplit, out);
-    else nq::attn_combine_kernel<64><<<nvec, 64, 0, stream>>>(part, nsplit, out);
-    return nq::cuda_status(cudaGetLastError());
+    const int rows = nq::kKvWarps * nq::kBlk * nbw;
+    // the combine as a programmatic dependent launch: its launch overlaps the
+    // split kernel's tail, griddepcontrol.wait orders its reads after it
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nvec);
+    cfg.blockDim = dim3(nq::kCombWarps * 32);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float *cpart = part;
+    const int mhq = M * heads_q;
+    if (c.head_dim == 128)
+        e = cudaLaunchKernelEx(&cfg, nq::attn_combine_kernel<128>, cpart, nsplit, rows, len, c.max_len, mhq, out);
+    else
+        e = cudaLaunchKernelEx(&cfg, nq::attn_combine_kernel<64>, cpart, nsplit, rows, len, c.max_len, mhq, out);
+    return nq::cuda_status(e);
 }

@@ -5,7 +5,9 @@ cache; accepted entries stay, the rejected suffix is discarded).
 Appending quantises rows exactly like the weights (bit-exact against the
 oracle's pack of the same rows); attention over either view agrees with the
 oracle's fp64 attention over the same dequantised rows (normwise, per output
-vector, far inside the linears' 2e-3).
+vector, within the linears' 2e-3: the kernel feeds the tensor cores fp16
+queries and fp16 probabilities, about 2^-11 relative each, and accumulates in
+fp32).
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ from quantized_self_speculative_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-4
+TOL = 2e-3
 
 
 def rows(seed, *shape):
