@@ -24,6 +24,11 @@ int sm_count();
 
 inline nq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA; }
 
+// Int8-activation linears on the streaming weight kernel (nq_linear.cu);
+// arguments already checked.
+nq_status linear_a8_entry(int count, const nq_weights *w, const int8_t *const *xq, const float *const *sx, int M,
+                          bool verify, float *const *y, cudaStream_t stream);
+
 // ---------------------------------------------------------------- device side
 __device__ __forceinline__ void set_status(unsigned int *status, unsigned int bits)
 {

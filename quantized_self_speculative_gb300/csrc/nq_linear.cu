@@ -64,7 +64,8 @@ struct Prob {
     const uint8_t *base;
     const uint8_t *resid;
     const void *scales;
-    const uint16_t *x;
+    const void *x;          // bf16 [M][k], or int8 codes [M][k] when the batch is a8
+    const float *sx;        // a8: the activation rows' scales [M]
     float *y;
     long long cost_begin;   // sum over earlier problems of units * k (load balancing)
     int n, k, unit_begin, pad;
@@ -74,6 +75,7 @@ template <int MAXP>
 struct Batch {
     long long total_cost;
     int count, total_units, M, xs_bytes;
+    int a8, pad;            // a8: int8 activation codes (exact in fp16), y scaled by sx
     Prob p[MAXP];
 };
 
@@ -273,7 +275,8 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     int c_N = 0, c_ng = 0, c_K = 0, c_rg = 0;
     bool in_unit = false;
     int staged_pi = -1, staged_begin = -1, cps = 1, RS = 0;
-    const uint16_t *c_x = nullptr;
+    const void *c_x = nullptr;
+    const float *c_sx = nullptr;
     float *c_y = nullptr;
     const float *c_rs = nullptr;   // FP8 row scales
     unsigned char *xs = smem;
@@ -291,14 +294,24 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         for (int i = threadIdx.x; i < total_pad; i += THREADS) {
             const bool valid = i < total;
             const int m = valid ? i / items_row : 0, it = valid ? i % items_row : 0;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid)
-                v = *reinterpret_cast<const uint4 *>(c_x + static_cast<size_t>(m) * c_K +
-                                                     static_cast<size_t>(c_begin) * CH + it * 8);
-            const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-            const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-            const float x4 = __uint_as_float(v.z << 16), x5 = __uint_as_float(v.z & 0xFFFF0000u);
-            const float x6 = __uint_as_float(v.w << 16), x7 = __uint_as_float(v.w & 0xFFFF0000u);
+            const size_t xoff = static_cast<size_t>(m) * c_K + static_cast<size_t>(c_begin) * CH + it * 8;
+            float x0, x1, x2, x3, x4, x5, x6, x7;
+            if (B.a8) {
+                // eight int8 codes (|code| <= 127: exact in fp16, and so is code / 16)
+                uint2 v = make_uint2(0u, 0u);
+                if (valid) v = *reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(c_x) + xoff);
+                x0 = static_cast<float>(static_cast<int8_t>(v.x)); x1 = static_cast<float>(static_cast<int8_t>(v.x >> 8));
+                x2 = static_cast<float>(static_cast<int8_t>(v.x >> 16)); x3 = static_cast<float>(static_cast<int8_t>(v.x >> 24));
+                x4 = static_cast<float>(static_cast<int8_t>(v.y)); x5 = static_cast<float>(static_cast<int8_t>(v.y >> 8));
+                x6 = static_cast<float>(static_cast<int8_t>(v.y >> 16)); x7 = static_cast<float>(static_cast<int8_t>(v.y >> 24));
+            } else {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid) v = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(c_x) + xoff);
+                x0 = __uint_as_float(v.x << 16); x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                x2 = __uint_as_float(v.y << 16); x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                x4 = __uint_as_float(v.z << 16); x5 = __uint_as_float(v.z & 0xFFFF0000u);
+                x6 = __uint_as_float(v.w << 16); x7 = __uint_as_float(v.w & 0xFFFF0000u);
+            }
             const float amax = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
                                      fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
             range |= amax > 65504.0f;
@@ -352,7 +365,10 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
                 float val = y[nt][e];
                 if constexpr (KIND != kNib) val = __fadd_rn(val, y2[nt][e]);
                 if constexpr (KIND == kFp8) val = __fmul_rn(e < 2 ? rs0 : rs1, val);
-                if (m < M && row < c_N) c_y[static_cast<size_t>(m) * c_N + row] = val;
+                if (m < M && row < c_N) {
+                    if (B.a8) val = __fmul_rn(c_sx[m], val);
+                    c_y[static_cast<size_t>(m) * c_N + row] = val;
+                }
             }
         }
     };
@@ -366,7 +382,7 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
         }
         if (!in_unit) {
             const Prob &P = B.p[c_pi];
-            c_N = P.n; c_K = P.k; c_ng = c_K / CH; c_x = P.x; c_y = P.y;
+            c_N = P.n; c_K = P.k; c_ng = c_K / CH; c_x = P.x; c_sx = P.sx; c_y = P.y;
             c_rs = static_cast<const float *>(P.scales);
             c_rg = (c_u - P.unit_begin) * ROWS + warp * 16 + g;
             c_grp = 0;
@@ -621,8 +637,8 @@ int xs_bytes_for(int kind, int M, int kmax, int group, int warps)
 }
 
 template <int MAXP>
-nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, int M, float *const *y,
-                    int kind, int planes, int group, cudaStream_t stream)
+nq_status run_batch(int count, const nq_weights *w, const void *const *x, int M, float *const *y,
+                    int kind, int planes, int group, cudaStream_t stream, const float *const *sx = nullptr)
 {
     unsigned int *status = device_status_ptr();
     if (!status) return NQ_ERR_CUDA;
@@ -652,7 +668,9 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
                 p.base = static_cast<const uint8_t *>(L.base);
                 p.resid = static_cast<const uint8_t *>(L.resid);
                 p.scales = L.scales;
-                p.x = x[i0 + i] + static_cast<size_t>(m0) * L.k_in;
+                // bf16 rows (2 bytes an input) or, with sx, int8 codes (1 byte)
+                p.x = static_cast<const char *>(x[i0 + i]) + static_cast<size_t>(m0) * L.k_in * (sx ? 1 : 2);
+                p.sx = sx ? sx[i0 + i] + m0 : nullptr;
                 p.y = y[i0 + i] + static_cast<size_t>(m0) * L.n_out;
                 p.n = L.n_out;
                 p.k = L.k_in;
@@ -668,6 +686,7 @@ nq_status run_batch(int count, const nq_weights *w, const uint16_t *const *x, in
             b.count = cnt;
             b.total_units = static_cast<int>(units);
             b.M = Mc;
+            b.a8 = sx ? 1 : 0;
             b.xs_bytes = xs_bytes_for(kind, Mc, kmax, group, warps);
             const cudaError_t e = launch_kind<MAXP>(kind, planes, group, nt, warps, b, stream, status);
             if (e != cudaSuccess) return NQ_ERR_CUDA;
@@ -698,11 +717,27 @@ nq_status linear_entry(int count, const nq_weights *w, const uint16_t *const *x,
         if (!aligned16(ws)) return NQ_ERR_ALIGN;
         return tc_run(count, w, x, M, y, verify, ws, stream);
     }
-    return count <= kSmallBatch ? run_batch<kSmallBatch>(count, w, x, M, y, kind, planes, group, stream)
-                                : run_batch<kLargeBatch>(count, w, x, M, y, kind, planes, group, stream);
+    const void *const *xv = reinterpret_cast<const void *const *>(x);
+    return count <= kSmallBatch ? run_batch<kSmallBatch>(count, w, xv, M, y, kind, planes, group, stream)
+                                : run_batch<kLargeBatch>(count, w, xv, M, y, kind, planes, group, stream);
 }
 
 }  // namespace
+
+// Int8-activation linears (nested planes: NESTED44 both planes or one, INT4
+// base plane) on the streaming kernel: the codes are staged like bf16
+// activations (exactly, as fp16), every per-group dot of codes is exact in the
+// fp32 accumulators, y = s_x sum_g s_g dot_g.  Arguments checked by the caller.
+nq_status linear_a8_entry(int count, const nq_weights *w, const int8_t *const *xq, const float *const *sx, int M,
+                          bool verify, float *const *y, cudaStream_t stream)
+{
+    const int group = w[0].group;
+    const void *const *xv = reinterpret_cast<const void *const *>(xq);
+    return count <= kSmallBatch
+               ? run_batch<kSmallBatch>(count, w, xv, M, y, kNib, verify ? 2 : 1, group, stream, sx)
+               : run_batch<kLargeBatch>(count, w, xv, M, y, kNib, verify ? 2 : 1, group, stream, sx);
+}
+
 }  // namespace nq
 
 extern "C" nq_status nq_draft_gemv(const nq_weights *w, const uint16_t *x, int M, float *y, cudaStream_t stream)
