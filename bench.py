@@ -448,8 +448,9 @@ class RoundLoop:
 def a8_sweep(device, iters=10):
     """BitNest's own precision (Table 1, "W4A8 -> W8A8"): the LLaMA-2-7B pass
     with int8 activation codes, draft at M = 1 (base plane) and verify at
-    M = k+1 = 5 (both planes), integer dots on the CUDA cores; plus the
-    per-row activation quantiser over one [M][4096] input.  Algorithmic bytes
+    M = k+1 = 5 (both planes), exact group dots on the streaming weight kernel
+    (warp MMA); plus the per-row activation quantiser over one [M][4096] input
+    (100 back-to-back calls, launch overhead included).  Algorithmic bytes
     as for the bf16-activation passes with 1-byte activations."""
     import torch
     from quantized_self_speculative_gb300 import nq, synth
