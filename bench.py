@@ -816,6 +816,25 @@ def profile_case(case, layers=8):
         M = {"draft": 1, "verify": 5, "draft16": 16, "verify144": 144, "int4": 1, "fp8": 5, "fp16": 5}[case]
         print(json.dumps({"case": case, **_time_pass(device, L, M, case not in ("draft", "draft16", "int4"), iters=2,
                                                       tensor_cores=case in ("draft16", "verify144"))}))
+    elif case in ("kv4", "kv8"):
+        # one LLaMA-2-7B-32K layer's cache (32 kv heads x 128, 32K rows; 276 MB
+        # of planes, beyond L2), the draft (KV4, M = 1) or verify (KV8, M = 5) read
+        planes = 1 if case == "kv4" else 2
+        M, ctx, H, d = (1 if planes == 1 else K_DRAFT + 1), 32768, 32, 128
+        gen = torch.Generator(device=device)
+        gen.manual_seed(5)
+        c = nq.KVCache(1, H, d, GROUP, ctx + 16, device)
+        for lo in range(0, ctx, 4096):
+            kv = torch.randn((1, H, 4096, d), generator=gen, device=device)
+            c.append(kv, kv, torch.tensor([lo], dtype=torch.int32, device=device))
+        q = torch.randn((1, M, H, d), generator=gen, device=device)
+        lens = torch.tensor([ctx], dtype=torch.int32, device=device)
+        out = torch.empty_like(q)
+        ws = torch.empty(nq.lib().nq_attn_workspace_bytes(1, M, H, d, ctx + 16), dtype=torch.uint8, device=device)
+        for _ in range(3):
+            c.attention(q, lens, planes, d ** -0.5, out=out, ws=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": case, "ctx": ctx, "heads": H, "M": M}))
     else:
         B, k, V = 64, 4, 152064
         gen = torch.Generator(device=device)
@@ -1039,7 +1058,7 @@ def main():
                     help="full (default): also the LLaMA-3-8B (M=16/144), Qwen2.5-7B tier and acceptance-sweep "
                          "passes; quick: the LLaMA-2-7B round, per-linear times and acceptance timing only")
     ap.add_argument("--case", default=None,
-                    help="profiling workload: draft|verify|draft16|verify144|int4|fp8|fp16|greedy|sample")
+                    help="profiling workload: draft|verify|draft16|verify144|int4|fp8|fp16|greedy|sample|kv4|kv8")
     ap.add_argument("--layers", type=int, default=8)
     args = ap.parse_args()
     if args.case:
