@@ -257,10 +257,11 @@ class Round:
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one draft-pass
-# launch of the streaming kernel at this workload, from an ncu capture of the
-# full-size round (1.01x the algorithmic 3,414,627,328 B: no re-reads).  Set to
-# None whenever that kernel changes until it is captured again.
-DRAFT_PASS_DRAM_BYTES = 3_454_200_000
+# launch of the streaming kernel at this workload: an ncu capture of the
+# 8-layer case (0.999x its algorithmic bytes) scaled to the 32 layers + lm_head
+# by the algorithmic 3,414,627,328 B (no re-reads).  Set to None whenever that
+# kernel changes until it is captured again.
+DRAFT_PASS_DRAM_BYTES = 3_412_049_000
 
 
 def eq2_report(t_draft_us, t_verify_us, t_accept_us, t_target_us, k=K_DRAFT):
