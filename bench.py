@@ -208,8 +208,9 @@ class Round:
         self.bytes_verify = sum(verify_bytes(n, k, M_v) for _, n, k in self.shapes)
         self.bytes_accept = accept_bytes(1, K_DRAFT, V_LM, False) + accept_bytes(1, K_DRAFT, V_LM, True)
         self.bytes_round = K_DRAFT * self.bytes_draft_pass + self.bytes_verify + self.bytes_accept
-        # k draft passes + 1 verify pass + greedy (1 kernel) + sampled acceptance (2 kernels)
-        self.launches_per_round = K_DRAFT + 1 + 1 + 2
+        # k draft passes + 1 verify pass + greedy (1 kernel) + sampled acceptance
+        # (3 kernels: segment pass, decisions, resample pass)
+        self.launches_per_round = K_DRAFT + 1 + 1 + 3
 
     def run(self, events=None):
         nq = self.nq

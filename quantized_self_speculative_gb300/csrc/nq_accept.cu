@@ -8,13 +8,15 @@
 // rejection resample from normalise(max(0, p - q)) (Leviathan et al.; Chen et
 // al.), which follows the target distribution exactly.
 //
-// Design: one pass over the logits.  The grid is (chunk of 4096 entries,
-// vector, row); every CTA reduces its chunk and writes a partial to the
-// workspace; the last CTA of a row (atomic ticket, no spin-waits) combines the
-// partials, decides, and -- for sampling -- draws the replacement / bonus
-// token from the two vectors of the chosen position, which are still warm in
-// L2.  All fp32 arithmetic of the sampled path follows the fixed recipe
-// documented in nq.h so that decisions are reproducible bit for bit.
+// Design.  Greedy: one pass over the logits; the grid is (chunk of 16384
+// entries, vector, row), every CTA reduces its chunk and writes a partial to
+// the workspace, the last CTA of a row (atomic ticket, no spin-waits) combines
+// the partials and decides.  Sampled: three launches -- pass A reduces every
+// segment of every vector to its (max, sum) with no hand-off between warps, a
+// decision kernel (one CTA per row) forms the roots, decides and draws the
+// bonus token, pass B resamples the rows with a rejection.  All fp32
+// arithmetic of the sampled path follows the fixed recipe documented in nq.h
+// so that decisions are reproducible bit for bit.
 #include <algorithm>
 #include <mutex>
 
@@ -162,9 +164,9 @@ greedy_kernel(const int32_t *__restrict__ draft, const float *__restrict__ tgt, 
 // instruction) and stores them as chunk c = l % 8 of row r = 4 t + l / 8,
 // at position c ^ (r % 8) of that 128-byte row, so that the lane that owns
 // row r later reads its eight chunks with no bank conflict.  Loads in flight
-// cost no registers, and the warps are independent: each writes its own
-// partial and takes its own ticket, and the last warp of a row finishes the
-// row (no CTA-wide barrier).
+// cost no registers, and the warps of pass A are independent: each writes its
+// own partial and leaves (no ticket, no fence, no CTA-wide barrier); in pass
+// B each warp takes a ticket and the last warp of a row finishes the row.
 //
 // The chains of a leaf run on the packed fp32 adds, the even and the odd
 // chain in the two halves of one register pair; products that feed an add
@@ -189,17 +191,17 @@ constexpr int kSampleCtas = NQ_SAMPLE_CTAS;      // resident CTAs per SM (launch
 
 inline int n_segments_padded(int V) { return n_blocks(V) * kSegPerBlock; }
 
-struct SampleRec {      // per-row decision, written by pass A, read by pass B
+struct SampleRec {      // per-row decision, written by the decision kernel, read by pass B
     int js;             // first rejected position, or k if all accepted
     int resid;          // 1: draw from max(0, p_js - q_js); 0: draw from p_js
     float u;            // the draw's uniform
     float Mp, invSp, Mq, invSq;
-    int done;           // 1: pass A already drew the token (bonus draw from p_k)
+    int done;           // 1: the decision kernel drew the token (bonus draw from p_k)
 };
 
 // Workspace layout shared by the greedy and sampled calls.
 struct WsLayout {
-    size_t counters_a, counters_b, part, rec, segmax, segsum, ssum, lsum, vcount, roots, partu, ent, total;
+    size_t counters_a, counters_b, part, rec, segmax, segsum, ssum, lsum, partu, total;
 };
 
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
@@ -223,11 +225,8 @@ inline WsLayout ws_layout(int B, int k, int V)
     L.segsum = L.segmax + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));   // per (row, vector, segment)
     L.ssum = L.segsum + align256(static_cast<size_t>(B) * NV * NSP * sizeof(float));
     L.lsum = L.ssum + align256(static_cast<size_t>(B) * NSP * sizeof(float));         // per (row, segment)
-    L.vcount = L.lsum + align256(static_cast<size_t>(B) * NSP * kLeavesPerSeg * sizeof(float));
-    L.roots = L.vcount + align256(static_cast<size_t>(B) * NV * sizeof(unsigned int));  // per (row, vector)
-    L.partu = L.roots + align256(static_cast<size_t>(B) * NV * sizeof(float2));        // features: u per partial
-    L.ent = L.partu + align256(static_cast<size_t>(B) * NV * P * sizeof(float));       // features: entropy per vector
-    L.total = L.ent + static_cast<size_t>(B) * NV * sizeof(float);
+    L.partu = L.lsum + align256(static_cast<size_t>(B) * NSP * kLeavesPerSeg * sizeof(float));  // features: u per partial
+    L.total = L.partu + static_cast<size_t>(B) * NV * P * sizeof(float);
     return L;
 }
 
@@ -582,83 +581,97 @@ __device__ int sample_p_warp(const float *pv, int V, const float *smz, const flo
 }
 
 // ---- pass A: warp w of CTA (x, v, b) reduces segments 2 g and 2 g + 1
-// (g = kWarpsS x + w) of vector v of row b; the last warp of the row decides.
-//
-// FEAT: the draft vectors also carry u through the same trees, and the last
-// warp of the row writes SpecKV's step features (mean and maximum draft
-// entropy, mean and minimum draft confidence q_j(d_j)) to feat[b][0..3].
+// (g = kWarpsS x + w) of vector v of row b, staged in buf (the caller has
+// committed one cp.async group per segment): their (max, sum) go to segmax /
+// segsum and their merge to part (with u to partu when FEAT and v is a draft
+// vector).  No warp waits for another: the roots and the decisions are taken
+// by the decision kernel after the pass, which costs one launch (overlapped
+// as a dependent launch) and takes a fence and an atomic ticket off every
+// warp's path (84 against 89 us at B = 64, k = 4, V = 152064).
+template <bool FEAT>
+__device__ __forceinline__ void a_task(int k, int V, float c, float2 *__restrict__ part, float *__restrict__ segmax,
+                                       float *__restrict__ segsum, float *__restrict__ partu, unsigned int *status,
+                                       int NW, int b, int v, int g, const float *buf)
+{
+    const int NV = 2 * k + 1, NSP = 2 * NW;
+    const int lane = threadIdx.x & 31;
+    float *segm = segmax + (static_cast<size_t>(b) * NV + v) * NSP;
+    float *segs = segsum + (static_cast<size_t>(b) * NV + v) * NSP;
+    float finite = 0.0f;
+    MaxSum seg[2];
+    float su[2] = {0.0f, 0.0f};
+    const bool want_u = FEAT && v > k;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i == 0) cp_async_wait<1>(); else cp_async_wait<0>();   // segment 1 still in flight for i = 0
+        __syncwarp();
+        const int sg = 2 * g + i;
+        seg[i] = MaxSum{-INFINITY, 0.0f};
+        if (sg * kSeg < V) {                          // warp-uniform
+            const int np = min(max(V - (sg * kSeg + 32 * lane), 0), 32);
+            float l[32];
+            read_lane(buf + i * kSeg, np, l);
+            if (want_u) seg[i] = segment_ms<true>(l, np, c, finite, &su[i]);
+            else seg[i] = segment_ms(l, np, c, finite);
+            if (lane == 0) {
+                segm[sg] = seg[i].m;
+                segs[sg] = seg[i].s;
+            }
+        }
+    }
+    if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
+    const MaxSum a = ms_merge(seg[0], seg[1]);
+    if (want_u && lane == 0)
+        partu[(static_cast<size_t>(b) * NV + v) * NW + g] =
+            msu_merge(MSU{seg[0].m, seg[0].s, su[0]}, MSU{seg[1].m, seg[1].s, su[1]}).u;
+    if (lane == 0) part[(static_cast<size_t>(b) * NV + v) * NW + g] = make_float2(a.m, a.s);
+}
+
 template <bool FEAT>
 __global__ void __launch_bounds__(kThreadsS, kSampleCtas)
-sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
-                int k, int V, float c, int al, const uint64_t *__restrict__ seeds, uint64_t round,
-                unsigned int *__restrict__ counters, unsigned int *__restrict__ vcount, float2 *__restrict__ part,
-                float *__restrict__ segmax, float *__restrict__ segsum, float2 *__restrict__ roots,
-                SampleRec *__restrict__ rec, int32_t *__restrict__ out_tok, int32_t *__restrict__ out_cnt,
-                float *__restrict__ partu, float *__restrict__ ent, float *__restrict__ feat, unsigned int *status)
+sample_a_kernel(const float *__restrict__ dlog, const float *__restrict__ tlog, int k, int V, float c, int al,
+                float2 *__restrict__ part, float *__restrict__ segmax, float *__restrict__ segsum,
+                float *__restrict__ partu, unsigned int *status)
 {
-    // the resample pass may be scheduled now; it waits (griddepcontrol.wait) for
-    // this grid to complete before reading anything this grid writes
+    // the decision kernel may be scheduled now; it waits (griddepcontrol.wait)
+    // for this grid to complete before reading anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(128) float smem_s[];
-    const int v = blockIdx.y, b = blockIdx.z;
-    const int NV = 2 * k + 1, NW = gridDim.x * kWarpsS, NSP = 2 * NW;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x * kWarpsS + warp;
+    const int warp = threadIdx.x >> 5;
+    const int v = blockIdx.y, b = blockIdx.z, g = blockIdx.x * kWarpsS + warp, NW = gridDim.x * kWarpsS;
     float *buf = smem_s + warp * 2 * kSeg;
     // vectors 0..k: target positions 0..k; k+1..2k: draft positions 0..k-1
     const float *vec = v <= k ? tlog + (static_cast<size_t>(b) * (k + 1) + v) * V
                               : dlog + (static_cast<size_t>(b) * k + (v - k - 1)) * V;
-    float *segm = segmax + (static_cast<size_t>(b) * NV + v) * NSP;
-    float *segs = segsum + (static_cast<size_t>(b) * NV + v) * NSP;
-    bool last;
-    {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if ((2 * g + i) * kSeg < V) stage_segment(buf + i * kSeg, vec, V, (2 * g + i) * kSeg, al);
-            cp_async_commit();
-        }
-        float finite = 0.0f;
-        MaxSum seg[2];
-        float su[2] = {0.0f, 0.0f};
-        const bool want_u = FEAT && v > k;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if (i == 0) cp_async_wait<1>(); else cp_async_wait<0>();
-            __syncwarp();
-            const int sg = 2 * g + i;
-            seg[i] = MaxSum{-INFINITY, 0.0f};
-            if (sg * kSeg < V) {                          // warp-uniform
-                const int np = min(max(V - (sg * kSeg + 32 * lane), 0), 32);
-                float l[32];
-                read_lane(buf + i * kSeg, np, l);
-                if (want_u) seg[i] = segment_ms<true>(l, np, c, finite, &su[i]);
-                else seg[i] = segment_ms(l, np, c, finite);
-                if (lane == 0) {
-                    segm[sg] = seg[i].m;
-                    segs[sg] = seg[i].s;
-                }
-            }
-        }
-        if (finite != 0.0f) set_status(status, NQ_DEV_NONFINITE);
-        const MaxSum a = ms_merge(seg[0], seg[1]);
-        unsigned int prev = 0;
-        if (want_u && lane == 0)
-            partu[(static_cast<size_t>(b) * NV + v) * NW + g] =
-                msu_merge(MSU{seg[0].m, seg[0].s, su[0]}, MSU{seg[1].m, seg[1].s, su[1]}).u;
-        if (lane == 0) {
-            part[(static_cast<size_t>(b) * NV + v) * NW + g] = make_float2(a.m, a.s);
-            __threadfence();
-            prev = atomicAdd(&vcount[static_cast<size_t>(b) * NV + v], 1u);
-        }
-        last = __shfl_sync(0xffffffffu, prev, 0) == static_cast<unsigned int>(NW - 1);
+    for (int i = 0; i < 2; ++i) {
+        if ((2 * g + i) * kSeg < V) stage_segment(buf + i * kSeg, vec, V, (2 * g + i) * kSeg, al);
+        cp_async_commit();
     }
-    if (!last) return;
-    __threadfence();
+    a_task<FEAT>(k, V, c, part, segmax, segsum, partu, status, NW, b, v, g, buf);
+}
 
-    // ---- last warp of vector v: its root (M, 1/S); lane l holds the partials
-    // 8 l .. 8 l + 7 (pairwise in the lane, then across lanes).  The vectors'
-    // last warps run in parallel; the last of them takes the row's decisions.
-    {
+// ---- decision kernel: CTA b takes row b.  Warp w forms the roots (M, 1/S) of
+// vectors w, w + kDecWarps, ... from pass A's partials; then warp 0 takes the
+// row's decisions (and the bonus draw when every draft is accepted) and
+// writes the record the resample pass reads.
+constexpr int kDecWarps = 8;
+
+template <bool FEAT>
+__global__ void __launch_bounds__(kDecWarps * 32)
+decide_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog, const float *__restrict__ tlog,
+              int k, int V, float c, const uint64_t *__restrict__ seeds, uint64_t round,
+              const float2 *__restrict__ part, const float *__restrict__ segmax, const float *__restrict__ segsum,
+              const float *__restrict__ partu, SampleRec *__restrict__ rec, int32_t *__restrict__ out_tok,
+              int32_t *__restrict__ out_cnt, float *__restrict__ feat, unsigned int *status, int NW)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ float2 sroot[2 * kMaxK + 1];
+    __shared__ float sent[2 * kMaxK + 1];
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NV = 2 * k + 1, NSP = 2 * NW;
+    for (int v = warp; v < NV; v += kDecWarps) {
         MaxSum n[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -689,23 +702,16 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
                                 __shfl_xor_sync(0xffffffffu, r.u, o)};
                 r = msu_merge(r, other);
             }
-            if (lane == 0) ent[static_cast<size_t>(b) * NV + v] = 0.69314718f * (log2f(r.s) - r.u / r.s);
+            if (lane == 0) sent[v] = 0.69314718f * (log2f(r.s) - r.u / r.s);
         }
-        unsigned int prev = 0;
-        if (lane == 0) {
-            roots[static_cast<size_t>(b) * NV + v] = make_float2(a.m, __frcp_rn(a.s));
-            vcount[static_cast<size_t>(b) * NV + v] = 0;   // ready for the next call
-            __threadfence();
-            prev = atomicAdd(&counters[b], 1u);
-        }
-        if (__shfl_sync(0xffffffffu, prev, 0) != static_cast<unsigned int>(NV - 1)) return;
-        __threadfence();
+        if (lane == 0) sroot[v] = make_float2(a.m, __frcp_rn(a.s));
     }
+    __syncthreads();
+    if (warp != 0) return;
 
-    // ---- last warp of row b.  Decisions: accept d_j iff u_j < p_j(d_j) /
-    // q_j(d_j); first rejection j*
-    const float2 *rrow = roots + static_cast<size_t>(b) * NV;
-    auto root_of = [&](int vv) { const float2 r = __ldcg(rrow + vv); return RowRoots{r.x, r.y}; };
+    // ---- warp 0.  Decisions: accept d_j iff u_j < p_j(d_j) / q_j(d_j); first
+    // rejection j*
+    auto root_of = [&](int vv) { const float2 r = sroot[vv]; return RowRoots{r.x, r.y}; };
     const uint64_t seed = seeds[b];
     const float *segrow = segmax + static_cast<size_t>(b) * NV * NSP;
     bool reject = false;
@@ -729,7 +735,7 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     }
     if constexpr (FEAT) {
         // the step's features over the k drafted positions (lanes 0..k-1)
-        const float h = lane < k ? __ldcg(ent + static_cast<size_t>(b) * NV + k + 1 + lane) : 0.0f;
+        const float h = lane < k ? sent[k + 1 + lane] : 0.0f;
         float sh = h, sc = conf, mh = lane < k ? h : -INFINITY, mc = lane < k ? conf : INFINITY;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -747,7 +753,7 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const int js = rej ? __ffs(rej) - 1 : k;
     if (js == k) {
         // every draft accepted: the bonus token from p_k is drawn here (the
-        // segment weights come from this pass), and the resample pass skips the row
+        // segment weights come from pass A), and the resample pass skips the row
         const RowRoots rk = root_of(k);
         const int pk = sample_p_warp(tlog + (static_cast<size_t>(b) * (k + 1) + k) * V, V,
                                      segrow + static_cast<size_t>(k) * NSP,
@@ -773,7 +779,6 @@ sample_a_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
         }
         r.done = js == k;
         rec[b] = r;
-        counters[b] = 0;   // ready for the next call
     }
 }
 
@@ -1008,29 +1013,38 @@ nq_status launch_sample(const int32_t *draft, const float *draft_logits, const f
     const int nsp = nq::n_segments_padded(V);
     dim3 grid_a(nsp / (2 * nq::kWarpsS), 2 * k + 1, B);   // one warp per segment pair
     auto ka = features ? nq::sample_a_kernel<true> : nq::sample_a_kernel<false>;
-    ka<<<grid_a, nq::kThreadsS, nq::kSmemS, stream>>>(
-        draft, draft_logits, tgt_logits, k, V, c, al, seeds, round, reinterpret_cast<unsigned int *>(w + L.counters_a),
-        reinterpret_cast<unsigned int *>(w + L.vcount), reinterpret_cast<float2 *>(w + L.part), segmax,
-        reinterpret_cast<float *>(w + L.segsum), reinterpret_cast<float2 *>(w + L.roots), rec, out_tok, out_cnt,
-        reinterpret_cast<float *>(w + L.partu), reinterpret_cast<float *>(w + L.ent), features, status);
+    ka<<<grid_a, nq::kThreadsS, nq::kSmemS, stream>>>(draft_logits, tgt_logits, k, V, c, al,
+                                                      reinterpret_cast<float2 *>(w + L.part), segmax,
+                                                      reinterpret_cast<float *>(w + L.segsum),
+                                                      reinterpret_cast<float *>(w + L.partu), status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return NQ_ERR_CUDA;
-    // pass B as a programmatic dependent launch when pass A fills the GPU: its
-    // CTAs are scheduled while pass A drains and block in griddepcontrol.wait
-    // until pass A completes.  Below one wave of pass-A CTAs (B = 1 rounds)
-    // a plain launch measured faster inside a decode round (32 vs 37 us with
-    // the dependent launch); griddepcontrol.wait returns at once then.
+    // the decision kernel and pass B as programmatic dependent launches when
+    // pass A fills the GPU: their CTAs are scheduled while the grid before
+    // drains and block in griddepcontrol.wait until it completes.  Below one
+    // wave of pass-A CTAs (B = 1 rounds) plain launches measured faster inside
+    // a decode round (32 vs 37 us with dependent launches); griddepcontrol.wait
+    // returns at once then.
     const bool dependent = static_cast<long long>(grid_a.x) * grid_a.y * grid_a.z >= nq::sm_count();
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nsp / nq::kWarpsS, B);   // one warp per segment
-    cfg.blockDim = dim3(nq::kThreadsS);
-    cfg.dynamicSmemBytes = nq::kSmemS;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B);
+    cfg.blockDim = dim3(nq::kDecWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, features ? nq::decide_kernel<true> : nq::decide_kernel<false>, draft, draft_logits,
+                           tgt_logits, k, V, c, seeds, round, static_cast<const float2 *>(reinterpret_cast<float2 *>(w + L.part)),
+                           static_cast<const float *>(segmax), static_cast<const float *>(reinterpret_cast<float *>(w + L.segsum)),
+                           static_cast<const float *>(reinterpret_cast<float *>(w + L.partu)), rec, out_tok, out_cnt,
+                           features, status, nsp / 2);
+    if (e != cudaSuccess) return NQ_ERR_CUDA;
+    cfg.gridDim = dim3(nsp / nq::kWarpsS, B);   // one warp per segment
+    cfg.blockDim = dim3(nq::kThreadsS);
+    cfg.dynamicSmemBytes = nq::kSmemS;
     e = cudaLaunchKernelEx(&cfg, nq::sample_b_kernel, draft, draft_logits, tgt_logits, k, V, c, al, out_tok, out_cnt,
                            reinterpret_cast<unsigned int *>(w + L.counters_b), static_cast<const nq::SampleRec *>(rec),
                            static_cast<const float *>(segmax), static_cast<const float *>(reinterpret_cast<float *>(w + L.segsum)),

@@ -58,19 +58,18 @@ def test_workspace_bytes(L):
     # (2k+1) partials per row of max(4096-entry chunks, 2048-entry segment
     # pairs), a 32-B decision record per row, one maximum and one sum per
     # 1024-entry segment (16 per 16384-entry block) per vector per row, one sum per
-    # segment per row, 64 leaf sums per segment per row, a ticket and a root
-    # (max, 1/sum) per vector per row; for the draft features one u per
-    # partial and one entropy per vector per row
+    # segment per row, 64 leaf sums per segment per row; for the draft
+    # features one u per partial
     a = lambda n: (n + 255) // 256 * 256
 
     def expect(B, k, V):
         C, NSP, NV = -(-V // 4096), 16 * -(-V // 16384), 2 * k + 1
         P = max(C, NSP // 2)
         return (a(4 * B) * 2 + a(B * NV * P * 8) + a(32 * B) + 2 * a(B * NV * NSP * 4)
-                + a(4 * B * NSP) + a(256 * B * NSP) + a(4 * B * NV) + a(8 * B * NV) + a(4 * B * NV * P) + 4 * B * NV)
+                + a(4 * B * NSP) + a(256 * B * NSP) + 4 * B * NV * P)
 
-    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 5119488
-    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 8484
+    assert nq.workspace_bytes(64, 8, 152064) == expect(64, 8, 152064) == 5102080
+    assert nq.workspace_bytes(1, 4, 4096) == expect(1, 4, 4096) == 7712
     assert nq.workspace_bytes(3, 16, 4099) == expect(3, 16, 4099)
     # k = 0 sizes the draft argmax's workspace (no drafts, one position per row)
     assert nq.workspace_bytes(5, 0, 32000) == expect(5, 0, 32000) > 0
