@@ -36,5 +36,7 @@ def test_acceptance_bytes_read_every_logit_once():
 
 
 def test_measured_traffic_constant_is_close_to_the_algorithmic_bytes():
+    # the algorithmic bytes count the activations and outputs, which may stay
+    # in L2: DRAM traffic can fall a little below them, never far
     ratio = bench.DRAFT_PASS_DRAM_BYTES / _pass_bytes(bench.draft_bytes, 1)
-    assert 1.0 <= ratio < 1.05
+    assert 0.99 <= ratio < 1.05
