@@ -123,19 +123,27 @@ __device__ __forceinline__ float ex2(float x)
 }
 
 // Codes of nibbles i (low half) and i + 4 (high half) of a word of eight
-// elements, as fp16 subnormals: KV4 (q4 + 8); KV8 from the base and
-// refinement words, 16 (q4 + 8) + (r + 8) = q8 + 136.
+// elements, as fp16 subnormals: KV4 (q4 + 8), where an odd i leaves the
+// nibbles in bits 4-7 of each half (16 (q4 + 8): one shift per two pairs
+// instead of one per pair; the other operand or the output carries the
+// 1/16); KV8 from the base and refinement words, 16 (q4 + 8) + (r + 8) =
+// q8 + 136.
 template <int PLANES>
 __device__ __forceinline__ uint32_t code_pair(uint32_t xb, uint32_t xr, int i)
 {
     if constexpr (PLANES == 1) {
-        return ((xb >> (4 * i)) & 0x000F000Fu) ^ 0x00080008u;
+        (void)xr;
+        const uint32_t x = i >= 2 ? xb >> 8 : xb;
+        return (i & 1) ? ((x & 0x00F000F0u) ^ 0x00800080u) : ((x & 0x000F000Fu) ^ 0x00080008u);
     } else {
         // xb, xr already have every nibble's sign bit flipped (offset binary)
         const uint32_t hi = i == 0 ? (xb << 4) : (xb >> (4 * i - 4));
         return (hi & 0x00F000F0u) | ((xr >> (4 * i)) & 0x000F000Fu);
     }
 }
+// Scale of the codes code_pair returns for pair index i (1 or 16).
+template <int PLANES>
+__host__ __device__ constexpr float code_scale(int i) { return PLANES == 1 && (i & 1) ? 16.0f : 1.0f; }
 
 // Byte offset of (row r, byte o) of a 16-row tile of rows of RB bytes in
 // shared memory: 16-byte chunks, chunk q = r RB / 16 + o / 16 stored at
@@ -272,8 +280,10 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
                     const int w = sl >> 1, i0 = 2 * (sl & 1);
                     // A-fragment registers: (row g, k 2t..2t+1), (row g + 8, same),
                     // (row g, k 2t+8..2t+9), (row g + 8, same)
+                    // (the second pair's codes come 16 times too large at KV4: x / 16 there, exact in fp16)
+                    constexpr float kInv = 1.0f / code_scale<PLANES>(1);
                     qa[h][sl][rr] = h2_pack(x[8 * w + i0], x[8 * w + i0 + 4]);
-                    qa[h][sl][2 + rr] = h2_pack(x[8 * w + i0 + 1], x[8 * w + i0 + 5]);
+                    qa[h][sl][2 + rr] = h2_pack(x[8 * w + i0 + 1] * kInv, x[8 * w + i0 + 5] * kInv);
                 }
             }
         }
@@ -486,7 +496,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int n = 2 * t + cc, dim = 64 * h + 8 * n + i;
-                    const float val = fmaf(16777216.0f, o[8 * h + i][2 * rr + cc],
+                    const float val = fmaf(16777216.0f / code_scale<PLANES>(i & 3), o[8 * h + i][2 * rr + cc],
                                            -static_cast<float>(OFF) * sig[NG == 2 ? h : 0][2 * rr]);
                     red_o[(warp * kQTile + row) * D + dim] = val;
                 }
