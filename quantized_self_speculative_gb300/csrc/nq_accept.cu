@@ -415,10 +415,8 @@ __device__ __forceinline__ float seg_factor(float mz_seg, float M, float inv_s)
 }
 
 // p(x) of entry x of one vector (recipe: RN(e2(t(x)) F_seg)).
-__device__ __forceinline__ float prob_at(const float *vec, const float *segm, int x, float c, RowRoots root)
+__device__ __forceinline__ float prob_from(float lx, float mz, float c, RowRoots root)
 {
-    const float mz = __ldcg(segm + (x >> 10));
-    const float lx = __ldcg(vec + x);
     return __fmul_rn(exp2_canon(__fmaf_rn(lx, c, -mz)), seg_factor(mz, root.M, root.inv_s));
 }
 
@@ -655,7 +653,7 @@ sample_a_kernel(const float *__restrict__ dlog, const float *__restrict__ tlog, 
 // vectors w, w + kDecWarps, ... from pass A's partials; then warp 0 takes the
 // row's decisions (and the bonus draw when every draft is accepted) and
 // writes the record the resample pass reads.
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;
 
 template <bool FEAT>
 __global__ void __launch_bounds__(kDecWarps * 32)
@@ -669,8 +667,23 @@ decide_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog,
     asm volatile("griddepcontrol.launch_dependents;");
     __shared__ float2 sroot[2 * kMaxK + 1];
     __shared__ float sent[2 * kMaxK + 1];
+    __shared__ int sbonus;
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NV = 2 * k + 1, NSP = 2 * NW;
+    const float *segrow = segmax + static_cast<size_t>(b) * NV * NSP;
+    // warp 0, lane j < k: the logits and segment maxima at the drafted id d_j,
+    // loaded while the roots are formed
+    int dj = 0;
+    float lxp = 0.0f, mzp = 0.0f, lxq = 0.0f, mzq = 0.0f;
+    if (warp == 0 && lane < k) {
+        dj = draft[static_cast<size_t>(b) * k + lane];
+        if (dj >= 0 && dj < V) {
+            lxp = __ldcg(tlog + (static_cast<size_t>(b) * (k + 1) + lane) * V + dj);
+            mzp = __ldcg(segrow + static_cast<size_t>(lane) * NSP + (dj >> 10));
+            lxq = __ldcg(dlog + (static_cast<size_t>(b) * k + lane) * V + dj);
+            mzq = __ldcg(segrow + static_cast<size_t>(k + 1 + lane) * NSP + (dj >> 10));
+        }
+    }
     for (int v = warp; v < NV; v += kDecWarps) {
         MaxSum n[8];
 #pragma unroll
@@ -707,26 +720,34 @@ decide_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog,
         if (lane == 0) sroot[v] = make_float2(a.m, __frcp_rn(a.s));
     }
     __syncthreads();
-    if (warp != 0) return;
+    if (warp > 1) return;
+    auto root_of = [&](int vv) { const float2 r = sroot[vv]; return RowRoots{r.x, r.y}; };
+    const uint64_t seed = seeds[b];
+    if (warp == 1) {
+        // the bonus token from p_k by the two-level rule (segment weights from
+        // pass A), drawn while warp 0 decides; used if every draft is accepted
+        const RowRoots rk = root_of(k);
+        const int pk = sample_p_warp(tlog + (static_cast<size_t>(b) * (k + 1) + k) * V, V,
+                                     segrow + static_cast<size_t>(k) * NSP,
+                                     segsum + (static_cast<size_t>(b) * NV + k) * NSP, NSP, c, rk.M, rk.inv_s,
+                                     philox_uniform(seed, static_cast<uint32_t>(k), 2u, round));
+        if (lane == 0) sbonus = pk;
+        asm volatile("bar.sync 1, 64;" ::: "memory");   // warps 0 and 1: sbonus is written
+        return;
+    }
 
     // ---- warp 0.  Decisions: accept d_j iff u_j < p_j(d_j) / q_j(d_j); first
     // rejection j*
-    auto root_of = [&](int vv) { const float2 r = sroot[vv]; return RowRoots{r.x, r.y}; };
-    const uint64_t seed = seeds[b];
-    const float *segrow = segmax + static_cast<size_t>(b) * NV * NSP;
     bool reject = false;
     float conf = 0.0f;
     if (lane < k) {
         const int j = lane;
-        const int d = draft[static_cast<size_t>(b) * k + j];
-        if (d < 0 || d >= V) {
+        if (dj < 0 || dj >= V) {
             set_status(status, NQ_DEV_BAD_TOKEN);
             reject = true;
         } else {
-            const float p = prob_at(tlog + (static_cast<size_t>(b) * (k + 1) + j) * V,
-                                    segrow + static_cast<size_t>(j) * NSP, d, c, root_of(j));
-            const float q = prob_at(dlog + (static_cast<size_t>(b) * k + j) * V,
-                                    segrow + static_cast<size_t>(k + 1 + j) * NSP, d, c, root_of(k + 1 + j));
+            const float p = prob_from(lxp, mzp, c, root_of(j));
+            const float q = prob_from(lxq, mzq, c, root_of(k + 1 + j));
             conf = q;
             const float ratio = __fdiv_rn(p, q);
             const float u = philox_uniform(seed, static_cast<uint32_t>(j), 0u, round);
@@ -751,16 +772,10 @@ decide_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlog,
     }
     const unsigned int rej = __ballot_sync(0xffffffffu, reject);
     const int js = rej ? __ffs(rej) - 1 : k;
-    if (js == k) {
-        // every draft accepted: the bonus token from p_k is drawn here (the
-        // segment weights come from pass A), and the resample pass skips the row
-        const RowRoots rk = root_of(k);
-        const int pk = sample_p_warp(tlog + (static_cast<size_t>(b) * (k + 1) + k) * V, V,
-                                     segrow + static_cast<size_t>(k) * NSP,
-                                     segsum + (static_cast<size_t>(b) * NV + k) * NSP, NSP, c, rk.M, rk.inv_s,
-                                     philox_uniform(seed, static_cast<uint32_t>(k), 2u, round));
-        if (lane == 0) write_row(out_tok, out_cnt, draft, b, k, k, pk);
-    }
+    // every draft accepted: the bonus token (warp 1's draw), and the resample
+    // pass skips the row
+    asm volatile("bar.sync 1, 64;" ::: "memory");       // warps 0 and 1: sbonus is written
+    if (js == k && lane == 0) write_row(out_tok, out_cnt, draft, b, k, k, sbonus);
     if (lane == 0) {
         const RowRoots rp = root_of(js);
         SampleRec r;
