@@ -135,6 +135,14 @@ def test_device_status_flags(nq):
     dl2[0, 0, 3] = np.inf
     nq.accept_sample(dev(d2), dev(dl2), dev(tl2), 1.0, seeds_dev(synth.seeds_for(7, B)), 0)
     assert nq.device_status() & nq.NQ_DEV_NONFINITE
+    # an out-of-range draft id in the sampled path: flagged, and treated as a
+    # rejection at its position (the row keeps at most that many drafts)
+    d3, dl3, tl3 = sample_case(B, k, V, 8303)
+    d3[1, 1] = V
+    tok, cnt = nq.accept_sample(dev(d3), dev(dl3), dev(tl3), 1.0, seeds_dev(synth.seeds_for(9, B)), 0)
+    assert nq.device_status() & nq.NQ_DEV_BAD_TOKEN
+    tok, cnt = tok.cpu().numpy(), cnt.cpu().numpy()
+    assert 1 <= cnt[1] <= 2 and np.all((tok[1, :cnt[1]] >= 0) & (tok[1, :cnt[1]] < V))
 
 
 def test_workspace_and_argument_checks(nq):
