@@ -12,9 +12,11 @@
 // value of an element is s q4 and the target value (s / 16)(16 q4 + r).
 //
 // Attention (one launch + a combine): the cache rows of a (sequence, kv head)
-// are cut into 256-row splits; a CTA of four warps takes one split and a tile
-// of 16 query vectors (query heads sharing the kv head, times query rows),
-// each warp 64 rows in four blocks of 16 with its own online softmax.  Both
+// are cut into splits of 256 to 1024 rows (chosen per call); a CTA of four
+// warps takes one split and a tile of 16 query vectors (query heads sharing
+// the kv head, times query rows), each warp a quarter of the split in blocks
+// of 16 rows, streamed through a four-stage cp.async ring, with its own
+// online softmax.  Both
 // products run on the tensor cores (warp MMA m16n8k16, fp16 operands, fp32
 // accumulators), in the manner of FlashAttention-2: S = Q K^T with the query
 // tile as the A rows and a block of K as two B tiles, then O += P V with P
@@ -24,7 +26,8 @@
 // placed with integer masks and byte permutes only.  The offset leaves S
 // through the accumulator's initial value and O through a running sum of P;
 // the group scales multiply S after its MMA and P before the V product.  The
-// warps' states merge in shared memory, the splits' in a second kernel.
+// warps' states merge in shared memory, the splits' in a second kernel (a
+// dependent launch).
 #include "nq_internal.cuh"
 
 #include <atomic>
