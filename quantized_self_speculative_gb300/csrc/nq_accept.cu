@@ -587,7 +587,7 @@ __device__ int sample_p_warp(const float *pv, int V, const float *smz, const flo
 // as a dependent launch) and takes a fence and an atomic ticket off every
 // warp's path (84 against 89 us at B = 64, k = 4, V = 152064).
 template <bool FEAT>
-__device__ __forceinline__ void a_task(int k, int V, float c, float2 *__restrict__ part, float *__restrict__ segmax,
+__device__ __forceinline__ void reduce_pair(int k, int V, float c, float2 *__restrict__ part, float *__restrict__ segmax,
                                        float *__restrict__ segsum, float *__restrict__ partu, unsigned int *status,
                                        int NW, int b, int v, int g, const float *buf)
 {
@@ -646,13 +646,14 @@ sample_a_kernel(const float *__restrict__ dlog, const float *__restrict__ tlog, 
         if ((2 * g + i) * kSeg < V) stage_segment(buf + i * kSeg, vec, V, (2 * g + i) * kSeg, al);
         cp_async_commit();
     }
-    a_task<FEAT>(k, V, c, part, segmax, segsum, partu, status, NW, b, v, g, buf);
+    reduce_pair<FEAT>(k, V, c, part, segmax, segsum, partu, status, NW, b, v, g, buf);
 }
 
 // ---- decision kernel: CTA b takes row b.  Warp w forms the roots (M, 1/S) of
-// vectors w, w + kDecWarps, ... from pass A's partials; then warp 0 takes the
-// row's decisions (and the bonus draw when every draft is accepted) and
-// writes the record the resample pass reads.
+// vectors w, w + kDecWarps, ... from pass A's partials (warp 0 first loads the
+// logits at the drafted ids); then warp 0 takes the row's decisions while
+// warp 1 draws the bonus token from p_k, and warp 0 writes the record the
+// resample pass reads (and the row's tokens when every draft is accepted).
 constexpr int kDecWarps = 16;
 
 template <bool FEAT>
