@@ -196,8 +196,10 @@ stream_kernel(const __grid_constant__ Batch<MAXP> B, unsigned int *status)
     // ring slots (R - 1 chunks in flight), measured per kind on whole-model
     // passes: nibbles 3 (both planes) / 5 (one plane, 128-input groups); E4M3
     // and fp16 rows 7 with one 8-column tile and 6 with two (4% faster than 5
-    // for E4M3 at M = 3..7)
-    constexpr int R = KIND == kNib ? (LANE_BYTES >= 64 ? 3 : (LANE_BYTES >= 32 ? 5 : 8)) : (NT == 1 ? 7 : 6);
+    // for E4M3 at M = 3..7).  Nibbles with two tiles (M = 9..16) keep one slot
+    // less, so that 16-warp units fit 128 registers a thread.
+    constexpr int R = KIND == kNib ? (LANE_BYTES >= 64 ? (NT == 2 ? 2 : 3) : (LANE_BYTES >= 32 ? (NT == 2 ? 4 : 5) : 8))
+                                   : (NT == 1 ? 7 : 6);
     constexpr int ROWS = 16 * WARPS;
     constexpr float kNeg8Ulp = -4.76837158203125e-07f;   // -8 * 2^-24
 
@@ -573,16 +575,13 @@ cudaError_t launch_stream(Batch<MAXP> &b, cudaStream_t s, unsigned int *status)
 // larger L1; measured 3-13% faster on whole-model passes at M = 1..9).  The
 // nibble kernels with two 8-column tiles need more than 128 registers and keep
 // 8-warp units.
-constexpr bool wide_units_ok(int kind, int nt) { return !(kind == kNib && nt == 2); }
-
 template <int KIND, int PLANES, int G, int NT, int MAXP>
 cudaError_t dispatch_w(Batch<MAXP> &b, int warps, cudaStream_t s, unsigned int *st)
 {
     if constexpr (MAXP == kSmallBatch) {
         return launch_stream<KIND, PLANES, G, NT, 4, MAXP>(b, s, st);
     } else {
-        if constexpr (wide_units_ok(KIND, NT))
-            if (warps == 16) return launch_stream<KIND, PLANES, G, NT, 16, MAXP>(b, s, st);
+        if (warps == 16) return launch_stream<KIND, PLANES, G, NT, 16, MAXP>(b, s, st);
         return warps == 8 ? launch_stream<KIND, PLANES, G, NT, 8, MAXP>(b, s, st)
                           : launch_stream<KIND, PLANES, G, NT, 4, MAXP>(b, s, st);
     }
@@ -657,7 +656,11 @@ nq_status run_batch(int count, const nq_weights *w, const void *const *x, int M,
             const int nt = Mc > 8 ? 2 : 1;
             int warps = 4;
             if (MAXP == kLargeBatch) {
-                if (wide_units_ok(kind, nt) && rows16 / 16 >= 2LL * sm_count()) warps = 16;
+                // (nibbles with two tiles used 8-warp units at 150 registers, one
+                // CTA per SM, until their ring lost a slot and 16-warp units fit:
+                // M = 16 draft 0.21 -> 0.42 and M = 9 0.29 -> 0.52 of the copy
+                // bandwidth on the LLaMA-3-8B pass)
+                if (rows16 / 16 >= 2LL * sm_count()) warps = 16;
                 else if (rows16 / 8 >= 2LL * sm_count()) warps = 8;
             }
             const int rows_per_unit = 16 * warps;
