@@ -73,6 +73,24 @@ def test_attention_matches_oracle(nq, B, Hq, Hkv, d, G, M, lens, planes):
     assert nq.device_status() == 0
 
 
+@pytest.mark.parametrize("planes,M", [(1, 1), (2, 5)])
+def test_attention_long_splits_match_oracle(nq, planes, M):
+    """Enough (sequence, kv head) pairs that the kernel takes its longest
+    splits (1024 cache rows per CTA, 16 blocks per warp through the four-stage
+    ring), with lengths that end inside a block and inside a split."""
+    B, H, d, G, L = 4, 16, 128, 128, 4096
+    lens = [4000, 3077, 1025, 4096]
+    cache, _, _ = fill(nq, B, H, d, G, L, lens, 5000 + planes)
+    q = rows(5100 + M, B, M, H, d)
+    ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = cache.attention(torch.from_numpy(q).cuda(), ln, planes, 0.09).cpu().numpy()
+    ref = O.attn_decode(q, cache.host_dict(), np.array(lens, np.int32), planes, 0.09)
+    err = max(normwise_err(out[b, m, h][None], ref[b, m, h][None])
+              for b in range(B) for m in range(M) for h in range(H))
+    assert err <= TOL, err
+    assert nq.device_status() == 0
+
+
 def test_draft_view_differs_from_target_view_and_suffix_discard(nq):
     """The 4-bit and 8-bit views give different attention (the base alone is
     a coarser copy); rows past a sequence's length are never read, so after a
