@@ -843,7 +843,7 @@ sample_b_kernel(const int32_t *__restrict__ draft, const float *__restrict__ dlo
     const int sg = blockIdx.x * kWarpsS + warp;
     float *pbuf = smem_s + warp * 2 * kSeg, *qbuf = pbuf + kSeg;
     const SampleRec R = rec[b];
-    if (R.done) return;                                  // the bonus draw was taken in pass A
+    if (R.done) return;                                  // the decision kernel drew the bonus token
     const float *pv = tlog + (static_cast<size_t>(b) * (k + 1) + R.js) * V;
     const float *qv = R.js < k ? dlog + (static_cast<size_t>(b) * k + R.js) * V : pv;
     const float *smp = segmax + (static_cast<size_t>(b) * NV + R.js) * NSP;
