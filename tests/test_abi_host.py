@@ -170,3 +170,48 @@ def test_product_and_oracle_share_nothing():
             src = open(os.path.join(ROOT, "oracle", f)).read()
             assert not re.search(r"^\s*(import|from)\s+quantized_self_speculative_gb300|nq_internal|libnq\.so|nq\.h",
                                  src, re.M), f
+
+
+def test_round_kv_and_int8_entry_points_validate_on_the_host(L):
+    """Sizes of the nested KV cache and the attention workspace, and argument
+    checks of the round bookkeeping, KV and int8-activation entry points: every
+    call here is rejected before any CUDA call."""
+    from quantized_self_speculative_gb300 import nq
+    A = 0x10000
+    pb, sb = C.c_size_t(), C.c_size_t()
+    assert L.nq_kv_cache_bytes(2, 4, 128, 64, 1000, C.byref(pb), C.byref(sb)) == nq.NQ_OK
+    assert pb.value == 2 * 4 * 1000 * 64 and sb.value == 2 * 4 * 1000 * 2 * 2      # planes of d/2, two scales a row
+    assert L.nq_kv_cache_bytes(1, 1, 96, 64, 10, None, None) == nq.NQ_ERR_SHAPE      # head_dim 64 or 128
+    assert L.nq_kv_cache_bytes(1, 1, 64, 128, 10, None, None) == nq.NQ_ERR_SHAPE     # group > head_dim
+    assert L.nq_kv_cache_bytes(0, 1, 64, 64, 10, None, None) == nq.NQ_ERR_ARG
+    # one (output, max, sum) record per (sequence, query row, query head, 256-row split)
+    assert L.nq_attn_workspace_bytes(2, 5, 8, 128, 1000) == 2 * 5 * 8 * 4 * 130 * 4
+    assert L.nq_attn_workspace_bytes(1, 1, 1, 96, 10) == 0
+    cache = nq.nq_kv_cache(1, 2, 128, 128, 512, 0, A, A, A, A, A, A)
+    need = L.nq_attn_workspace_bytes(1, 5, 4, 128, 512)
+    assert L.nq_attn_decode(C.byref(cache), A, 5, 4, A, 3, 0.1, A, A, need, None) == nq.NQ_ERR_ARG      # planes
+    assert L.nq_attn_decode(C.byref(cache), A, 5, 3, A, 2, 0.1, A, A, need, None) == nq.NQ_ERR_ARG      # heads ratio
+    assert L.nq_attn_decode(C.byref(cache), A + 4, 5, 4, A, 2, 0.1, A, A, need, None) == nq.NQ_ERR_ALIGN
+    assert L.nq_attn_decode(C.byref(cache), A, 5, 4, A, 2, 0.1, A, A, need - 4, None) == nq.NQ_ERR_WORKSPACE
+    assert L.nq_attn_decode(C.byref(cache), A, 5, 4, A, 2, 0.0, A, A, need, None) == nq.NQ_ERR_ARG      # scale
+    assert L.nq_kv_append(C.byref(cache), A, A, 0, A, None) == nq.NQ_ERR_ARG                           # n_new
+    assert L.nq_kv_append(C.byref(cache), A + 4, A, 1, A, None) == nq.NQ_ERR_ALIGN
+    odd = nq.nq_kv_cache(1, 2, 128, 128, 512, 0, A + 8, A, A, A, A, A)
+    assert L.nq_kv_append(C.byref(odd), A, A, 1, A, None) == nq.NQ_ERR_ALIGN
+    # int8 activations
+    assert L.nq_quantize_act_int8(A, 0, 64, A, A, None) == nq.NQ_ERR_ARG
+    assert L.nq_quantize_act_int8(A + 2, 1, 64, A, A, None) == nq.NQ_ERR_ALIGN
+    W = nq.nq_weights(256, 512, 128, nq.FMT_NESTED44, A, A, A)
+    ptrs = (C.c_void_p * 1)(A)
+    assert L.nq_linear_a8_batch(0, C.byref(W), ptrs, ptrs, 1, 1, ptrs, None) == nq.NQ_ERR_ARG
+    f8 = nq.nq_weights(256, 512, 0, nq.FMT_FP8E4M3_ROW, A, None, A)
+    assert L.nq_linear_a8_batch(1, C.byref(f8), ptrs, ptrs, 1, 1, ptrs, None) == nq.NQ_ERR_ARG        # nested planes only
+    i4 = nq.nq_weights(256, 512, 128, nq.FMT_INT4, A, None, A)
+    assert L.nq_linear_a8_batch(1, C.byref(i4), ptrs, ptrs, 1, 1, ptrs, None) == nq.NQ_ERR_ARG        # INT4 verify
+    bad = (C.c_void_p * 1)(A + 4)
+    assert L.nq_linear_a8_batch(1, C.byref(W), bad, ptrs, 1, 1, ptrs, None) == nq.NQ_ERR_ALIGN
+    # round bookkeeping
+    assert L.nq_embed_rows(A, 100, 12, A, 1, 1, A, None) == nq.NQ_ERR_ARG                              # d % 8
+    assert L.nq_embed_rows(A + 2, 100, 16, A, 1, 1, A, None) == nq.NQ_ERR_ALIGN
+    assert L.spec_round_commit(A, A, 0, 4, A, A, 10, A, None) == nq.NQ_ERR_ARG
+    assert L.spec_round_commit(A, A, 2, 4, A + 2, A, 10, A, None) == nq.NQ_ERR_ALIGN
