@@ -110,6 +110,24 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The same product when rows 8..15 of A are zero (a tile with at most 8
+// query vectors): only the accumulators of rows 0..7 (d[0], d[1]) are kept;
+// d[2], d[3] are neither read nor written, so they take no registers.
+template <int RR>
+__device__ __forceinline__ void mma16816_rows(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    if constexpr (RR == 2) {
+        mma16816(d, a, b0, b1);
+    } else {
+        float d2, d3;
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                     "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%10,%10};"
+                     : "+f"(d[0]), "+f"(d[1]), "=f"(d2), "=f"(d3)
+                     : "r"(a[0]), "r"(0u), "r"(a[2]), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
+        (void)d2;
+        (void)d3;
+    }
+}
 __device__ __forceinline__ uint32_t h2_pack(float lo, float hi)
 {
     uint32_t r;
@@ -130,7 +148,9 @@ __device__ __forceinline__ float ex2(float x)
 // nibbles in bits 4-7 of each half (16 (q4 + 8): one shift per two pairs
 // instead of one per pair; the other operand or the output carries the
 // 1/16); KV8 from the base and refinement words, 16 (q4 + 8) + (r + 8) =
-// q8 + 136.
+// q8 + 136: the code bytes of the even nibbles (0, 2, 4, 6) and of the odd
+// ones are formed first (one shift and one bit-select each, shared by two
+// pairs), then each pair is one mask or one byte permute.
 template <int PLANES>
 __device__ __forceinline__ uint32_t code_pair(uint32_t xb, uint32_t xr, int i)
 {
@@ -139,9 +159,11 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t xb, uint32_t xr, int i)
         const uint32_t x = i >= 2 ? xb >> 8 : xb;
         return (i & 1) ? ((x & 0x00F000F0u) ^ 0x00800080u) : ((x & 0x000F000Fu) ^ 0x00080008u);
     } else {
-        // xb, xr already have every nibble's sign bit flipped (offset binary)
-        const uint32_t hi = i == 0 ? (xb << 4) : (xb >> (4 * i - 4));
-        return (hi & 0x00F000F0u) | ((xr >> (4 * i)) & 0x000F000Fu);
+        // xb, xr already have every nibble's sign bit flipped (offset binary);
+        // byte j of x is the code of nibble 2 j + (i & 1)
+        const uint32_t x = (i & 1) ? ((xb & 0xF0F0F0F0u) | ((xr >> 4) & 0x0F0F0F0Fu))
+                                   : (((xb << 4) & 0xF0F0F0F0u) | (xr & 0x0F0F0F0Fu));
+        return i >= 2 ? __byte_perm(x, 0u, 0x4341) : (x & 0x00FF00FFu);
     }
 }
 // Scale of the codes code_pair returns for pair index i (1 or 16).
@@ -185,6 +207,11 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     constexpr int OFF = PLANES == 2 ? 136 : 8;
     constexpr float FK = PLANES == 2 ? 1048576.0f : 16777216.0f;   // 2^24 undoes the code scale; s/16 for KV8
     static_assert(NG == 1 || (NG == 2 && D == 128), "groups");
+    // rows of the tile whose accumulators are kept: the empty rows 8..15 of a
+    // one-row-block tile are dropped in the KV8 read with one group per row
+    // (measured: the KV4 read is faster with the full products; with two
+    // groups the register limit would spill)
+    constexpr int RK = PLANES == 2 && NG == 1 ? RR : 2;
     extern __shared__ __align__(128) unsigned char sm[];
     const int g8 = C.H == 0 ? 1 : Hq / C.H, nq_all = M * g8;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / qtiles, qt = blockIdx.z % qtiles;
@@ -246,15 +273,22 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     // scale log2(e) (scores in base 2), fp16, in the dimension order of the
     // K fragments; and per group the offset term of the scores
     uint32_t qa[HALVES][4][4];
-    float cinit[NG][2];
+    float cinit[NG][2] = {};
     int lim[2];
     {
         float qsum[NG][2];
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) qsum[gr][0] = qsum[gr][1] = 0.0f;
         const float qs = scale * 1.4426950408889634f;
+        if constexpr (RK == 1) {
+            lim[1] = Lb;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
+            for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) qa[h][sl][1] = qa[h][sl][3] = 0u;
+        }
+#pragma unroll
+        for (int rr = 0; rr < RK; ++rr) {
             const int v = qt * kQTile + g + 8 * rr;
             const bool valid = v < nq_all;
             const int m = valid ? v / g8 : 0, hq = kvh * g8 + (valid ? v % g8 : 0);
@@ -293,7 +327,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
+            for (int rr = 0; rr < RK; ++rr) {
                 float v = qsum[gr][rr];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -353,7 +387,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
                 for (int kt = 0; kt < 2; ++kt) {
                     const uint32_t b0 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0);
                     const uint32_t b1 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0 + 1);
-                    mma16816(acc[h][kt], qa[h][sl], b0, b1);
+                    mma16816_rows<RK>(acc[h][kt], qa[h][sl], b0, b1);
                 }
         }
         // ---- scores of rows (g, g + 8) x cache rows 4t + kk, kk = 0..3, then the
@@ -436,7 +470,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
         }
         // sum of P' per row and group through the tensor cores: B = all ones
 #pragma unroll
-        for (int gr = 0; gr < NG; ++gr) mma16816(sig[gr], pa[gr], 0x3C003C00u, 0x3C003C00u);
+        for (int gr = 0; gr < NG; ++gr) mma16816_rows<RK>(sig[gr], pa[gr], 0x3C003C00u, 0x3C003C00u);
         // ---- O += P' V: n-tile (h, i) holds dimension 64 h + 8 n + i in column n
 #pragma unroll
         for (int h = 0; h < HALVES; ++h) {
@@ -464,7 +498,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
             for (int i = 0; i < 8; ++i) {
                 const uint32_t b0 = code_pair<PLANES>(u0[i >> 2], r0[i >> 2], i & 3);
                 const uint32_t b1 = code_pair<PLANES>(u1[i >> 2], r1[i >> 2], i & 3);
-                mma16816(o[8 * h + i], pa[NG == 2 ? h : 0], b0, b1);
+                mma16816_rows<RK>(o[8 * h + i], pa[NG == 2 ? h : 0], b0, b1);
             }
         }
         __syncwarp();                           // every lane is done with this stage: refill it
@@ -477,7 +511,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     // ---- the warp's state: l summed over the four lanes of a row; the P'
     // sums (every column of sig holds its row's sum); O = 2^24 acc - off sum(P')
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
+    for (int rr = 0; rr < RR; ++rr) {
         lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 1);
         lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 2);
     }
