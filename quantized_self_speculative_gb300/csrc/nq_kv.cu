@@ -110,24 +110,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// The same product when rows 8..15 of A are zero (a tile with at most 8
-// query vectors): only the accumulators of rows 0..7 (d[0], d[1]) are kept;
-// d[2], d[3] are neither read nor written, so they take no registers.
-template <int RR>
-__device__ __forceinline__ void mma16816_rows(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    if constexpr (RR == 2) {
-        mma16816(d, a, b0, b1);
-    } else {
-        float d2, d3;
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-                     "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%10,%10};"
-                     : "+f"(d[0]), "+f"(d[1]), "=f"(d2), "=f"(d3)
-                     : "r"(a[0]), "r"(0u), "r"(a[2]), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
-        (void)d2;
-        (void)d3;
-    }
-}
 __device__ __forceinline__ uint32_t h2_pack(float lo, float hi)
 {
     uint32_t r;
@@ -207,11 +189,6 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     constexpr int OFF = PLANES == 2 ? 136 : 8;
     constexpr float FK = PLANES == 2 ? 1048576.0f : 16777216.0f;   // 2^24 undoes the code scale; s/16 for KV8
     static_assert(NG == 1 || (NG == 2 && D == 128), "groups");
-    // rows of the tile whose accumulators are kept: the empty rows 8..15 of a
-    // one-row-block tile are dropped in the KV8 read with one group per row
-    // (measured: the KV4 read is faster with the full products; with two
-    // groups the register limit would spill)
-    constexpr int RK = PLANES == 2 && NG == 1 ? RR : 2;
     extern __shared__ __align__(128) unsigned char sm[];
     const int g8 = C.H == 0 ? 1 : Hq / C.H, nq_all = M * g8;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / qtiles, qt = blockIdx.z % qtiles;
@@ -273,22 +250,15 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     // scale log2(e) (scores in base 2), fp16, in the dimension order of the
     // K fragments; and per group the offset term of the scores
     uint32_t qa[HALVES][4][4];
-    float cinit[NG][2] = {};
+    float cinit[NG][2];
     int lim[2];
     {
         float qsum[NG][2];
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) qsum[gr][0] = qsum[gr][1] = 0.0f;
         const float qs = scale * 1.4426950408889634f;
-        if constexpr (RK == 1) {
-            lim[1] = Lb;
 #pragma unroll
-            for (int h = 0; h < HALVES; ++h)
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) qa[h][sl][1] = qa[h][sl][3] = 0u;
-        }
-#pragma unroll
-        for (int rr = 0; rr < RK; ++rr) {
+        for (int rr = 0; rr < 2; ++rr) {
             const int v = qt * kQTile + g + 8 * rr;
             const bool valid = v < nq_all;
             const int m = valid ? v / g8 : 0, hq = kvh * g8 + (valid ? v % g8 : 0);
@@ -327,7 +297,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-            for (int rr = 0; rr < RK; ++rr) {
+            for (int rr = 0; rr < 2; ++rr) {
                 float v = qsum[gr][rr];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -387,7 +357,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
                 for (int kt = 0; kt < 2; ++kt) {
                     const uint32_t b0 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0);
                     const uint32_t b1 = code_pair<PLANES>(xb[kt][h][w], xr[kt][h][w], i0 + 1);
-                    mma16816_rows<RK>(acc[h][kt], qa[h][sl], b0, b1);
+                    mma16816(acc[h][kt], qa[h][sl], b0, b1);
                 }
         }
         // ---- scores of rows (g, g + 8) x cache rows 4t + kk, kk = 0..3, then the
@@ -470,7 +440,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
         }
         // sum of P' per row and group through the tensor cores: B = all ones
 #pragma unroll
-        for (int gr = 0; gr < NG; ++gr) mma16816_rows<RK>(sig[gr], pa[gr], 0x3C003C00u, 0x3C003C00u);
+        for (int gr = 0; gr < NG; ++gr) mma16816(sig[gr], pa[gr], 0x3C003C00u, 0x3C003C00u);
         // ---- O += P' V: n-tile (h, i) holds dimension 64 h + 8 n + i in column n
 #pragma unroll
         for (int h = 0; h < HALVES; ++h) {
@@ -498,7 +468,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
             for (int i = 0; i < 8; ++i) {
                 const uint32_t b0 = code_pair<PLANES>(u0[i >> 2], r0[i >> 2], i & 3);
                 const uint32_t b1 = code_pair<PLANES>(u1[i >> 2], r1[i >> 2], i & 3);
-                mma16816_rows<RK>(o[8 * h + i], pa[NG == 2 ? h : 0], b0, b1);
+                mma16816(o[8 * h + i], pa[NG == 2 ? h : 0], b0, b1);
             }
         }
         __syncwarp();                           // every lane is done with this stage: refill it
@@ -511,7 +481,7 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     // ---- the warp's state: l summed over the four lanes of a row; the P'
     // sums (every column of sig holds its row's sum); O = 2^24 acc - off sum(P')
 #pragma unroll
-    for (int rr = 0; rr < RR; ++rr) {
+    for (int rr = 0; rr < 2; ++rr) {
         lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 1);
         lrun[rr] += __shfl_xor_sync(0xffffffffu, lrun[rr], 2);
     }
@@ -557,6 +527,392 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
             }
         }
         const int v = qt * kQTile + r, m = v / g8, hq = kvh * g8 + v % g8;
+        part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
+    }
+}
+
+// ---- keys as rows, at most 8 query vectors per kv head (D = 128)
+//
+// S^T = K Q^T and O^T = V^T P'^T: the 16 cache rows of a block are the MMA's
+// M dimension and the query vectors (up to 8) its N dimension, so no MMA row
+// is empty: half the products and half the output accumulators of the
+// query-tile kernel above when that tile would hold 8 or fewer vectors.  P'
+// reaches the second product's B operand through a 256-byte shared tile per
+// group (two 32-bit stores per lane, one ldmatrix.trans).  Same partials
+// layout as the kernel above, merged by the same combine.
+constexpr int kNQ = 8;
+
+// Byte offset of (row r, byte o) of a 16-row block of 64-byte rows: 16-byte
+// chunk c = o / 16 of row r at slot (4 (r mod 2) + c) xor 2 (r / 2 mod 4) of
+// 128-byte line r / 2.  The K fragment reads (rows g and g + 8, 8 bytes at
+// 32 h + 8 t) and the V fragment reads (rows 2 t + {0, 1, 8, 9}, 4 bytes at
+// 32 h + 4 g) are then free of bank conflicts.
+__device__ __forceinline__ uint32_t swz_kt(int r, int o)
+{
+    const int line = r >> 1, slot = ((4 * (r & 1)) + (o >> 4)) ^ (2 * (line & 3));
+    return static_cast<uint32_t>((line << 7) + (slot << 4) + (o & 15));
+}
+
+template <int PLANES>
+struct AttnKtGeo {
+    static constexpr int TILE = kBlk * 64;                    // one plane of one block
+    static constexpr int STAGE = 2 * PLANES * TILE;           // K and V planes of one block
+    static constexpr int SCALES = 2 * kBlk * 2 * 2;           // K and V scales of one block (fp16, up to 2 groups)
+    static constexpr int PT = 2 * kBlk * kNQ * 2;             // P' tiles [group][cache row][query] fp16
+    static constexpr int WARP = kStages * STAGE + kMaxBlkPerWarp * SCALES + PT;
+    static constexpr int MERGE = kKvWarps * kNQ * (128 + 2) * 4;
+    static constexpr int SMEM = kKvWarps * WARP > MERGE ? kKvWarps * WARP : MERGE;
+};
+
+template <int PLANES, int NG>
+__global__ void __launch_bounds__(kKvWarps * 32, PLANES == 1 ? 4 : 3)
+attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int32_t *__restrict__ len,
+                     float scale, float *__restrict__ part, int nsplit, int nbw)
+{
+    constexpr int D = 128, RB = 64, HALVES = 2;
+    using Geo = AttnKtGeo<PLANES>;
+    constexpr int TILE = Geo::TILE;
+    constexpr int OFF = PLANES == 2 ? 136 : 8;
+    constexpr float FK = PLANES == 2 ? 1048576.0f : 16777216.0f;   // 2^24 undoes the code scale; s/16 for KV8
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int g8 = C.H == 0 ? 1 : Hq / C.H, nq_all = M * g8;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int Lb = min(len[b], C.L);
+    const int t_begin = split * kKvWarps * kBlk * nbw, t_end = min(t_begin + kKvWarps * kBlk * nbw, Lb);
+    if (t_begin >= Lb) return;                // past the sequence: the combine does not read this split
+    const size_t rowbase = (static_cast<size_t>(b) * C.H + kvh) * C.L;
+
+    // ---- this warp's blocks through a ring of kStages shared-memory stages
+    unsigned char *wsm = sm + warp * Geo::WARP;
+    const int key_w = t_begin + warp * nbw * kBlk;
+    const int nblk = t_end > key_w ? min(nbw, (t_end - key_w + kBlk - 1) / kBlk) : 0;
+    const uint8_t *planes[4] = {C.kb, C.vb, C.kr, C.vr};
+    auto issue = [&](int bi) {
+        const uint32_t st = static_cast<uint32_t>(__cvta_generic_to_shared(wsm + (bi % kStages) * Geo::STAGE));
+#pragma unroll
+        for (int pl = 0; pl < 2 * PLANES; ++pl) {
+#pragma unroll
+            for (int qq = lane; qq < TILE / 16; qq += 32) {
+                const int r = qq / (RB / 16), c = qq % (RB / 16);
+                const int key = min(key_w + bi * kBlk + r, C.L - 1);
+                const uint8_t *src = planes[pl] + (rowbase + key) * RB + 16 * c;
+                const uint32_t dst = st + pl * TILE + swz_kt(r, 16 * c);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+            }
+        }
+    };
+#pragma unroll
+    for (int bi = 0; bi < kStages; ++bi) {
+        if (bi < nblk) issue(bi);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    constexpr int PER_BLK = 2 * kBlk * NG;
+    unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + kStages * Geo::STAGE);
+    {
+        constexpr int NSC = kMaxBlkPerWarp * PER_BLK / 32;
+        unsigned short sv[NSC];
+#pragma unroll
+        for (int k = 0; k < NSC; ++k) {
+            const int e = lane + 32 * k;
+            const int bi = e / PER_BLK, rem = e % PER_BLK, which = rem / (kBlk * NG), idx = rem % (kBlk * NG);
+            const int key = min(key_w + bi * kBlk + idx / NG, C.L - 1);
+            const unsigned short *src = reinterpret_cast<const unsigned short *>(which ? C.vs : C.ks);
+            sv[k] = bi < nblk ? ld_nc_u16(src + (rowbase + key) * NG + idx % NG) : static_cast<unsigned short>(0);
+        }
+#pragma unroll
+        for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
+    }
+    unsigned char *ptile = wsm + kStages * Geo::STAGE + kMaxBlkPerWarp * Geo::SCALES;
+
+    // ---- query fragments (B operand of S^T): query vector g, scaled by
+    // scale log2(e), fp16, dimensions 64 h + 16 t .. + 15 in the order of the
+    // K fragments; the offset term of the scores for columns 2t, 2t + 1
+    uint32_t qb[HALVES][4][2];
+    float cinit[NG][2];
+    int lim[2];
+    {
+        float qsum[NG] = {};
+        const float qs = scale * 1.4426950408889634f;
+        const bool valid = g < nq_all;
+        const int m = valid ? g / g8 : 0, hq = kvh * g8 + (valid ? g % g8 : 0);
+        const float *qrow = q + ((static_cast<size_t>(b) * M + m) * Hq + hq) * D;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            float x[16];
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                float4 f = valid ? *reinterpret_cast<const float4 *>(qrow + 64 * h + 16 * t + 4 * j4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[4 * j4] = __half2float(__float2half_rn(__fmul_rn(f.x, qs)));
+                x[4 * j4 + 1] = __half2float(__float2half_rn(__fmul_rn(f.y, qs)));
+                x[4 * j4 + 2] = __half2float(__float2half_rn(__fmul_rn(f.z, qs)));
+                x[4 * j4 + 3] = __half2float(__float2half_rn(__fmul_rn(f.w, qs)));
+            }
+            float sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sum += x[j];
+            qsum[NG == 2 ? h : 0] += sum;
+            // k-step sl: word w = sl / 2 of the lane's 16 dimensions, nibbles
+            // i0, i0 + 4 (slots 2t, 2t + 1) and i0 + 1, i0 + 5 (slots 2t + 8, 2t + 9);
+            // the second pair's codes come 16 times too large at KV4: x / 16 there
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+                const int w = sl >> 1, i0 = 2 * (sl & 1);
+                constexpr float kInv = 1.0f / code_scale<PLANES>(1);
+                qb[h][sl][0] = h2_pack(x[8 * w + i0], x[8 * w + i0 + 4]);
+                qb[h][sl][1] = h2_pack(x[8 * w + i0 + 1] * kInv, x[8 * w + i0 + 5] * kInv);
+            }
+        }
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+            float v = qsum[gr];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);                 // query g's sum, in lanes 4g .. 4g + 3
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                cinit[gr][c] = -static_cast<float>(OFF) * 5.9604644775390625e-08f *
+                               __shfl_sync(0xffffffffu, v, 4 * (2 * t + c));
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int n = 2 * t + c;
+            lim[c] = n < nq_all ? Lb - (M - 1 - n / g8) : Lb;
+        }
+    }
+
+    // O^T tile (h, i): row g = dimension 64 h + 8 g + i, row g + 8 = 64 h + 8 g + 4 + i;
+    // columns 2t, 2t + 1 = queries
+    float o[HALVES * 4][4];
+#pragma unroll
+    for (int ti = 0; ti < HALVES * 4; ++ti) o[ti][0] = o[ti][1] = o[ti][2] = o[ti][3] = 0.0f;
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.0f, 0.0f}, sig[NG][4];
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) sig[gr][0] = sig[gr][1] = sig[gr][2] = sig[gr][3] = 0.0f;
+    int limw = min(t_end, min(lim[0], lim[1]));
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) limw = min(limw, __shfl_xor_sync(0xffffffffu, limw, o2));
+    const uint32_t pt_s = static_cast<uint32_t>(__cvta_generic_to_shared(ptile));
+    for (int bi = 0; bi < nblk; ++bi) {
+        asm volatile("cp.async.wait_group %0;" :: "n"(kStages - 1) : "memory");
+        __syncwarp();
+        const unsigned char *st = wsm + (bi % kStages) * Geo::STAGE;
+        const int key0 = key_w + bi * kBlk;
+        // ---- S^T: rows g, g + 8 = cache rows key0 + g, key0 + g + 8; four
+        // independent chains (half, word); the offset term enters the first
+        // chain of each group
+        float acc[HALVES][2][4];
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const bool first = w == 0 && (NG == 2 || h == 0);
+                acc[h][w][0] = acc[h][w][2] = first ? cinit[NG == 2 ? h : 0][0] : 0.0f;
+                acc[h][w][1] = acc[h][w][3] = first ? cinit[NG == 2 ? h : 0][1] : 0.0f;
+            }
+        uint32_t xb[HALVES][2][2], xr[HALVES][2][2];
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const uint2 wb = *reinterpret_cast<const uint2 *>(st + swz_kt(g + 8 * rr, 32 * h + 8 * t));
+                uint2 wr = make_uint2(0u, 0u);
+                if constexpr (PLANES == 2) wr = *reinterpret_cast<const uint2 *>(st + 2 * TILE + swz_kt(g + 8 * rr, 32 * h + 8 * t));
+                xb[h][rr][0] = PLANES == 2 ? wb.x ^ 0x88888888u : wb.x;
+                xb[h][rr][1] = PLANES == 2 ? wb.y ^ 0x88888888u : wb.y;
+                xr[h][rr][0] = wr.x ^ 0x88888888u;
+                xr[h][rr][1] = wr.y ^ 0x88888888u;
+            }
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const int w = sl >> 1, i0 = 2 * (sl & 1);
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                const uint32_t a[4] = {code_pair<PLANES>(xb[h][0][w], xr[h][0][w], i0),
+                                       code_pair<PLANES>(xb[h][1][w], xr[h][1][w], i0),
+                                       code_pair<PLANES>(xb[h][0][w], xr[h][0][w], i0 + 1),
+                                       code_pair<PLANES>(xb[h][1][w], xr[h][1][w], i0 + 1)};
+                mma16816(acc[h][w], a, qb[h][sl][0], qb[h][sl][1]);
+            }
+        }
+        // ---- scores of cache rows (g, g + 8) x queries (2t, 2t + 1), the
+        // online softmax (base 2) and P' = p times the V row's group scale,
+        // stored as [cache row][query] for the transposing load
+        float sk[2][NG], sv[2][NG];
+        {
+            const unsigned short *sc = ssm + bi * 2 * kBlk * NG;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    sk[rr][gr] = __fmul_rn(__half2float(__ushort_as_half(sc[(g + 8 * rr) * NG + gr])), FK);
+                    const float v = __half2float(__ushort_as_half(sc[kBlk * NG + (g + 8 * rr) * NG + gr]));
+                    sv[rr][gr] = PLANES == 2 ? __fmul_rn(v, 0.0625f) : v;
+                }
+        }
+        float alpha[2];
+        auto softmax_block = [&](auto mask_c) {
+            constexpr bool MASK = decltype(mask_c)::value;
+            float s[2][2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float v = 0.0f;
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        v = fmaf(sk[rr][NG == 2 ? h : 0], acc[h][0][2 * rr + c] + acc[h][1][2 * rr + c], v);
+                    if constexpr (MASK) {
+                        const int key = key0 + g + 8 * rr;
+                        v = (key < t_end && key < lim[c]) ? v : -INFINITY;
+                    }
+                    s[rr][c] = v;
+                }
+            float p[2][2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float mx = fmaxf(s[0][c], s[1][c]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(mrun[c], mx);
+                alpha[c] = mrun[c] == -INFINITY ? 0.0f : ex2(mrun[c] - mn);
+                mrun[c] = mn;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                    p[rr][c] = MASK ? (s[rr][c] == -INFINITY ? 0.0f : ex2(s[rr][c] - mn)) : ex2(s[rr][c] - mn);
+                lrun[c] = fmaf(lrun[c], alpha[c], p[0][c] + p[1][c]);
+            }
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    float pw[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)      // masked rows may hold any scale bits: keep them out
+                        pw[c] = MASK ? (p[rr][c] > 0.0f ? __fmul_rn(p[rr][c], sv[rr][gr]) : 0.0f)
+                                     : __fmul_rn(p[rr][c], sv[rr][gr]);
+                    *reinterpret_cast<uint32_t *>(ptile + gr * (kBlk * kNQ * 2) + (g + 8 * rr) * (kNQ * 2) + 4 * t) =
+                        h2_pack(pw[0], pw[1]);
+                }
+        };
+        if (key0 + kBlk <= limw) softmax_block(std::false_type{});
+        else softmax_block(std::true_type{});
+        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+            for (int ti = 0; ti < HALVES * 4; ++ti) {
+                o[ti][0] *= alpha[0]; o[ti][1] *= alpha[1];
+                o[ti][2] *= alpha[0]; o[ti][3] *= alpha[1];
+            }
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                sig[gr][0] *= alpha[0]; sig[gr][1] *= alpha[1];
+                sig[gr][2] *= alpha[0]; sig[gr][3] *= alpha[1];
+            }
+        }
+        __syncwarp();                           // P' tiles written by every lane
+        // B operand of O^T: (cache rows 2t, 2t + 1; query g) and (2t + 8, 2t + 9; g)
+        uint32_t pb[NG][2];
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+            const uint32_t addr = pt_s + gr * (kBlk * kNQ * 2) + (lane & 15) * (kNQ * 2);
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                         : "=r"(pb[gr][0]), "=r"(pb[gr][1]) : "r"(addr) : "memory");
+        }
+        // sum of P' per query and group through the tensor cores: A = all ones
+        {
+            const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) mma16816(sig[gr], ones, pb[gr][0], pb[gr][1]);
+        }
+        // ---- O^T += V^T P'^T
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            uint32_t vb[4], vr[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int row = 2 * t + (kk & 1) + 8 * (kk >> 1);
+                vb[kk] = *reinterpret_cast<const uint32_t *>(st + TILE + swz_kt(row, 32 * h + 4 * g));
+                if constexpr (PLANES == 2) {
+                    vr[kk] = *reinterpret_cast<const uint32_t *>(st + 3 * TILE + swz_kt(row, 32 * h + 4 * g)) ^ 0x88888888u;
+                    vb[kk] ^= 0x88888888u;
+                } else {
+                    vr[kk] = 0u;
+                }
+            }
+            // byte-interleave cache rows (2t, 2t + 1) and (2t + 8, 2t + 9): nibble i
+            // of the first row of a pair lands at bit 4 i, of the second at 16 + 4 i
+            const uint32_t u0[2] = {__byte_perm(vb[0], vb[1], 0x5410), __byte_perm(vb[0], vb[1], 0x7632)};
+            const uint32_t u1[2] = {__byte_perm(vb[2], vb[3], 0x5410), __byte_perm(vb[2], vb[3], 0x7632)};
+            uint32_t r0[2] = {0u, 0u}, r1[2] = {0u, 0u};
+            if constexpr (PLANES == 2) {
+                r0[0] = __byte_perm(vr[0], vr[1], 0x5410); r0[1] = __byte_perm(vr[0], vr[1], 0x7632);
+                r1[0] = __byte_perm(vr[2], vr[3], 0x5410); r1[1] = __byte_perm(vr[2], vr[3], 0x7632);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a[4] = {code_pair<PLANES>(u0[0], r0[0], i), code_pair<PLANES>(u0[1], r0[1], i),
+                                       code_pair<PLANES>(u1[0], r1[0], i), code_pair<PLANES>(u1[1], r1[1], i)};
+                mma16816(o[4 * h + i], a, pb[NG == 2 ? h : 0][0], pb[NG == 2 ? h : 0][1]);
+            }
+        }
+        __syncwarp();                           // every lane is done with this stage and the P' tiles
+        if (bi + kStages < nblk) issue(bi + kStages);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+    // ---- the warp's state: l summed over the eight lanes of a query; O =
+    // 2^24 acc - off sum(P') (every row of sig holds its query's sum)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        lrun[c] += __shfl_xor_sync(0xffffffffu, lrun[c], 4);
+        lrun[c] += __shfl_xor_sync(0xffffffffu, lrun[c], 8);
+        lrun[c] += __shfl_xor_sync(0xffffffffu, lrun[c], 16);
+    }
+    __syncthreads();                           // every warp is done with its stages
+    float *red_m = reinterpret_cast<float *>(sm);                 // [warp][query]
+    float *red_l = red_m + kKvWarps * kNQ;                        // [warp][query]
+    float *red_o = red_l + kKvWarps * kNQ;                        // [warp][query][D]
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int n = 2 * t + c;
+        if (g == 0) {
+            red_m[warp * kNQ + n] = mrun[c];
+            red_l[warp * kNQ + n] = lrun[c];
+        }
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int dim = 64 * h + 8 * g + 4 * rr + i;
+                    const float val = fmaf(16777216.0f / code_scale<PLANES>(i), o[4 * h + i][2 * rr + c],
+                                           -static_cast<float>(OFF) * sig[NG == 2 ? h : 0][c]);
+                    red_o[(warp * kNQ + n) * D + dim] = val;
+                }
+    }
+    __syncthreads();
+    const int nqv = min(kNQ, nq_all);
+    for (int i = threadIdx.x; i < nqv * (D + 2); i += kKvWarps * 32) {
+        const int r = i / (D + 2), j = i % (D + 2);
+        float M2 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w * kNQ + r]);
+        float val = 0.0f;
+        if (j == D) {
+            val = M2;
+        } else {
+#pragma unroll
+            for (int w = 0; w < kKvWarps; ++w) {
+                const float mw = red_m[w * kNQ + r];
+                const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M2);
+                val = fmaf(f, j == D + 1 ? red_l[w * kNQ + r] : red_o[(w * kNQ + r) * D + j], val);
+            }
+        }
+        const int m = r / g8, hq = kvh * g8 + r % g8;
         part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
     }
 }
@@ -663,15 +1019,42 @@ cudaError_t launch_attn_r(int rr, dim3 grid, cudaStream_t s, Cache C, const floa
     return rr == 1 ? launch_attn_t<PLANES, D, NG, 1>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
                    : launch_attn_t<PLANES, D, NG, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
 }
+template <int PLANES, int NG>
+cudaError_t launch_attn_kt(dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq, const int32_t *len,
+                           float scale, float *part, int nsplit, int nbw)
+{
+    constexpr int smem = AttnKtGeo<PLANES>::SMEM;
+    static std::atomic<bool> done[64];          // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev].load()) {
+        e = cudaFuncSetAttribute(attn_split_kt_kernel<PLANES, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        done[dev].store(true);
+    }
+    attn_split_kt_kernel<PLANES, NG><<<grid, kKvWarps * 32, smem, s>>>(C, q, M, Hq, len, scale, part, nsplit, nbw);
+    return cudaGetLastError();
+}
+// D = 128 with at most 8 query vectors per kv head: keys as rows; otherwise
+// the query-tile kernel
 cudaError_t launch_attn(int planes, int d, int ng, int rr, dim3 grid, cudaStream_t s, Cache C, const float *q, int M,
                         int Hq, const int32_t *len, float scale, float *part, int nsplit, int qtiles, int nbw)
 {
     if (d == 128) {
+        if (rr == 1) {
+            if (ng == 2)
+                return planes == 1 ? launch_attn_kt<1, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, nbw)
+                                   : launch_attn_kt<2, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, nbw);
+            return planes == 1 ? launch_attn_kt<1, 1>(grid, s, C, q, M, Hq, len, scale, part, nsplit, nbw)
+                               : launch_attn_kt<2, 1>(grid, s, C, q, M, Hq, len, scale, part, nsplit, nbw);
+        }
         if (ng == 2)
-            return planes == 1 ? launch_attn_r<1, 128, 2>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
-                               : launch_attn_r<2, 128, 2>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
-        return planes == 1 ? launch_attn_r<1, 128, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
-                           : launch_attn_r<2, 128, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
+            return planes == 1 ? launch_attn_t<1, 128, 2, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                               : launch_attn_t<2, 128, 2, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
+        return planes == 1 ? launch_attn_t<1, 128, 1, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
+                           : launch_attn_t<2, 128, 1, 2>(grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);
     }
     return planes == 1 ? launch_attn_r<1, 64, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw)
                        : launch_attn_r<2, 64, 1>(rr, grid, s, C, q, M, Hq, len, scale, part, nsplit, qtiles, nbw);

@@ -57,6 +57,9 @@ def test_append_matches_oracle_pack(nq, d, G):
     (1, 4, 4, 128, 128, 5, [700]),            # MHA verify over k + 1 = 5 positions
     (3, 8, 2, 64, 64, 9, [257, 40, 1000]),    # GQA (4 query heads per kv head), batch of unequal lengths
     (2, 28, 4, 128, 128, 3, [513, 600]),      # Qwen2.5-7B head layout
+    (2, 28, 4, 128, 128, 1, [513, 600]),      # its draft step: 7 query vectors per kv head (keys-as-rows kernel)
+    (1, 8, 2, 128, 64, 2, [333]),             # two groups per row, exactly 8 query vectors per kv head
+    (1, 8, 2, 128, 64, 3, [450]),             # two groups per row, 12 query vectors per kv head (query tiles)
 ])
 @pytest.mark.parametrize("planes", [1, 2])
 def test_attention_matches_oracle(nq, B, Hq, Hkv, d, G, M, lens, planes):
