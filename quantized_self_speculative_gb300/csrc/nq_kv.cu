@@ -553,25 +553,30 @@ __device__ __forceinline__ uint32_t swz_kt(int r, int o)
     return static_cast<uint32_t>((line << 7) + (slot << 4) + (o & 15));
 }
 
-template <int PLANES>
+// Four CTAs per SM: the KV8 read keeps three stages (the same bytes in
+// flight per SM as four stages at three CTAs) and its one-group form fits
+// 4 x (54 KB + 1 KB) in the SM's 228 KB; the two-group KV8 form stays at three.
+template <int PLANES, int NG>
 struct AttnKtGeo {
+    static constexpr int STAGES = PLANES == 2 ? 3 : kStages;
+    static constexpr int CTAS = PLANES == 2 && NG == 2 ? 3 : 4;
     static constexpr int TILE = kBlk * 64;                    // one plane of one block
     static constexpr int STAGE = 2 * PLANES * TILE;           // K and V planes of one block
-    static constexpr int SCALES = 2 * kBlk * 2 * 2;           // K and V scales of one block (fp16, up to 2 groups)
-    static constexpr int PT = 2 * kBlk * kNQ * 2;             // P' tiles [group][cache row][query] fp16
-    static constexpr int WARP = kStages * STAGE + kMaxBlkPerWarp * SCALES + PT;
+    static constexpr int SCALES = 2 * kBlk * NG * 2;          // K and V scales of one block (fp16)
+    static constexpr int PT = NG * kBlk * kNQ * 2;            // P' tiles [group][cache row][query] fp16
+    static constexpr int WARP = STAGES * STAGE + kMaxBlkPerWarp * SCALES + PT;
     static constexpr int MERGE = kKvWarps * kNQ * (128 + 2) * 4;
     static constexpr int SMEM = kKvWarps * WARP > MERGE ? kKvWarps * WARP : MERGE;
 };
 
 template <int PLANES, int NG>
-__global__ void __launch_bounds__(kKvWarps * 32, PLANES == 1 ? 4 : 3)
+__global__ void __launch_bounds__(kKvWarps * 32, AttnKtGeo<PLANES, NG>::CTAS)
 attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int32_t *__restrict__ len,
                      float scale, float *__restrict__ part, int nsplit, int nbw)
 {
     constexpr int D = 128, RB = 64, HALVES = 2;
-    using Geo = AttnKtGeo<PLANES>;
-    constexpr int TILE = Geo::TILE;
+    using Geo = AttnKtGeo<PLANES, NG>;
+    constexpr int TILE = Geo::TILE, STG = Geo::STAGES;
     constexpr int OFF = PLANES == 2 ? 136 : 8;
     constexpr float FK = PLANES == 2 ? 1048576.0f : 16777216.0f;   // 2^24 undoes the code scale; s/16 for KV8
     extern __shared__ __align__(128) unsigned char sm[];
@@ -584,13 +589,13 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
     if (t_begin >= Lb) return;                // past the sequence: the combine does not read this split
     const size_t rowbase = (static_cast<size_t>(b) * C.H + kvh) * C.L;
 
-    // ---- this warp's blocks through a ring of kStages shared-memory stages
+    // ---- this warp's blocks through a ring of STG shared-memory stages
     unsigned char *wsm = sm + warp * Geo::WARP;
     const int key_w = t_begin + warp * nbw * kBlk;
     const int nblk = t_end > key_w ? min(nbw, (t_end - key_w + kBlk - 1) / kBlk) : 0;
     const uint8_t *planes[4] = {C.kb, C.vb, C.kr, C.vr};
     auto issue = [&](int bi) {
-        const uint32_t st = static_cast<uint32_t>(__cvta_generic_to_shared(wsm + (bi % kStages) * Geo::STAGE));
+        const uint32_t st = static_cast<uint32_t>(__cvta_generic_to_shared(wsm + (bi % STG) * Geo::STAGE));
 #pragma unroll
         for (int pl = 0; pl < 2 * PLANES; ++pl) {
 #pragma unroll
@@ -604,12 +609,12 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
         }
     };
 #pragma unroll
-    for (int bi = 0; bi < kStages; ++bi) {
+    for (int bi = 0; bi < STG; ++bi) {
         if (bi < nblk) issue(bi);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     constexpr int PER_BLK = 2 * kBlk * NG;
-    unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + kStages * Geo::STAGE);
+    unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + STG * Geo::STAGE);
     {
         constexpr int NSC = kMaxBlkPerWarp * PER_BLK / 32;
         unsigned short sv[NSC];
@@ -624,7 +629,7 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
 #pragma unroll
         for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
     }
-    unsigned char *ptile = wsm + kStages * Geo::STAGE + kMaxBlkPerWarp * Geo::SCALES;
+    unsigned char *ptile = wsm + STG * Geo::STAGE + kMaxBlkPerWarp * Geo::SCALES;
 
     // ---- query fragments (B operand of S^T): query vector g, scaled by
     // scale log2(e), fp16, dimensions 64 h + 16 t .. + 15 in the order of the
@@ -695,9 +700,9 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
     for (int o2 = 1; o2 < 32; o2 <<= 1) limw = min(limw, __shfl_xor_sync(0xffffffffu, limw, o2));
     const uint32_t pt_s = static_cast<uint32_t>(__cvta_generic_to_shared(ptile));
     for (int bi = 0; bi < nblk; ++bi) {
-        asm volatile("cp.async.wait_group %0;" :: "n"(kStages - 1) : "memory");
+        asm volatile("cp.async.wait_group %0;" :: "n"(STG - 1) : "memory");
         __syncwarp();
-        const unsigned char *st = wsm + (bi % kStages) * Geo::STAGE;
+        const unsigned char *st = wsm + (bi % STG) * Geo::STAGE;
         const int key0 = key_w + bi * kBlk;
         // ---- S^T: rows g, g + 8 = cache rows key0 + g, key0 + g + 8; four
         // independent chains (half, word); the offset term enters the first
@@ -858,7 +863,7 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
             }
         }
         __syncwarp();                           // every lane is done with this stage and the P' tiles
-        if (bi + kStages < nblk) issue(bi + kStages);
+        if (bi + STG < nblk) issue(bi + STG);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -1023,7 +1028,7 @@ template <int PLANES, int NG>
 cudaError_t launch_attn_kt(dim3 grid, cudaStream_t s, Cache C, const float *q, int M, int Hq, const int32_t *len,
                            float scale, float *part, int nsplit, int nbw)
 {
-    constexpr int smem = AttnKtGeo<PLANES>::SMEM;
+    constexpr int smem = AttnKtGeo<PLANES, NG>::SMEM;
     static std::atomic<bool> done[64];          // per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
