@@ -116,3 +116,26 @@ def test_draft_view_differs_from_target_view_and_suffix_discard(nq):
     ref = ref_cache.attention(q, torch.tensor([402], dtype=torch.int32, device="cuda"), 2, 0.1)
     assert torch.equal(short, ref)
     assert nq.device_status() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,kv_sel", [(32, 32, [0, 9, 22, 31]), (28, 4, [0, 3])])
+def test_attention_32k_bench_workload_sampled_heads(nq, Hq, Hkv, kv_sel):
+    """The benchmark's attention workload at full size: one sequence of 32768
+    cached rows in a cache of 32768 + 16, d = 128, G = 128, LLaMA-2-7B-32K
+    (MHA) and Qwen2.5-7B (GQA) heads; the draft read of the KV4 view at M = 1
+    and the verify read of the KV8 view at M = k + 1 = 5, through the same
+    entry point and split rule.  The oracle recomputes every query head of a
+    few kv heads (the heads are independent)."""
+    B, d, G, ctx = 1, 128, 128, 32768
+    cache, _, _ = fill(nq, B, Hkv, d, G, ctx + 16, [ctx], 6000 + Hkv)
+    sub = {n: np.ascontiguousarray(a[:, kv_sel]) for n, a in cache.host_dict().items()}
+    g = Hq // Hkv
+    q_sel = [kv * g + j for kv in kv_sel for j in range(g)]
+    ln = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+    for M, planes in ((1, 1), (5, 2)):
+        q = rows(6100 + 10 * M + Hkv, B, M, Hq, d)
+        out = cache.attention(torch.from_numpy(q).cuda(), ln, planes, d ** -0.5).cpu().numpy()[:, :, q_sel]
+        ref = O.attn_decode(np.ascontiguousarray(q[:, :, q_sel]), sub, np.array([ctx], np.int32), planes, d ** -0.5)
+        err = max(normwise_err(out[0, m, i][None], ref[0, m, i][None]) for m in range(M) for i in range(len(q_sel)))
+        assert err <= TOL, (M, planes, err)
+    assert nq.device_status() == 0
