@@ -174,6 +174,57 @@ struct AttnGeo {
     static constexpr int SMEM = kKvWarps * WARP > MERGE ? kKvWarps * WARP : MERGE;
 };
 
+// Scales of a warp's blocks into its shared-memory slice, [block][K / V][row]
+// [group] fp16: every load first, then the stores (one exposed latency, not
+// one per load); rows past the warp's blocks are not read.
+template <int NG>
+__device__ __forceinline__ void stage_scales(unsigned short *ssm, const Cache &C, size_t rowbase, int key_w, int nblk,
+                                             int lane)
+{
+    constexpr int PER_BLK = 2 * kBlk * NG, NSC = kMaxBlkPerWarp * PER_BLK / 32;
+    unsigned short sv[NSC];
+#pragma unroll
+    for (int k = 0; k < NSC; ++k) {
+        const int e = lane + 32 * k;
+        const int bi = e / PER_BLK, rem = e % PER_BLK, which = rem / (kBlk * NG), idx = rem % (kBlk * NG);
+        const int key = min(key_w + bi * kBlk + idx / NG, C.L - 1);
+        const unsigned short *src = reinterpret_cast<const unsigned short *>(which ? C.vs : C.ks);
+        sv[k] = bi < nblk ? ld_nc_u16(src + (rowbase + key) * NG + idx % NG) : static_cast<unsigned short>(0);
+    }
+#pragma unroll
+    for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
+}
+
+// The CTA's partials of query vectors v0 .. v0 + nqv - 1: the four warps'
+// states (red_m, red_l: [warp][row]; red_o: [warp][row][D], NQT rows per
+// warp) merged to one running maximum M2, sum and output per vector, stored
+// as part[b][m][hq][split][D + 2] = (o[0..D-1], M2, l).
+template <int D, int NQT>
+__device__ __forceinline__ void store_partials(const float *red_m, const float *red_l, const float *red_o, int nqv,
+                                               int v0, int g8, int kvh, int b, int M, int Hq, int nsplit, int split,
+                                               float *__restrict__ part)
+{
+    for (int i = threadIdx.x; i < nqv * (D + 2); i += kKvWarps * 32) {
+        const int r = i / (D + 2), j = i % (D + 2);
+        float M2 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w * NQT + r]);
+        float val = 0.0f;
+        if (j == D) {
+            val = M2;
+        } else {
+#pragma unroll
+            for (int w = 0; w < kKvWarps; ++w) {
+                const float mw = red_m[w * NQT + r];
+                const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M2);
+                val = fmaf(f, j == D + 1 ? red_l[w * NQT + r] : red_o[(w * NQT + r) * D + j], val);
+            }
+        }
+        const int v = v0 + r, m = v / g8, hq = kvh * g8 + v % g8;
+        part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
+    }
+}
+
 // Partial attention of one split of cache rows for one tile of 16 query
 // vectors.  Query vector v = 16 z' + r (z' the tile index) = (query row m,
 // query head hq) with m = v / g, hq = kvh g + v % g.  NG = D / G groups per
@@ -200,7 +251,6 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
     const int t_begin = split * kKvWarps * kBlk * nbw, t_end = min(t_begin + kKvWarps * kBlk * nbw, Lb);
     if (t_begin >= Lb) return;                // past the sequence: the combine does not read this split
     const size_t rowbase = (static_cast<size_t>(b) * C.H + kvh) * C.L;
-    const int gpr = D / C.G;
 
     // ---- this warp's blocks: K and V planes through a ring of kStages
     // shared-memory stages (cp.async), all of its scales up front (by lanes)
@@ -227,24 +277,8 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
         if (bi < nblk) issue(bi);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    // scales: [block][K / V][row][group] fp16
-    constexpr int PER_BLK = 2 * kBlk * NG;
     unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + kStages * Geo::STAGE);
-    {
-        // every load first, then the stores (one exposed latency, not one per load)
-        constexpr int NSC = kMaxBlkPerWarp * PER_BLK / 32;
-        unsigned short sv[NSC];
-#pragma unroll
-        for (int k = 0; k < NSC; ++k) {
-            const int e = lane + 32 * k;
-            const int bi = e / PER_BLK, rem = e % PER_BLK, which = rem / (kBlk * NG), idx = rem % (kBlk * NG);
-            const int key = min(key_w + bi * kBlk + idx / NG, C.L - 1);
-            const unsigned short *src = reinterpret_cast<const unsigned short *>(which ? C.vs : C.ks);
-            sv[k] = bi < nblk ? ld_nc_u16(src + (rowbase + key) * gpr + idx % NG) : static_cast<unsigned short>(0);
-        }
-#pragma unroll
-        for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
-    }
+    stage_scales<NG>(ssm, C, rowbase, key_w, nblk, lane);
 
     // ---- query fragments (A operand): rows g and g + 8 of the tile, scaled by
     // scale log2(e) (scores in base 2), fp16, in the dimension order of the
@@ -509,26 +543,8 @@ attn_split_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const int
                 }
     }
     __syncthreads();
-    const int nqv = min(kQTile, nq_all - qt * kQTile);
-    for (int i = threadIdx.x; i < nqv * (D + 2); i += kKvWarps * 32) {
-        const int r = i / (D + 2), j = i % (D + 2);
-        float M2 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w * kQTile + r]);
-        float val = 0.0f;
-        if (j == D) {
-            val = M2;
-        } else {
-#pragma unroll
-            for (int w = 0; w < kKvWarps; ++w) {
-                const float mw = red_m[w * kQTile + r];
-                const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M2);
-                val = fmaf(f, j == D + 1 ? red_l[w * kQTile + r] : red_o[(w * kQTile + r) * D + j], val);
-            }
-        }
-        const int v = qt * kQTile + r, m = v / g8, hq = kvh * g8 + v % g8;
-        part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
-    }
+    store_partials<D, kQTile>(red_m, red_l, red_o, min(kQTile, nq_all - qt * kQTile), qt * kQTile, g8, kvh, b, M, Hq,
+                              nsplit, split, part);
 }
 
 // ---- keys as rows, at most 8 query vectors per kv head (D = 128)
@@ -613,22 +629,8 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
         if (bi < nblk) issue(bi);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    constexpr int PER_BLK = 2 * kBlk * NG;
     unsigned short *ssm = reinterpret_cast<unsigned short *>(wsm + STG * Geo::STAGE);
-    {
-        constexpr int NSC = kMaxBlkPerWarp * PER_BLK / 32;
-        unsigned short sv[NSC];
-#pragma unroll
-        for (int k = 0; k < NSC; ++k) {
-            const int e = lane + 32 * k;
-            const int bi = e / PER_BLK, rem = e % PER_BLK, which = rem / (kBlk * NG), idx = rem % (kBlk * NG);
-            const int key = min(key_w + bi * kBlk + idx / NG, C.L - 1);
-            const unsigned short *src = reinterpret_cast<const unsigned short *>(which ? C.vs : C.ks);
-            sv[k] = bi < nblk ? ld_nc_u16(src + (rowbase + key) * NG + idx % NG) : static_cast<unsigned short>(0);
-        }
-#pragma unroll
-        for (int k = 0; k < NSC; ++k) ssm[lane + 32 * k] = sv[k];
-    }
+    stage_scales<NG>(ssm, C, rowbase, key_w, nblk, lane);
     unsigned char *ptile = wsm + STG * Geo::STAGE + kMaxBlkPerWarp * Geo::SCALES;
 
     // ---- query fragments (B operand of S^T): query vector g, scaled by
@@ -900,26 +902,7 @@ attn_split_kt_kernel(Cache C, const float *__restrict__ q, int M, int Hq, const 
                 }
     }
     __syncthreads();
-    const int nqv = min(kNQ, nq_all);
-    for (int i = threadIdx.x; i < nqv * (D + 2); i += kKvWarps * 32) {
-        const int r = i / (D + 2), j = i % (D + 2);
-        float M2 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kKvWarps; ++w) M2 = fmaxf(M2, red_m[w * kNQ + r]);
-        float val = 0.0f;
-        if (j == D) {
-            val = M2;
-        } else {
-#pragma unroll
-            for (int w = 0; w < kKvWarps; ++w) {
-                const float mw = red_m[w * kNQ + r];
-                const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M2);
-                val = fmaf(f, j == D + 1 ? red_l[w * kNQ + r] : red_o[(w * kNQ + r) * D + j], val);
-            }
-        }
-        const int m = r / g8, hq = kvh * g8 + r % g8;
-        part[((((static_cast<size_t>(b) * M + m) * Hq + hq) * nsplit) + split) * (D + 2) + j] = val;
-    }
+    store_partials<D, kNQ>(red_m, red_l, red_o, min(kNQ, nq_all), 0, g8, kvh, b, M, Hq, nsplit, split, part);
 }
 
 // out[b][m][hq][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the
