@@ -571,7 +571,7 @@ __device__ __forceinline__ uint32_t swz_kt(int r, int o)
 
 // Four CTAs per SM: the KV8 read keeps three stages (the same bytes in
 // flight per SM as four stages at three CTAs) and its one-group form fits
-// 4 x (54 KB + 1 KB) in the SM's 228 KB; the two-group KV8 form stays at three.
+// 4 x (53 KB + 1 KB reserved) in the SM's 228 KB; the two-group KV8 form stays at three.
 template <int PLANES, int NG>
 struct AttnKtGeo {
     static constexpr int STAGES = PLANES == 2 ? 3 : kStages;
